@@ -1,0 +1,424 @@
+// C ABI of the packed double-binary matmul library: argument checks,
+// workspace sizing, kernel-path choice and launches.  No call allocates
+// device memory; all scratch lives in the caller's workspace.
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// Device status word, one per device the library runs on.
+__device__ int g_dbf_status;
+
+constexpr int kMaxDevices = 64;
+constexpr int kDecodeMaxTokens = 16;
+constexpr size_t kAlign = 256;
+
+thread_local char g_last_error[256] = "";
+
+int cuda_fail(cudaError_t e, const char *where) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+    return DBF_ERR_CUDA;
+}
+
+int current_device() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
+}
+
+int *status_ptr() {
+    static int *ptrs[kMaxDevices] = {nullptr};
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dbf_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int *>(p);
+    }
+    return ptrs[dev];
+}
+
+int num_sms() {
+    static int sms[kMaxDevices] = {0};
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 148;
+    if (!sms[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms[dev] = v > 0 ? v : 148;
+    }
+    return sms[dev];
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+// V row length in halves: round_up(R, 64) keeps every row 128-byte aligned
+// and covers the K extent of both paths.
+inline int64_t v_ld(int64_t R) { return round_up(R, 64); }
+inline int64_t xs_ld(int64_t M) { return round_up(M, 64); }
+
+int check_dims(int64_t N, int64_t M, int64_t R, int64_t ell) {
+    if (N < 1 || M < 1 || R < 1) return DBF_ERR_INVALID_ARG;
+    if (ell < 1 || ell > 4) return DBF_ERR_INVALID_ARG;
+    if (N > (1 << 24) || M > (1 << 24) || R > (1 << 20)) return DBF_ERR_UNSUPPORTED;
+    return DBF_OK;
+}
+
+int check_factors(const dbf_factors *f) {
+    if (!f) return DBF_ERR_INVALID_ARG;
+    int rc = check_dims(f->N, f->M, f->R, f->ell);
+    if (rc) return rc;
+    if (!f->B1 || !f->B2 || !f->alpha || !f->beta || !f->gamma) return DBF_ERR_INVALID_ARG;
+    if (f->ldw1 < ceil_div(f->R, 32) || f->ldw2 < ceil_div(f->M, 32)) return DBF_ERR_INVALID_ARG;
+    if (!aligned16(f->B1) || !aligned16(f->B2) || !aligned16(f->alpha) || !aligned16(f->beta) ||
+        !aligned16(f->gamma))
+        return DBF_ERR_ALIGNMENT;
+    return DBF_OK;
+}
+
+int resolve_path(int path, int64_t T) {
+    if (path == DBF_PATH_AUTO) return T <= kDecodeMaxTokens ? DBF_PATH_DECODE : DBF_PATH_PREFILL;
+    return path;
+}
+
+size_t ws_decode(int64_t N, int64_t M, int64_t R, int64_t ell, int64_t T) {
+    (void)N;
+    (void)M;
+    return align_up(size_t(ell * T) * v_ld(R) * 2);
+}
+
+size_t ws_prefill(int64_t N, int64_t M, int64_t R, int64_t ell, int64_t T) {
+    (void)N;
+    return align_up(size_t(ell * T) * xs_ld(M) * 2) + align_up(size_t(ell * T) * v_ld(R) * 2);
+}
+
+size_t ws_for(const dbf_factors *f, int64_t T, int path) {
+    path = resolve_path(path, T);
+    if (path == DBF_PATH_DECODE) return ws_decode(f->N, f->M, f->R, f->ell, T);
+    return ws_prefill(f->N, f->M, f->R, f->ell, T);
+}
+
+// decode path: stage 1 (x -> V), stage 2 (V -> y)
+int run_decode(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *ws,
+               cudaStream_t stream) {
+    using namespace dbfk;
+    const int ell = f->ell;
+    const int64_t cols = std::min<int64_t>(ell * T, 64);
+    DecArgs a = {};
+    a.ell = ell;
+    a.T = static_cast<int>(T);
+    a.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    a.ldx = f->M;
+    a.gamma = reinterpret_cast<const __half *>(f->gamma);
+    a.beta = reinterpret_cast<const __half *>(f->beta);
+    a.alpha = reinterpret_cast<const __half *>(f->alpha);
+    a.V = static_cast<__half *>(ws);
+    a.ldv = static_cast<int>(v_ld(f->R));
+    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    a.ldy = f->N;
+    a.accumulate = accumulate;
+    a.status = status_ptr();
+
+    // stage 1: rows of B2, K = M
+    DecArgs a1 = a;
+    a1.bits = f->B2;
+    a1.ldw = f->ldw2;
+    a1.rows = f->R;
+    a1.rows_cover = static_cast<int>(round_up(f->R, 32));
+    a1.K = f->M;
+    a1.Kw = static_cast<int>(ceil_div(f->M, 32));
+    DecPlan p1 = plan_decode_stage(a1.rows_cover, a1.Kw, static_cast<int>(cols), 8, num_sms());
+    a1.RB = p1.RB;
+    a1.KS = p1.KS;
+    a1.Wc = p1.Wc;
+    // stage 2: rows of B1, K = R
+    DecArgs a2 = a;
+    a2.bits = f->B1;
+    a2.ldw = f->ldw1;
+    a2.rows = f->N;
+    a2.rows_cover = f->N;
+    a2.K = f->R;
+    a2.Kw = static_cast<int>(ceil_div(f->R, 32));
+    DecPlan p2 = plan_decode_stage(a2.rows_cover, a2.Kw, static_cast<int>(cols), p1.CT, num_sms());
+    p2.CT = p1.CT;  // both stages use the same column chunking
+    a2.RB = p2.RB;
+    a2.KS = p2.KS;
+    a2.Wc = p2.Wc;
+    if (p1.CT == 0 || p2.CT == 0) return DBF_ERR_UNSUPPORTED;
+    cudaError_t e = launch_decode_stage(1, false, p1, a1, 1, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "decode stage 1");
+    e = launch_decode_stage(2, false, p2, a2, 1, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "decode stage 2");
+    return DBF_OK;
+}
+
+int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *ws,
+                cudaStream_t stream) {
+    using namespace dbfk;
+    const int ell = f->ell;
+    const int64_t C = ell * T;
+    if (C > (int64_t(1) << 30)) return DBF_ERR_UNSUPPORTED;
+    const int ldxs = static_cast<int>(xs_ld(f->M));
+    const int ldv = static_cast<int>(v_ld(f->R));
+    __half *xs = static_cast<__half *>(ws);
+    __half *V = reinterpret_cast<__half *>(static_cast<char *>(ws) + align_up(size_t(C) * ldxs * 2));
+    const int bn = prefill_bn(ell);
+
+    cudaError_t e = launch_prefill_prologue(reinterpret_cast<const __nv_bfloat16 *>(x), static_cast<int>(T), f->M,
+                                            f->M, reinterpret_cast<const __half *>(f->gamma), ell, xs, ldxs, stream,
+                                            true);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill prologue");
+
+    CUtensorMap map1, map2;
+    if (!encode_act_map(&map1, xs, static_cast<int>(C), ldxs, ldxs, bn) ||
+        !encode_act_map(&map2, V, static_cast<int>(C), ldv, ldv, bn)) {
+        snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
+        return DBF_ERR_CUDA;
+    }
+    PfArgs a = {};
+    a.ell = ell;
+    a.C = static_cast<int>(C);
+    a.V = V;
+    a.ldv = ldv;
+    a.beta = reinterpret_cast<const __half *>(f->beta);
+    a.alpha = reinterpret_cast<const __half *>(f->alpha);
+    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    a.ldy = f->N;
+    a.accumulate = accumulate;
+    a.status = status_ptr();
+
+    PfArgs a1 = a;
+    a1.bits = f->B2;
+    a1.ldw = f->ldw2;
+    a1.rows = f->R;
+    a1.rows_store = ldv;
+    a1.Kw = static_cast<int>(ceil_div(f->M, 32));
+    a1.nk = static_cast<int>(ceil_div(f->M, 64));
+    e = launch_prefill_gemm(1, map1, a1, bn, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill gemm 1");
+
+    PfArgs a2 = a;
+    a2.bits = f->B1;
+    a2.ldw = f->ldw1;
+    a2.rows = f->N;
+    a2.rows_store = f->N;
+    a2.Kw = static_cast<int>(ceil_div(f->R, 32));
+    a2.nk = static_cast<int>(ceil_div(f->R, 64));
+    e = launch_prefill_gemm(2, map2, a2, bn, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill gemm 2");
+    return DBF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dbf_status_string(int code) {
+    switch (code) {
+        case DBF_OK: return "ok";
+        case DBF_ERR_INVALID_ARG: return "invalid argument";
+        case DBF_ERR_ALIGNMENT: return "pointer not aligned as required";
+        case DBF_ERR_UNSUPPORTED: return "shape not supported";
+        case DBF_ERR_WORKSPACE: return "workspace missing or too small";
+        case DBF_ERR_CUDA: return "CUDA error";
+        case DBF_ERR_TIMEOUT: return "device wait timed out";
+        case DBF_ERR_DEVICE_ARG: return "device-side argument out of range";
+        default: return "unknown status";
+    }
+}
+
+const char *dbf_last_cuda_error(void) { return g_last_error; }
+
+int dbf_decode_max_tokens(void) { return kDecodeMaxTokens; }
+
+int dbf_pack(const int8_t *signs, int64_t rows, int64_t cols, uint32_t *words, int64_t ldw, void *stream) {
+    if (rows < 0 || cols < 0) return DBF_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return DBF_OK;
+    if (!signs || !words) return DBF_ERR_INVALID_ARG;
+    if (ldw < ceil_div(cols, 32)) return DBF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(words) & 3) != 0) return DBF_ERR_ALIGNMENT;
+    cudaError_t e = dbfk::launch_pack(signs, rows, cols, words, ldw, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "dbf_pack");
+}
+
+int dbf_unpack(const uint32_t *words, int64_t rows, int64_t cols, int64_t ldw, int8_t *signs, void *stream) {
+    if (rows < 0 || cols < 0) return DBF_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return DBF_OK;
+    if (!signs || !words) return DBF_ERR_INVALID_ARG;
+    if (ldw < ceil_div(cols, 32)) return DBF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(words) & 3) != 0) return DBF_ERR_ALIGNMENT;
+    cudaError_t e = dbfk::launch_unpack(words, rows, cols, ldw, signs, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "dbf_unpack");
+}
+
+size_t dbf_workspace_bytes_path(const dbf_factors *f, int64_t T, int path) {
+    if (check_factors(f) != DBF_OK || T < 0) return 0;
+    if (path < DBF_PATH_AUTO || path > DBF_PATH_PREFILL) return 0;
+    return ws_for(f, T, path);
+}
+
+size_t dbf_workspace_bytes(const dbf_factors *f, int64_t T) {
+    return dbf_workspace_bytes_path(f, T, DBF_PATH_AUTO);
+}
+
+int dbf_matmul_path(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *workspace,
+                    size_t ws_bytes, void *stream, int path) {
+    int rc = check_factors(f);
+    if (rc) return rc;
+    if (T < 0 || (accumulate != 0 && accumulate != 1)) return DBF_ERR_INVALID_ARG;
+    if (path < DBF_PATH_AUTO || path > DBF_PATH_PREFILL) return DBF_ERR_INVALID_ARG;
+    if (T == 0) return DBF_OK;
+    if (T > (int64_t(1) << 26)) return DBF_ERR_UNSUPPORTED;
+    if (!x || !y) return DBF_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return DBF_ERR_ALIGNMENT;
+    path = resolve_path(path, T);
+    const size_t need = ws_for(f, T, path);
+    if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
+    if (!status_ptr()) return cuda_fail(cudaGetLastError(), "status word");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (path == DBF_PATH_DECODE) return run_decode(f, x, T, y, accumulate, workspace, s);
+    return run_prefill(f, x, T, y, accumulate, workspace, s);
+}
+
+int dbf_matmul(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *workspace,
+               size_t ws_bytes, void *stream) {
+    return dbf_matmul_path(f, x, T, y, accumulate, workspace, ws_bytes, stream, DBF_PATH_AUTO);
+}
+
+size_t dbf_hostio_workspace_bytes(const dbf_factors *f, int64_t T) {
+    if (check_factors(f) != DBF_OK || T < 0) return 0;
+    return align_up(size_t(T) * f->M * 2) + align_up(size_t(T) * f->N * 2) + ws_for(f, T, DBF_PATH_AUTO);
+}
+
+int dbf_matmul_hostio(const dbf_factors *f, const uint16_t *x_host, int64_t T, uint16_t *y_host, int accumulate,
+                      void *workspace, size_t ws_bytes, void *stream) {
+    int rc = check_factors(f);
+    if (rc) return rc;
+    if (T < 0 || (accumulate != 0 && accumulate != 1)) return DBF_ERR_INVALID_ARG;
+    if (T == 0) return DBF_OK;
+    if (!x_host || !y_host) return DBF_ERR_INVALID_ARG;
+    const size_t need = dbf_hostio_workspace_bytes(f, T);
+    if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *base = static_cast<char *>(workspace);
+    uint16_t *xd = reinterpret_cast<uint16_t *>(base);
+    uint16_t *yd = reinterpret_cast<uint16_t *>(base + align_up(size_t(T) * f->M * 2));
+    char *inner = base + align_up(size_t(T) * f->M * 2) + align_up(size_t(T) * f->N * 2);
+    const size_t inner_bytes = ws_bytes - size_t(inner - base);
+    cudaError_t e = cudaMemcpyAsync(xd, x_host, size_t(T) * f->M * 2, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "hostio x copy");
+    if (accumulate) {
+        e = cudaMemcpyAsync(yd, y_host, size_t(T) * f->N * 2, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "hostio y copy");
+    }
+    rc = dbf_matmul(f, xd, T, yd, accumulate, inner, inner_bytes, stream);
+    if (rc) return rc;
+    e = cudaMemcpyAsync(y_host, yd, size_t(T) * f->N * 2, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "hostio y readback");
+    return DBF_OK;
+}
+
+size_t dbf_segmented_workspace_bytes(int32_t N, int32_t M, int32_t R, int32_t ell, int64_t T, int32_t S) {
+    (void)S;
+    if (check_dims(N, M, R, ell) != DBF_OK || T < 0) return 0;
+    return ws_decode(N, M, R, ell, T);
+}
+
+int dbf_matmul_segmented(const dbf_factors *d_adapters, int32_t n_adapters, int32_t N, int32_t M, int32_t R,
+                         int32_t ell, const uint16_t *x, int64_t T, uint16_t *y, const int32_t *d_seg_offsets,
+                         const int32_t *d_seg_adapter, int32_t S, int accumulate, void *workspace, size_t ws_bytes,
+                         void *stream) {
+    using namespace dbfk;
+    int rc = check_dims(N, M, R, ell);
+    if (rc) return rc;
+    if (T < 0 || S < 0 || n_adapters < 0 || (accumulate != 0 && accumulate != 1)) return DBF_ERR_INVALID_ARG;
+    if (T == 0 || S == 0) return DBF_OK;
+    if (S > 65535 || T > (int64_t(1) << 26)) return DBF_ERR_UNSUPPORTED;
+    if (!d_adapters || n_adapters < 1 || !x || !y || !d_seg_offsets || !d_seg_adapter) return DBF_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(d_adapters)) return DBF_ERR_ALIGNMENT;
+    const size_t need = dbf_segmented_workspace_bytes(N, M, R, ell, T, S);
+    if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
+    if (!status_ptr()) return cuda_fail(cudaGetLastError(), "status word");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // columns per chunk sized for about twice the mean segment length
+    const int64_t mean_tok = ceil_div(T, S);
+    const int64_t tok = std::min<int64_t>(T, std::max<int64_t>(2 * mean_tok, 4));
+    const int64_t cols = std::min<int64_t>(ell * tok, 64);
+
+    DecArgs a = {};
+    a.ell = ell;
+    a.T = static_cast<int>(T);
+    a.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    a.ldx = M;
+    a.V = static_cast<__half *>(workspace);
+    a.ldv = static_cast<int>(v_ld(R));
+    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    a.ldy = N;
+    a.accumulate = accumulate;
+    a.seg_off = d_seg_offsets;
+    a.seg_ad = d_seg_adapter;
+    a.adapters = d_adapters;
+    a.n_adapters = n_adapters;
+    a.status = status_ptr();
+
+    DecArgs a1 = a;
+    a1.rows = R;
+    a1.rows_cover = static_cast<int>(round_up(R, 32));
+    a1.K = M;
+    a1.Kw = static_cast<int>(ceil_div(M, 32));
+    DecPlan p1 = plan_decode_stage(a1.rows_cover, a1.Kw, static_cast<int>(cols), 8, num_sms() / std::max(1, S));
+    a1.RB = p1.RB;
+    a1.KS = p1.KS;
+    a1.Wc = p1.Wc;
+    DecArgs a2 = a;
+    a2.rows = N;
+    a2.rows_cover = N;
+    a2.K = R;
+    a2.Kw = static_cast<int>(ceil_div(R, 32));
+    DecPlan p2 = plan_decode_stage(a2.rows_cover, a2.Kw, static_cast<int>(cols), p1.CT, num_sms() / std::max(1, S));
+    p2.CT = p1.CT;
+    a2.RB = p2.RB;
+    a2.KS = p2.KS;
+    a2.Wc = p2.Wc;
+    if (p1.CT == 0 || p2.CT == 0) return DBF_ERR_UNSUPPORTED;
+    cudaError_t e = launch_decode_stage(1, true, p1, a1, S, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "segmented stage 1");
+    e = launch_decode_stage(2, true, p2, a2, S, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "segmented stage 2");
+    return DBF_OK;
+}
+
+int dbf_check_status(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dbf_check_status sync");
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_dbf_status, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "dbf_check_status read");
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_dbf_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "dbf_check_status clear");
+    return v;
+}
+
+int dbf_selftest_bounded_wait(int64_t limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 2000000) return DBF_ERR_INVALID_ARG;
+    int *st = status_ptr();
+    if (!st) return cuda_fail(cudaGetLastError(), "status word");
+    cudaError_t e = dbfk::launch_selftest_wait(st, static_cast<uint64_t>(limit_us) * 1000ull,
+                                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "dbf_selftest_bounded_wait");
+}
+
+}  // extern "C"

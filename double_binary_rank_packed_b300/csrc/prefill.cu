@@ -1,0 +1,434 @@
+// Prefill-regime kernels: the same product for thousands of tokens, where the
+// two sign contractions are genuine dense GEMMs (DBF page, section 2,
+// "Cálculo en la inferencia": ((((X . b^T) B^T) . m^T) A^T) . a^T).
+//
+// Layout of one projection:
+//   prologue   X'[t*ell+i][k]  = fp16(gamma_i[k] * x[t][k])          (activation order)
+//   gemm<1>    V [t*ell+i][r]  = fp16(beta_i[r] * sum_k B2[r][k] X'[t*ell+i][k])
+//   gemm<2>    y [t][n]        = bf16(sum_i alpha_i[n] * sum_r B1[n][r] V[t*ell+i][r])
+//
+// GEMM design (one CTA = 128 weight rows x BN activation rows, 192 threads):
+//   warp 0      TMA producer: 64-wide K slices of the activation tile
+//               (128-byte swizzle) into a 6-stage shared-memory ring
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma
+//   warps 2..5  unpack: each thread owns one weight row (= one TMEM lane),
+//               reads two packed words per K step and writes 32 columns of
+//               +-1 fp16 pairs straight into tensor memory with tcgen05.st;
+//               the MMA reads that as its A operand.  Afterwards the same
+//               warps run the epilogue from the fp32 accumulator.
+// The sign matrix never goes through shared memory, which leaves the shared
+// memory bandwidth to the activation operand.  Every mbarrier wait is
+// bounded; a timeout records DBF_ERR_TIMEOUT, drains in-flight copies and
+// MMAs, frees tensor memory and exits.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dbfk {
+
+namespace {
+
+constexpr int kPfThreads = 192;
+constexpr int kStages = 6;
+constexpr int kBK = 64;  // K elements per stage (128 bytes of fp16)
+
+template <int BN>
+struct PfSmem {
+    static constexpr int kTileBytes = BN * 128;
+    static constexpr int kBarOffset = kStages * kTileBytes;
+    static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+};
+
+__device__ __forceinline__ uint32_t tmem_lane_base(int q) { return static_cast<uint32_t>(32 * q) << 16; }
+
+template <int BN, int STAGE, int ELL>
+__global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
+                                                                 const PfArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PfSmem<BN>::kBarOffset);
+    uint64_t *act_full = bars;                 // [kStages]
+    uint64_t *a_full = bars + kStages;         // [kStages]
+    uint64_t *empty = bars + 2 * kStages;      // [kStages]
+    uint64_t *acc_full = bars + 3 * kStages;   // [1]
+    uint64_t *drain = acc_full + 1;            // [1]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    constexpr uint32_t kTmemCols = 512;
+    constexpr uint32_t kAccCols = 256;           // accumulator columns [0, BN)
+    constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col0 = blockIdx.x * BN;   // first activation row (token*ell + term)
+    const int row0 = blockIdx.y * 128;  // first weight row
+    const int nk = a.nk;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&act_full[s], 1);
+            mbar_init(&a_full[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&act_map);
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            pdl_wait();  // the activations are written by the previous kernel
+            int issued = 0;
+            for (int ks = 0; ks < nk; ++ks) {
+                const int s = ks % kStages;
+                const uint32_t n = ks / kStages;
+                if (!mbar_wait_bounded(&empty[s], (n & 1) ^ 1, abort_flag)) {
+                    *abort_flag = 1;
+                    record_status(a.status, DBF_ERR_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_expect_tx(&act_full[s], PfSmem<BN>::kTileBytes);
+                tma_load_2d(smem + s * PfSmem<BN>::kTileBytes, &act_map, &act_full[s], ks * kBK, col0);
+                ++issued;
+            }
+            if (*abort_flag) {
+                // let every copy still in flight land before the block can exit
+                for (int ks = (issued > kStages ? issued - kStages : 0); ks < issued; ++ks)
+                    mbar_wait_bounded(&act_full[ks % kStages], (ks / kStages) & 1, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int issued = 0;
+            for (int ks = 0; ks < nk; ++ks) {
+                const int s = ks % kStages;
+                const uint32_t par = (ks / kStages) & 1;
+                if (!mbar_wait_bounded(&act_full[s], par, abort_flag) ||
+                    !mbar_wait_bounded(&a_full[s], par, abort_flag)) {
+                    *abort_flag = 1;
+                    record_status(a.status, DBF_ERR_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_col = tmem + kAccCols + s * 32;
+                const uint32_t b_addr = smem_u32(smem + s * PfSmem<BN>::kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    tc_mma_ts(tmem, a_col + kk * 8, desc_sw128(b_addr + kk * 32), kIdesc, (ks | kk) != 0);
+                tc_commit(&empty[s]);
+                ++issued;
+            }
+            if (*abort_flag) {
+                tc_commit(drain);
+                mbar_wait_bounded(drain, 0, nullptr);
+            } else {
+                tc_commit(acc_full);
+            }
+        }
+    } else {
+        // ------------------------------------------------ unpack, then epilogue
+        const int q = warp & 3;                // TMEM lane quarter this warp may access
+        const int row = row0 + 32 * q + lane;  // weight row == TMEM lane
+        const bool row_ok = row < a.rows;
+        const uint32_t *wrow = a.bits + static_cast<size_t>(row_ok ? row : 0) * a.ldw;
+        const uint32_t lane_addr = tmem_lane_base(q);
+        uint32_t cur[8], nxt[8];
+        auto load_block = [&](uint32_t (&dst)[8], int kb) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int w = kb * 8 + j;
+                dst[j] = (row_ok && w < a.Kw) ? __ldg(wrow + w) : 0u;
+            }
+        };
+        const int nkb = (nk + 3) / 4;
+        load_block(cur, 0);
+        bool ok = true;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+            if (kb + 1 < nkb) load_block(nxt, kb + 1);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int ks = kb * 4 + u;
+                if (ks >= nk || !ok) break;
+                const int s = ks % kStages;
+                const uint32_t n = ks / kStages;
+                // warp-uniform decision: tcgen05.st below is a warp-collective instruction
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (n & 1) ^ 1, abort_flag))) {
+                    *abort_flag = 1;
+                    record_status(a.status, DBF_ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();  // the MMAs that read this stage are complete
+                uint32_t v[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    v[j] = sign_pair(cur[2 * u], 15 - j);
+                    v[16 + j] = sign_pair(cur[2 * u + 1], 15 - j);
+                }
+                tmem_st_32x32b_x32(tmem + lane_addr + kAccCols + s * 32, v);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&a_full[s]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+        }
+
+        // epilogue
+        pdl_wait();  // outputs may still be read by the previous kernel
+        const bool acc_ready = ok && __all_sync(0xffffffffu, mbar_wait_bounded(acc_full, 0, abort_flag));
+        if (acc_ready) {
+            tc_fence_after();
+            if constexpr (STAGE == 1) {
+                // V[c][perm(row)] = fp16(beta_{c%ELL}[row] * acc), 0 for rows >= R
+                float bsc[ELL];
+#pragma unroll
+                for (int i = 0; i < ELL; ++i)
+                    bsc[i] = row_ok ? __half2float(a.beta[static_cast<size_t>(i) * a.rows + row]) : 0.f;
+                const bool store_row = row < a.rows_store;  // whole 32-row groups agree
+                const int pos = (row & ~31) + 2 * (lane & 15);
+                constexpr int CW = 8 * ELL;  // columns per chunk (whole tokens)
+                for (int cb = 0; cb < BN; cb += CW) {
+                    uint32_t raw[32];
+                    if constexpr (CW == 8) {
+                        uint32_t (&r8)[8] = *reinterpret_cast<uint32_t(*)[8]>(raw);
+                        tmem_ld_32x32b_x8(tmem + lane_addr + cb, r8);
+                    } else if constexpr (CW == 16) {
+                        tmem_ld_32x32b_x16(tmem + lane_addr + cb, raw);
+                    } else if constexpr (CW == 24) {
+                        tmem_ld_32x32b_x16(tmem + lane_addr + cb, raw);
+                        uint32_t (&r8)[8] = *reinterpret_cast<uint32_t(*)[8]>(raw + 16);
+                        tmem_ld_32x32b_x8(tmem + lane_addr + cb + 16, r8);
+                    } else {
+                        tmem_ld_32x32b_x16(tmem + lane_addr + cb, raw);
+                        tmem_ld_32x32b_x16(tmem + lane_addr + cb + 16, raw + 16);
+                    }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < CW; j += 2) {
+                        const float v0 = bsc[j % ELL] * __uint_as_float(raw[j]);
+                        const float v1 = bsc[(j + 1) % ELL] * __uint_as_float(raw[j + 1]);
+                        // lanes s and s+16 hold rows that land at positions 2s and 2s+1
+                        const float send = (lane < 16) ? v1 : v0;
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        const int c = col0 + cb + j + (lane < 16 ? 0 : 1);
+                        const __half2 h = (lane < 16) ? __floats2half2_rn(v0, recv) : __floats2half2_rn(recv, v1);
+                        if (store_row && c < a.C)
+                            *reinterpret_cast<__half2 *>(a.V + static_cast<size_t>(c) * a.ldv + pos) = h;
+                    }
+                }
+            } else {
+                // y[t][row] = bf16(sum_i alpha_i[row] * acc[t*ELL+i] (+ y))
+                float asc[ELL];
+#pragma unroll
+                for (int i = 0; i < ELL; ++i)
+                    asc[i] = row_ok ? __half2float(a.alpha[static_cast<size_t>(i) * a.rows + row]) : 0.f;
+                const bool paired = (a.ldy % 2 == 0) && (a.rows_store % 2 == 0);
+                constexpr int CW = 8 * ELL;
+                const int T = a.C / ELL;
+                for (int cb = 0; cb < BN; cb += CW) {
+                    uint32_t raw[32];
+                    if constexpr (CW == 8) {
+                        uint32_t (&r8)[8] = *reinterpret_cast<uint32_t(*)[8]>(raw);
+                        tmem_ld_32x32b_x8(tmem + lane_addr + cb, r8);
+                    } else if constexpr (CW == 16) {
+                        tmem_ld_32x32b_x16(tmem + lane_addr + cb, raw);
+                    } else if constexpr (CW == 24) {
+                        tmem_ld_32x32b_x16(tmem + lane_addr + cb, raw);
+                        uint32_t (&r8)[8] = *reinterpret_cast<uint32_t(*)[8]>(raw + 16);
+                        tmem_ld_32x32b_x8(tmem + lane_addr + cb + 16, r8);
+                    } else {
+                        tmem_ld_32x32b_x16(tmem + lane_addr + cb, raw);
+                        tmem_ld_32x32b_x16(tmem + lane_addr + cb + 16, raw + 16);
+                    }
+                    tmem_ld_wait();
+                    const int tb = (col0 + cb) / ELL;
+                    float out[8];
+#pragma unroll
+                    for (int tt = 0; tt < 8; ++tt) {
+                        float s = 0.f;
+#pragma unroll
+                        for (int i = 0; i < ELL; ++i) s += asc[i] * __uint_as_float(raw[tt * ELL + i]);
+                        out[tt] = s;
+                    }
+                    if (paired) {
+#pragma unroll
+                        for (int tt = 0; tt < 8; tt += 2) {
+                            // even lanes write tokens tt, odd lanes tokens tt+1, as bf16 pairs (n, n+1)
+                            const bool even = (lane & 1) == 0;
+                            const float send = even ? out[tt + 1] : out[tt];
+                            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                            const int t = tb + tt + (even ? 0 : 1);
+                            const int n = even ? row : row - 1;
+                            float lo = even ? out[tt] : recv;
+                            float hi = even ? recv : out[tt + 1];
+                            if (t < T && n < a.rows_store) {
+                                __nv_bfloat162 *yp =
+                                    reinterpret_cast<__nv_bfloat162 *>(a.y + static_cast<size_t>(t) * a.ldy + n);
+                                if (a.accumulate) {
+                                    const float2 old = __bfloat1622float2(*yp);
+                                    lo += old.x;
+                                    hi += old.y;
+                                }
+                                *yp = __floats2bfloat162_rn(lo, hi);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int tt = 0; tt < 8; ++tt) {
+                            const int t = tb + tt;
+                            if (t < T && row < a.rows_store) {
+                                __nv_bfloat16 *yp = a.y + static_cast<size_t>(t) * a.ldy + row;
+                                float s = out[tt];
+                                if (a.accumulate) s += __bfloat162float(*yp);
+                                *yp = __float2bfloat16_rn(s);
+                            }
+                        }
+                    }
+                }
+            }
+        } else {
+            *abort_flag = 1;
+            record_status(a.status, DBF_ERR_TIMEOUT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// x [T][M] bf16 -> X' [T*ell + i][ldxs] fp16 in activation order, zero past M.
+__global__ void pf_prologue_kernel(const __nv_bfloat16 *__restrict__ x, int T, int M, int ldx,
+                                   const __half *__restrict__ gamma, int ell, __half *__restrict__ xs, int ldxs) {
+    pdl_trigger();
+    pdl_wait();
+    const int groups = ldxs / 32;
+    const int64_t total = static_cast<int64_t>(T) * groups * 16;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int s = static_cast<int>(e & 15);
+        const int64_t tg = e >> 4;
+        const int g = static_cast<int>(tg % groups);
+        const int t = static_cast<int>(tg / groups);
+        const int k = 32 * g + s;
+        const __nv_bfloat16 *xr = x + static_cast<size_t>(t) * ldx;
+        const float xlo = (k < M) ? __bfloat162float(xr[k]) : 0.f;
+        const float xhi = (k + 16 < M) ? __bfloat162float(xr[k + 16]) : 0.f;
+        for (int i = 0; i < ell; ++i) {
+            const __half *gi = gamma + static_cast<size_t>(i) * M;
+            const float glo = (k < M) ? __half2float(gi[k]) : 0.f;
+            const float ghi = (k + 16 < M) ? __half2float(gi[k + 16]) : 0.f;
+            *reinterpret_cast<__half2 *>(xs + (static_cast<size_t>(t) * ell + i) * ldxs + 32 * g + 2 * s) =
+                __floats2half2_rn(glo * xlo, ghi * xhi);
+        }
+    }
+}
+
+template <int BN, int STAGE, int ELL>
+cudaError_t launch_gemm_t(const CUtensorMap &map, const PfArgs &a, cudaStream_t stream, bool pdl) {
+    auto kern = pf_gemm_kernel<BN, STAGE, ELL>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PfSmem<BN>::kBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int rows_cover = (STAGE == 1) ? a.rows_store : a.rows;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.C + BN - 1) / BN, (rows_cover + 127) / 128, 1);
+    cfg.blockDim = dim3(kPfThreads, 1, 1);
+    cfg.dynamicSmemBytes = PfSmem<BN>::kBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, map, a);
+}
+
+template <int STAGE>
+cudaError_t launch_gemm_stage(const CUtensorMap &map, const PfArgs &a, cudaStream_t stream, bool pdl) {
+    switch (a.ell) {
+        case 1: return launch_gemm_t<256, STAGE, 1>(map, a, stream, pdl);
+        case 2: return launch_gemm_t<256, STAGE, 2>(map, a, stream, pdl);
+        case 3: return launch_gemm_t<240, STAGE, 3>(map, a, stream, pdl);
+        case 4: return launch_gemm_t<256, STAGE, 4>(map, a, stream, pdl);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+int prefill_bn(int ell) { return ell == 3 ? 240 : 256; }
+
+cudaError_t launch_prefill_prologue(const __nv_bfloat16 *x, int T, int M, int ldx, const __half *gamma, int ell,
+                                    __half *xs, int ldxs, cudaStream_t stream, bool pdl) {
+    const int64_t total = static_cast<int64_t>(T) * (ldxs / 32) * 16;
+    int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 148 * 16));
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, pf_prologue_kernel, x, T, M, ldx, gamma, ell, xs, ldxs);
+}
+
+cudaError_t launch_prefill_gemm(int stage, const CUtensorMap &act_map, const PfArgs &args, int bn,
+                                cudaStream_t stream, bool pdl) {
+    (void)bn;
+    return stage == 1 ? launch_gemm_stage<1>(act_map, args, stream, pdl)
+                      : launch_gemm_stage<2>(act_map, args, stream, pdl);
+}
+
+// Tensor map over an fp16 activation matrix [rows][ld] (logical K extent
+// cols_pad), box = 64 K elements x box_rows rows, 128-byte swizzle, zero fill
+// outside the matrix.
+bool encode_act_map(CUtensorMap *map, const __half *base, int rows, int cols_pad, int ld, int box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols_pad), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace dbfk

@@ -1,0 +1,272 @@
+"""ctypes binding of libdbf.so (packed double-binary matmul, sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  PyTorch supplies device memory and the current stream.  Importing
+this module loads libdbf.so and fails loudly when it is missing; there is no
+fallback implementation.
+
+Names follow the C ABI in include/dbf.h: pack, unpack, workspace_bytes,
+matmul, matmul_path, matmul_hostio, matmul_segmented, check_status.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdbf.so")
+
+DBF_OK = 0
+DBF_ERR_INVALID_ARG = -1
+DBF_ERR_ALIGNMENT = -2
+DBF_ERR_UNSUPPORTED = -3
+DBF_ERR_WORKSPACE = -4
+DBF_ERR_CUDA = -5
+DBF_ERR_TIMEOUT = -6
+DBF_ERR_DEVICE_ARG = -7
+
+PATH_AUTO = 0
+PATH_DECODE = 1
+PATH_PREFILL = 2
+
+EXPORTED = (
+    "dbf_pack", "dbf_unpack", "dbf_workspace_bytes", "dbf_workspace_bytes_path",
+    "dbf_decode_max_tokens", "dbf_matmul", "dbf_matmul_path", "dbf_hostio_workspace_bytes",
+    "dbf_matmul_hostio", "dbf_segmented_workspace_bytes", "dbf_matmul_segmented",
+    "dbf_check_status", "dbf_selftest_bounded_wait", "dbf_status_string", "dbf_last_cuda_error",
+)
+
+
+class DbfFactors(ctypes.Structure):
+    """Mirror of struct dbf_factors (include/dbf.h)."""
+
+    _fields_ = [
+        ("N", ctypes.c_int32), ("M", ctypes.c_int32), ("R", ctypes.c_int32), ("ell", ctypes.c_int32),
+        ("ldw1", ctypes.c_int32), ("ldw2", ctypes.c_int32),
+        ("B1", ctypes.c_void_p), ("B2", ctypes.c_void_p),
+        ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
+    ]
+
+
+class DbfError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = f"{what}: {status_string(code)} ({code})"
+        if code == DBF_ERR_CUDA:
+            msg += f" [{last_cuda_error()}]"
+        super().__init__(msg)
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libdbf.so not found at {LIB_PATH}; build it with "
+            "`python -m double_binary_rank_packed_b300.build` (no CPU fallback exists)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, sz, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_int
+    fp = ctypes.POINTER(DbfFactors)
+    sig = {
+        "dbf_pack": (ci, [vp, i64, i64, vp, i64, vp]),
+        "dbf_unpack": (ci, [vp, i64, i64, i64, vp, vp]),
+        "dbf_workspace_bytes": (sz, [fp, i64]),
+        "dbf_workspace_bytes_path": (sz, [fp, i64, ci]),
+        "dbf_decode_max_tokens": (ci, []),
+        "dbf_matmul": (ci, [fp, vp, i64, vp, ci, vp, sz, vp]),
+        "dbf_matmul_path": (ci, [fp, vp, i64, vp, ci, vp, sz, vp, ci]),
+        "dbf_hostio_workspace_bytes": (sz, [fp, i64]),
+        "dbf_matmul_hostio": (ci, [fp, vp, i64, vp, ci, vp, sz, vp]),
+        "dbf_segmented_workspace_bytes": (sz, [i32, i32, i32, i32, i64, i32]),
+        "dbf_matmul_segmented": (ci, [vp, i32, i32, i32, i32, i32, vp, i64, vp, vp, vp, i32, ci, vp, sz, vp]),
+        "dbf_check_status": (ci, [vp]),
+        "dbf_selftest_bounded_wait": (ci, [i64, vp]),
+        "dbf_status_string": (ctypes.c_char_p, [ci]),
+        "dbf_last_cuda_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def status_string(code: int) -> str:
+    return _lib.dbf_status_string(int(code)).decode()
+
+
+def last_cuda_error() -> str:
+    return _lib.dbf_last_cuda_error().decode()
+
+
+def _check(code: int, what: str):
+    if code != DBF_OK:
+        raise DbfError(code, what)
+
+
+def _stream_handle(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def words_per_row(cols: int) -> int:
+    return (cols + 31) // 32
+
+
+# ------------------------------------------------------------------ packing
+
+def pack(signs: torch.Tensor, ldw: int | None = None, stream=None) -> torch.Tensor:
+    """Pack a device int8 sign matrix [rows, cols] into uint32 words [rows, ldw] (dbf_pack)."""
+    if signs.dtype != torch.int8 or signs.dim() != 2 or not signs.is_cuda:
+        raise ValueError("signs must be a 2-D int8 CUDA tensor")
+    signs = signs.contiguous()
+    rows, cols = signs.shape
+    if ldw is None:
+        ldw = words_per_row(cols)
+    words = torch.empty((rows, ldw), dtype=torch.int32, device=signs.device)
+    _check(_lib.dbf_pack(_ptr(signs), rows, cols, _ptr(words), ldw, _stream_handle(stream)), "dbf_pack")
+    return words
+
+
+def unpack(words: torch.Tensor, cols: int, stream=None) -> torch.Tensor:
+    """Inverse of pack: int8 +1/-1 [rows, cols] (dbf_unpack)."""
+    rows, ldw = words.shape
+    signs = torch.empty((rows, cols), dtype=torch.int8, device=words.device)
+    _check(_lib.dbf_unpack(_ptr(words), rows, cols, ldw, _ptr(signs), _stream_handle(stream)), "dbf_unpack")
+    return signs
+
+
+# ------------------------------------------------------------------ factors
+
+class PackedFactors:
+    """Device tensors of one factor set: packed B1, B2 and fp16 scales.
+
+    B1w int32 [N, ldw1], B2w int32 [R, ldw2], alpha [ell, N], beta [ell, R],
+    gamma [ell, M] (torch.float16).  Keeps the tensors alive for as long as
+    the struct handed to the library may be used.
+    """
+
+    def __init__(self, B1w, B2w, alpha, beta, gamma, N, M, R):
+        self.B1w, self.B2w = B1w, B2w
+        self.alpha, self.beta, self.gamma = alpha.contiguous(), beta.contiguous(), gamma.contiguous()
+        self.N, self.M, self.R = int(N), int(M), int(R)
+        self.ell = int(alpha.shape[0])
+        self._struct = DbfFactors(self.N, self.M, self.R, self.ell, int(B1w.shape[1]), int(B2w.shape[1]),
+                                  B1w.data_ptr(), B2w.data_ptr(), self.alpha.data_ptr(),
+                                  self.beta.data_ptr(), self.gamma.data_ptr())
+
+    @classmethod
+    def from_signs(cls, B1, B2, alpha, beta, gamma, ldw1=None, ldw2=None, stream=None):
+        """Pack device int8 sign matrices with dbf_pack and wrap them."""
+        N, R = B1.shape
+        _, M = B2.shape
+        return cls(pack(B1, ldw1, stream), pack(B2, ldw2, stream), alpha, beta, gamma, N, M, R)
+
+    @property
+    def struct(self) -> DbfFactors:
+        return self._struct
+
+    def struct_bytes(self) -> bytes:
+        return ctypes.string_at(ctypes.addressof(self._struct), ctypes.sizeof(DbfFactors))
+
+
+def workspace_bytes(f: PackedFactors, T: int, path: int = PATH_AUTO) -> int:
+    return int(_lib.dbf_workspace_bytes_path(ctypes.byref(f.struct), T, path))
+
+
+def decode_max_tokens() -> int:
+    return int(_lib.dbf_decode_max_tokens())
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns blocks aligned to at least 512 bytes
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ matmul
+
+def matmul_path(f: PackedFactors, x: torch.Tensor, y: torch.Tensor | None = None, accumulate: bool = False,
+                workspace: torch.Tensor | None = None, path: int = PATH_AUTO, stream=None) -> torch.Tensor:
+    """y = sum_i alpha_i . B1 (beta_i . (B2 (gamma_i . x))) for x bf16 [T, M] (dbf_matmul_path)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != f.M:
+        raise ValueError("x must be bf16 [T, M]")
+    x = x.contiguous()
+    T = x.shape[0]
+    if y is None:
+        if accumulate:
+            raise ValueError("accumulate needs y")
+        y = torch.empty((T, f.N), dtype=torch.bfloat16, device=x.device)
+    need = workspace_bytes(f, T, path)
+    if workspace is None:
+        workspace = new_workspace(need, x.device)
+    rc = _lib.dbf_matmul_path(ctypes.byref(f.struct), _ptr(x), T, _ptr(y), int(bool(accumulate)),
+                              _ptr(workspace), workspace.numel(), _stream_handle(stream), int(path))
+    _check(rc, "dbf_matmul")
+    return y
+
+
+def matmul(f: PackedFactors, x: torch.Tensor, y: torch.Tensor | None = None, accumulate: bool = False,
+           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    return matmul_path(f, x, y, accumulate, workspace, PATH_AUTO, stream)
+
+
+def hostio_workspace_bytes(f: PackedFactors, T: int) -> int:
+    return int(_lib.dbf_hostio_workspace_bytes(ctypes.byref(f.struct), T))
+
+
+def matmul_hostio(f: PackedFactors, x_host: torch.Tensor, y_host: torch.Tensor, accumulate: bool = False,
+                  workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Host (pinned) bf16 x [T, M] in, host bf16 y [T, N] out (dbf_matmul_hostio); asynchronous."""
+    T = x_host.shape[0]
+    if workspace is None:
+        workspace = new_workspace(hostio_workspace_bytes(f, T), torch.device("cuda"))
+    rc = _lib.dbf_matmul_hostio(ctypes.byref(f.struct), _ptr(x_host), T, _ptr(y_host), int(bool(accumulate)),
+                                _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(rc, "dbf_matmul_hostio")
+    return y_host
+
+
+def adapter_table(adapters, device) -> torch.Tensor:
+    """Device array of dbf_factors structs for matmul_segmented."""
+    raw = b"".join(a.struct_bytes() for a in adapters)
+    host = torch.frombuffer(bytearray(raw), dtype=torch.uint8)
+    return host.to(device)
+
+
+def segmented_workspace_bytes(N, M, R, ell, T, S) -> int:
+    return int(_lib.dbf_segmented_workspace_bytes(N, M, R, ell, T, S))
+
+
+def matmul_segmented(table: torch.Tensor, n_adapters: int, N: int, M: int, R: int, ell: int, x: torch.Tensor,
+                     seg_offsets: torch.Tensor, seg_adapter: torch.Tensor, y: torch.Tensor | None = None,
+                     accumulate: bool = False, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Routed multi-adapter call (dbf_matmul_segmented); offsets/adapters are device int32."""
+    T = x.shape[0]
+    S = seg_adapter.shape[0]
+    if y is None:
+        y = torch.zeros((T, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = new_workspace(segmented_workspace_bytes(N, M, R, ell, T, S), x.device)
+    rc = _lib.dbf_matmul_segmented(_ptr(table), n_adapters, N, M, R, ell, _ptr(x), T, _ptr(y),
+                                   _ptr(seg_offsets), _ptr(seg_adapter), S, int(bool(accumulate)),
+                                   _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(rc, "dbf_matmul_segmented")
+    return y
+
+
+def check_status(stream=None) -> int:
+    """Synchronise the stream, return and clear the device status word (dbf_check_status)."""
+    return int(_lib.dbf_check_status(_stream_handle(stream)))
+
+
+def selftest_bounded_wait(limit_us: int, stream=None) -> int:
+    return int(_lib.dbf_selftest_bounded_wait(limit_us, _stream_handle(stream)))

@@ -1,0 +1,193 @@
+/*
+ * dbf.h - C ABI of the packed double-binary matmul library (libdbf.so).
+ *
+ * The operation (LoRDBA - "Adaptación Binaria Doble de Bajo Rango", section 2,
+ * Metodología / Arquitectura Central; and "Addition is almost all you need:
+ * Compressing large language models with double binary factorization",
+ * section 2, Formulación Matemática / Cálculo en la inferencia):
+ *
+ *     y = sum_{i=1..ell} alpha_i . B1 (beta_i . (B2 (gamma_i . x)))
+ *
+ * for every token row x of a batch, i.e. y = x dW^T with
+ * dW = sum_i diag(alpha_i) B1 diag(beta_i) B2 diag(gamma_i).
+ * B1 in {+1,-1}^{N x R} and B2 in {+1,-1}^{R x M} are stored at one bit per
+ * entry; alpha_i, beta_i, gamma_i are fp16 per-channel scales.  The two sign
+ * contractions replace multiplications by additions and subtractions (same
+ * sections: "Núcleo de Inferencia" on the LoRDBA page, the evaluation order
+ * on the DBF page).
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* or documented as "device" are CUDA device memory
+ *     owned by the caller; the library keeps no pointer after a call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream.
+ *   - The library never allocates device memory.  Scratch space is passed in
+ *     as `workspace` (device, 256-byte aligned, at least the size the
+ *     matching *_workspace_bytes call returns).
+ *   - fp16 and bf16 values are passed as uint16_t bit patterns.
+ *   - Return value: DBF_OK (0) or a negative DBF_ERR_* code for errors the
+ *     host can see (bad argument, alignment, workspace too small, CUDA launch
+ *     error).  Errors seen on the device (a bounded wait that ran out, an
+ *     invalid segment table) are recorded in a device status word that
+ *     dbf_check_status() reads and clears.
+ *   - T = 0 (no tokens) is a no-op that returns DBF_OK.
+ */
+#ifndef DBF_H
+#define DBF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+enum {
+    DBF_OK = 0,
+    DBF_ERR_INVALID_ARG = -1,  /* null pointer, bad size, ell out of [1,4]   */
+    DBF_ERR_ALIGNMENT = -2,    /* a pointer lacks the stated alignment        */
+    DBF_ERR_UNSUPPORTED = -3,  /* shape outside what the kernels handle       */
+    DBF_ERR_WORKSPACE = -4,    /* workspace null or smaller than required     */
+    DBF_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed        */
+    DBF_ERR_TIMEOUT = -6,      /* device: a bounded wait ran out              */
+    DBF_ERR_DEVICE_ARG = -7    /* device: segment table out of range          */
+};
+
+/* Kernel path selection for dbf_matmul_path (dbf_matmul uses DBF_PATH_AUTO). */
+enum {
+    DBF_PATH_AUTO = 0,     /* decode for T <= dbf_decode_max_tokens(), else prefill */
+    DBF_PATH_DECODE = 1,   /* fused sign-accumulate skinny GEMM (mma.sync, register unpack) */
+    DBF_PATH_PREFILL = 2   /* tcgen05 GEMM, signs unpacked into tensor memory */
+};
+
+/*
+ * One set of factors.  All pointers are device memory.
+ *   B1    uint32 [N][ldw1]  packed rows of B1 (R sign bits each), 16-byte aligned
+ *   B2    uint32 [R][ldw2]  packed rows of B2 (M sign bits each), 16-byte aligned
+ *   alpha fp16   [ell][N]   term-major, 16-byte aligned
+ *   beta  fp16   [ell][R]
+ *   gamma fp16   [ell][M]
+ * Packing: bit j of word w of a row is the sign of column 32*w + j (1 = +1,
+ * 0 = -1); bits past the last column must be 0 (dbf_pack writes them so).
+ * ldw1 >= ceil(R/32), ldw2 >= ceil(M/32); any such stride is accepted.
+ * 1 <= ell <= 4; N, M, R >= 1.
+ */
+typedef struct dbf_factors {
+    int32_t N, M, R, ell;
+    int32_t ldw1, ldw2;
+    const uint32_t *B1;
+    const uint32_t *B2;
+    const uint16_t *alpha;
+    const uint16_t *beta;
+    const uint16_t *gamma;
+} dbf_factors;
+
+/*
+ * dbf_pack: signs (device int8 [rows][cols], row-major, row stride = cols)
+ * -> words (device uint32 [rows][ldw]).  Bit j of word w of row r is 1 when
+ * signs[r][32w+j] > 0, else 0; so +1 -> 1, -1 -> 0, and 0 (sign(0)) counts
+ * as -1 unless callers map it to +1 first.  Bits and words past ceil(cols/32)
+ * words are written as 0.  Storage format: one bit per binary factor entry
+ * (LoRDBA page, section 2, "Eficiencia de Almacenamiento"); the bit order is
+ * this library's own.  ldw >= ceil(cols/32); words 16-byte aligned.
+ */
+int dbf_pack(const int8_t *signs, int64_t rows, int64_t cols,
+             uint32_t *words, int64_t ldw, void *stream);
+
+/* dbf_unpack: inverse of dbf_pack, writes +1/-1 int8 [rows][cols]. */
+int dbf_unpack(const uint32_t *words, int64_t rows, int64_t cols, int64_t ldw,
+               int8_t *signs, void *stream);
+
+/* Device workspace (bytes) dbf_matmul needs for this shape and token count. */
+size_t dbf_workspace_bytes(const dbf_factors *f, int64_t T);
+
+/* Largest T that DBF_PATH_AUTO sends to the decode kernels. */
+int dbf_decode_max_tokens(void);
+
+/*
+ * dbf_matmul: y = sum_i alpha_i . B1 (beta_i . (B2 (gamma_i . x))) per row.
+ *   f          host pointer to a dbf_factors whose pointers are device memory
+ *   x          device bf16 [T][M] row-major, 16-byte aligned
+ *   y          device bf16 [T][N] row-major, 16-byte aligned
+ *   accumulate 0: y = branch;  1: y = bf16(y + branch) (y read, then written)
+ * Arithmetic: fp32 accumulation of the sign sums, intermediates fp32
+ * (decode) or fp16 (prefill), one round-to-nearest-even to bf16 at the end.
+ * Preconditions: |gamma_i * x| and |beta_i * u| stay below 65504 (fp16 range
+ * of the intermediates).
+ */
+int dbf_matmul(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
+               int accumulate, void *workspace, size_t ws_bytes, void *stream);
+
+/* As dbf_matmul, with an explicit kernel path (DBF_PATH_*).  Both paths
+ * compute the same product; the choice only affects speed. */
+int dbf_matmul_path(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
+                    int accumulate, void *workspace, size_t ws_bytes, void *stream,
+                    int path);
+
+/* Workspace bytes for dbf_matmul_path with an explicit path. */
+size_t dbf_workspace_bytes_path(const dbf_factors *f, int64_t T, int path);
+
+/*
+ * dbf_matmul_hostio: the same call with HOST activations and outputs.
+ *   x_host  bf16 [T][M] in host memory (pinned for asynchronous copies)
+ *   y_host  bf16 [T][N] in host memory; read first when accumulate = 1
+ * The call copies x_host into the workspace, runs dbf_matmul, and copies y
+ * back, all on `stream`; y_host is valid after the stream synchronises.
+ * Workspace: dbf_hostio_workspace_bytes(f, T), device memory.
+ */
+size_t dbf_hostio_workspace_bytes(const dbf_factors *f, int64_t T);
+int dbf_matmul_hostio(const dbf_factors *f, const uint16_t *x_host, int64_t T,
+                      uint16_t *y_host, int accumulate, void *workspace,
+                      size_t ws_bytes, void *stream);
+
+/*
+ * dbf_matmul_segmented: a sorted token batch routed to many adapters
+ * (multi-adapter serving of unmerged adapters, S-LoRA / Punica style, as on
+ * the LoRDBA page, section 1).  Tokens [off[s], off[s+1]) use adapter
+ * seg_adapter[s]; each segment is one dbf_matmul with that adapter's factors.
+ *   d_adapters    device array of n_adapters dbf_factors; every entry must
+ *                 have the given N, M, R and ell
+ *   x, y          device bf16 [T][M], [T][N]
+ *   d_seg_offsets device int32 [S+1], non-decreasing, off[0] = 0, off[S] = T
+ *   d_seg_adapter device int32 [S], each in [0, n_adapters)
+ * Rows of y outside every segment are not written.  The table is read on the
+ * device (no host synchronisation); an out-of-range entry skips that segment
+ * and records DBF_ERR_DEVICE_ARG for dbf_check_status.
+ */
+size_t dbf_segmented_workspace_bytes(int32_t N, int32_t M, int32_t R, int32_t ell,
+                                     int64_t T, int32_t S);
+int dbf_matmul_segmented(const dbf_factors *d_adapters, int32_t n_adapters,
+                         int32_t N, int32_t M, int32_t R, int32_t ell,
+                         const uint16_t *x, int64_t T, uint16_t *y,
+                         const int32_t *d_seg_offsets, const int32_t *d_seg_adapter,
+                         int32_t S, int accumulate, void *workspace, size_t ws_bytes,
+                         void *stream);
+
+/*
+ * dbf_check_status: synchronises `stream`, then returns and clears the device
+ * status word of the current device (DBF_OK when no kernel recorded an
+ * error).  A CUDA error from the synchronisation returns DBF_ERR_CUDA.
+ */
+int dbf_check_status(void *stream);
+
+/*
+ * dbf_selftest_bounded_wait: launches one block that waits on an mbarrier
+ * nobody arrives on, with the library's bounded wait and a limit of
+ * `limit_us` microseconds (1..2000000).  The wait gives up, records
+ * DBF_ERR_TIMEOUT in the device status word and the block exits normally;
+ * the CUDA context stays usable.  For tests of the failure path.
+ */
+int dbf_selftest_bounded_wait(int64_t limit_us, void *stream);
+
+/* Human-readable text for a DBF_* code (static string). */
+const char *dbf_status_string(int code);
+
+/* Text of the last CUDA error the library saw on this thread (static buffer). */
+const char *dbf_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DBF_H */

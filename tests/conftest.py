@@ -16,3 +16,16 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """The CUDA library on a GPU; GPU tests fail (not skip) when it cannot load."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without CUDA")
+    from double_binary_rank_packed_b300 import build
+    build.build()
+    from double_binary_rank_packed_b300 import dbf
+    torch.cuda.init()
+    return dbf

@@ -1,0 +1,110 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function
+include/dbf.h declares, and rejects bad arguments on the host before any
+device work (fake pointers are never dereferenced)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from double_binary_rank_packed_b300 import build
+    build.build()
+    from double_binary_rank_packed_b300 import dbf
+    return dbf
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "dbf.h")) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dbf_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary_calls():
+    names = declared_functions()
+    for must in ("dbf_pack", "dbf_matmul", "dbf_matmul_segmented", "dbf_check_status", "dbf_workspace_bytes"):
+        assert must in names
+
+
+def test_every_declared_function_is_exported(lib):
+    cdll = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(cdll, n)]
+    assert not missing, missing
+    assert set(lib.EXPORTED) <= set(declared_functions())
+
+
+def test_struct_layout_matches_header(lib):
+    assert ctypes.sizeof(lib.DbfFactors) == 64
+    assert lib.DbfFactors.B1.offset == 24
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        assert lib.status_string(code) != "unknown status"
+    assert lib.status_string(5) == "unknown status"
+
+
+FAKE = 0x10000000  # 256-byte aligned, never dereferenced by the checks below
+
+
+def _factors(lib, N=64, M=64, R=32, ell=1, ldw1=None, ldw2=None, base=FAKE):
+    return lib.DbfFactors(N, M, R, ell, ldw1 if ldw1 is not None else (R + 31) // 32,
+                          ldw2 if ldw2 is not None else (M + 31) // 32,
+                          base, base + 0x1000, base + 0x2000, base + 0x3000, base + 0x4000)
+
+
+def _call(lib, f, x=FAKE + 0x5000, T=4, y=FAKE + 0x6000, ws=FAKE + 0x7000, ws_bytes=1 << 30, acc=0, path=0):
+    fp = ctypes.byref(f) if f is not None else None
+    return lib._lib.dbf_matmul_path(fp, ctypes.c_void_p(x), T, ctypes.c_void_p(y), acc, ctypes.c_void_p(ws),
+                                    ws_bytes, None, path)
+
+
+def test_host_side_argument_checks(lib):
+    assert _call(lib, None) == lib.DBF_ERR_INVALID_ARG
+    assert _call(lib, _factors(lib, ell=0)) == lib.DBF_ERR_INVALID_ARG
+    assert _call(lib, _factors(lib, ell=5)) == lib.DBF_ERR_INVALID_ARG
+    assert _call(lib, _factors(lib, N=0)) == lib.DBF_ERR_INVALID_ARG
+    assert _call(lib, _factors(lib, ldw2=1)) == lib.DBF_ERR_INVALID_ARG       # M=64 needs 2 words
+    assert _call(lib, _factors(lib, ldw1=0)) == lib.DBF_ERR_INVALID_ARG
+    assert _call(lib, _factors(lib, base=FAKE + 4)) == lib.DBF_ERR_ALIGNMENT
+    assert _call(lib, _factors(lib), x=FAKE + 2) == lib.DBF_ERR_ALIGNMENT
+    assert _call(lib, _factors(lib), y=0) == lib.DBF_ERR_INVALID_ARG
+    assert _call(lib, _factors(lib), T=-1) == lib.DBF_ERR_INVALID_ARG
+    assert _call(lib, _factors(lib), acc=2) == lib.DBF_ERR_INVALID_ARG
+    assert _call(lib, _factors(lib), path=7) == lib.DBF_ERR_INVALID_ARG
+    assert _call(lib, _factors(lib), ws_bytes=16) == lib.DBF_ERR_WORKSPACE
+    assert _call(lib, _factors(lib), ws=0) == lib.DBF_ERR_WORKSPACE
+    assert _call(lib, _factors(lib), ws=FAKE + 0x7010) == lib.DBF_ERR_ALIGNMENT
+    # T = 0 is a no-op and needs nothing else
+    assert _call(lib, _factors(lib), T=0, x=0, y=0, ws=0, ws_bytes=0) == lib.DBF_OK
+
+
+def test_workspace_sizes(lib):
+    f = _factors(lib, N=4096, M=4096, R=3072, ell=1, ldw1=96, ldw2=128)
+    dec = lib._lib.dbf_workspace_bytes_path(ctypes.byref(f), 8, lib.PATH_DECODE)
+    pre = lib._lib.dbf_workspace_bytes_path(ctypes.byref(f), 8, lib.PATH_PREFILL)
+    assert dec >= 8 * 3072 * 2 and dec % 256 == 0
+    assert pre >= 8 * (4096 + 3072) * 2
+    assert lib._lib.dbf_workspace_bytes(ctypes.byref(f), 8) == dec  # T <= 16 goes to decode
+    assert lib._lib.dbf_workspace_bytes(ctypes.byref(f), 2048) == \
+        lib._lib.dbf_workspace_bytes_path(ctypes.byref(f), 2048, lib.PATH_PREFILL)
+    assert lib._lib.dbf_workspace_bytes(None, 8) == 0
+
+
+def test_pack_and_segmented_host_checks(lib):
+    L = lib._lib
+    assert L.dbf_pack(ctypes.c_void_p(FAKE), 4, 40, ctypes.c_void_p(FAKE), 1, None) == lib.DBF_ERR_INVALID_ARG
+    assert L.dbf_pack(ctypes.c_void_p(FAKE), 4, 40, ctypes.c_void_p(FAKE + 2), 2, None) == lib.DBF_ERR_ALIGNMENT
+    assert L.dbf_pack(None, 0, 40, None, 2, None) == lib.DBF_OK
+    assert L.dbf_matmul_segmented(None, 1, 64, 64, 32, 1, None, 0, None, None, None, 1, 0, None, 0, None) == lib.DBF_OK
+    assert L.dbf_matmul_segmented(None, 1, 64, 64, 32, 5, None, 8, None, None, None, 1, 0, None, 0, None) \
+        == lib.DBF_ERR_INVALID_ARG
+    assert L.dbf_matmul_segmented(None, 1, 64, 64, 32, 1, ctypes.c_void_p(FAKE), 8, ctypes.c_void_p(FAKE), None,
+                                  None, 1, 0, None, 0, None) == lib.DBF_ERR_INVALID_ARG
+    assert L.dbf_selftest_bounded_wait(0, None) == lib.DBF_ERR_INVALID_ARG
