@@ -1,0 +1,604 @@
+"""Benchmark of the packed double-binary matmul on B300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-also]
+
+One step = one pass of the hot path over one batch of synthetic input: for the
+decode workloads, L back-to-back dbf_matmul calls, each on its own factor set,
+activations and outputs (L chosen so one step touches more than 4x the L2
+cache, so no timed step is served from L2), captured in one CUDA graph with
+programmatic dependent launch between the kernels.  The headline workload is
+the LoRDBA adapter branch on a 4096x4096 projection (R=64, ell=1) at T=16
+decode tokens.  `value` is tokens per second through one projection call,
+summed over all ranks; `roofline` compares the per-call algorithmic bytes
+(sign bits + fp16 scales + x + y) per call duration with the measured HBM
+copy bandwidth.  The other workloads (1.5-bit DBF projection, the DBF MLP in
+prefill, multi-adapter serving, the tiny case) are measured the same way and
+reported under "also".
+
+--impl reference times the fp64 CPU oracle on the host cores instead (the
+same metric on a bounded sample of the headline workload).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import configs as CFG  # noqa: E402
+from workloads import generators as G  # noqa: E402
+
+METRIC = "tokens/s + % roofline: HBM GB/s (decode T≤16), tensor-pipe util (T=2048)"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+KERNEL_SOURCES = ["decode.cu", "prefill.cu", "misc.cu", "common.cuh", "dbf_api.cu", "kernels.h"]
+
+
+# --------------------------------------------------------------------- setup
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--only", default=None, help="run only this workload key (debugging)")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "double_binary_rank_packed_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload_key):
+    """DRAM bytes per call from a committed ncu summary, if taken on the current kernels."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    e = d.get(workload_key)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_call")
+
+
+def aggregate(local_ms: float, local_units: float, dist_mod=None):
+    """Max elapsed time over ranks and the sum of units: (max_ms, total_units)."""
+    if dist_mod is None:
+        return local_ms, local_units
+    import torch
+    t = torch.tensor([local_ms], dtype=torch.float64)
+    u = torch.tensor([local_units], dtype=torch.float64)
+    if dist_mod.get_backend() == "nccl":
+        t, u = t.cuda(), u.cuda()
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    dist_mod.all_reduce(u, op=dist_mod.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------- clock sampling
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while running."""
+
+    REASONS = {
+        "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+        "hw_power_brake_slowdown": 0x80, "sw_power_cap": 0x4,
+    }
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.samples = []
+        self.reasons = set()
+        self.ok = False
+        self.max_mhz = None
+        self.period = period_s
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.ok = False
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                get = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                    self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+                mask = get(self.h)
+                for name, bit in self.REASONS.items():
+                    if mask & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._t is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------ device inputs
+
+def to_device_factors(dbf, f):
+    import torch
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return dbf.PackedFactors.from_signs(t(f.B1), t(f.B2), t(f.alpha), t(f.beta), t(f.gamma))
+
+
+def clone_factors(dbf, pf):
+    return dbf.PackedFactors(pf.B1w.clone(), pf.B2w.clone(), pf.alpha.clone(), pf.beta.clone(),
+                             pf.gamma.clone(), pf.N, pf.M, pf.R)
+
+
+def bf16_dev(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def call_footprint(N, M, R, ell, T, ldw1, ldw2):
+    return N * ldw1 * 4 + R * ldw2 * 4 + 2 * ell * (N + R + M) + 2 * T * (M + N)
+
+
+# ---------------------------------------------------------------- workloads
+
+class DecodeWorkload:
+    """L independent dbf_matmul calls per step (streamed decode)."""
+
+    def __init__(self, dbf, key, proj, T, outlier_scale=0.0, max_calls=4096):
+        import torch
+        self.dbf, self.key, self.T = dbf, key, T
+        self.N, self.M, self.R, self.ell = proj.N, proj.M, proj.R, proj.ell
+        f = G.make_factors(proj.N, proj.M, proj.R, proj.ell, proj.seed, proj.sign_mode, proj.scale_mode)
+        base = to_device_factors(dbf, f)
+        fp = call_footprint(self.N, self.M, self.R, self.ell, T, base.B1w.shape[1], base.B2w.shape[1])
+        self.L = int(min(max_calls, max(8, math.ceil(4 * L2_BYTES / fp))))
+        xb = G.make_x(T, proj.M, proj.seed, outlier_scale=outlier_scale)
+        x0 = bf16_dev(xb)
+        self.factors = [base] + [clone_factors(dbf, base) for _ in range(self.L - 1)]
+        self.x = [x0] + [x0.clone() for _ in range(self.L - 1)]
+        self.y = [torch.empty((T, proj.N), dtype=torch.bfloat16, device="cuda") for _ in range(self.L)]
+        self.ws = dbf.new_workspace(dbf.workspace_bytes(base, T), "cuda")
+        self.launches_per_call = 2 if T <= dbf.decode_max_tokens() else 3
+        self.bytes_per_call = CFG.algorithmic_bytes(self.N, self.M, self.R, self.ell, T)
+        self.flops_per_call = CFG.flops(self.N, self.M, self.R, self.ell, T)
+        self.bound = "hbm"
+        self.graph = None
+
+    def run_eager(self):
+        for l in range(self.L):
+            self.dbf.matmul(self.factors[l], self.x[l], self.y[l], workspace=self.ws)
+
+    def capture(self):
+        import torch
+        self.run_eager()
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self.run_eager()
+        torch.cuda.synchronize()
+        self.graph = g
+
+    def step(self):
+        self.graph.replay()
+
+    @property
+    def calls(self):
+        return self.L
+
+    @property
+    def tokens_per_step(self):
+        return self.L * self.T
+
+
+class PrefillWorkload:
+    """The DBF MLP layer: up- and down-projection calls per step."""
+
+    def __init__(self, dbf, key, projs, T):
+        import torch
+        self.dbf, self.key, self.T = dbf, key, T
+        self.items = []
+        for p in projs:
+            f = G.make_factors(p.N, p.M, p.R, p.ell, p.seed, p.sign_mode, p.scale_mode)
+            pf = to_device_factors(dbf, f)
+            x = bf16_dev(G.make_x(T, p.M, p.seed))
+            y = torch.empty((T, p.N), dtype=torch.bfloat16, device="cuda")
+            ws = dbf.new_workspace(dbf.workspace_bytes(pf, T), "cuda")
+            self.items.append((pf, x, y, ws, p))
+            del f
+        self.L = len(self.items)
+        self.launches_per_call = 3
+        self.bytes_per_call = sum(CFG.algorithmic_bytes(p.N, p.M, p.R, p.ell, T) for *_, p in self.items) / self.L
+        self.flops_per_call = sum(CFG.flops(p.N, p.M, p.R, p.ell, T) for *_, p in self.items) / self.L
+        self.bound = "tensor"
+        self.graph = None
+
+    def run_eager(self):
+        for pf, x, y, ws, _ in self.items:
+            self.dbf.matmul(pf, x, y, workspace=ws)
+
+    capture = DecodeWorkload.capture
+    step = DecodeWorkload.step
+
+    @property
+    def calls(self):
+        return self.L
+
+    @property
+    def tokens_per_step(self):
+        return self.L * self.T
+
+
+class SegmentedWorkload:
+    """Routed multi-adapter batches: one dbf_matmul_segmented call per adapter pool, L pools per step."""
+
+    def __init__(self, dbf, key, w, max_calls=512):
+        import torch
+        self.dbf, self.key = dbf, key
+        self.T = w.tokens[0]
+        p0 = w.projections[0]
+        self.N, self.M, self.R, self.ell = p0.N, p0.M, p0.R, p0.ell
+        adapters = [to_device_factors(dbf, G.make_factors(p.N, p.M, p.R, p.ell, p.seed)) for p in w.projections]
+        off, ad, _ = G.make_routing(self.T, w.n_adapters, w.routing_seed)
+        touched = sorted(set(int(a) for a in ad))
+        self.S = len(ad)
+        ldw1, ldw2 = adapters[0].B1w.shape[1], adapters[0].B2w.shape[1]
+        pool = len(adapters) * (self.N * ldw1 * 4 + self.R * ldw2 * 4 + 2 * self.ell * (self.N + self.R + self.M))
+        fp = pool + 2 * self.T * (self.M + self.N)
+        self.L = int(min(max_calls, max(4, math.ceil(4 * L2_BYTES / fp))))
+        self.pools = []
+        for l in range(self.L):
+            ads = adapters if l == 0 else [clone_factors(dbf, a) for a in adapters]
+            self.pools.append((ads, dbf.adapter_table(ads, "cuda")))
+        self.off = torch.from_numpy(off).cuda()
+        self.ad = torch.from_numpy(ad).cuda()
+        x0 = bf16_dev(G.make_x(self.T, self.M, w.routing_seed))
+        self.x = [x0] + [x0.clone() for _ in range(self.L - 1)]
+        self.y = [torch.zeros((self.T, self.N), dtype=torch.bfloat16, device="cuda") for _ in range(self.L)]
+        self.ws = dbf.new_workspace(dbf.segmented_workspace_bytes(self.N, self.M, self.R, self.ell, self.T, self.S),
+                                    "cuda")
+        self.launches_per_call = 2
+        # bytes: the sign bits and scales of every adapter the batch touches, plus x and y
+        per_adapter = (self.R * (self.N + self.M)) // 8 + 2 * self.ell * (self.N + self.R + self.M)
+        self.bytes_per_call = len(touched) * per_adapter + 2 * self.T * (self.M + self.N)
+        self.flops_per_call = CFG.flops(self.N, self.M, self.R, self.ell, self.T)
+        self.bound = "hbm"
+        self.graph = None
+
+    def run_eager(self):
+        for l in range(self.L):
+            ads, table = self.pools[l]
+            self.dbf.matmul_segmented(table, len(ads), self.N, self.M, self.R, self.ell, self.x[l], self.off,
+                                      self.ad, self.y[l], workspace=self.ws)
+
+    capture = DecodeWorkload.capture
+    step = DecodeWorkload.step
+
+    @property
+    def calls(self):
+        return self.L
+
+    @property
+    def tokens_per_step(self):
+        return self.L * self.T
+
+
+def time_steps(wl, steps, warmup, dist_mod=None, sampler=None):
+    import torch
+    for _ in range(warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    if dist_mod is not None:
+        dist_mod.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        e0.record(stream)
+        for _ in range(steps):
+            wl.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if dist_mod is not None:
+        dist_mod.barrier()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def roofline_obj(wl, ms_per_call, peaks, traffic):
+    if wl.bound == "hbm":
+        achieved = wl.bytes_per_call / (ms_per_call * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    else:
+        achieved = wl.flops_per_call / (ms_per_call * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    d = {"bound": wl.bound, "achieved": round(achieved, 3), "peak": peak, "unit": unit,
+         "frac": round(achieved / peak, 4), "traffic": traffic}
+    if wl.bound == "tensor":
+        d["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
+    return d
+
+
+# --------------------------------------------------------------- e2e (host io)
+
+def measure_e2e(dbf, wl, steps):
+    """Same calls through dbf_matmul_hostio: pinned host x in, host y out, copies timed."""
+    import torch
+    T, M, N = wl.T, wl.M, wl.N
+    xh_all = torch.empty((wl.L, T, M), dtype=torch.bfloat16, pin_memory=True)
+    yh_all = torch.empty((wl.L, T, N), dtype=torch.bfloat16, pin_memory=True)
+    xh = [xh_all[l] for l in range(wl.L)]
+    yh = [yh_all[l] for l in range(wl.L)]
+    x_host = wl.x[0].cpu()
+    for l in range(wl.L):
+        xh[l].copy_(x_host)
+    ws = dbf.new_workspace(dbf.hostio_workspace_bytes(wl.factors[0], T), "cuda")
+
+    def one_step():
+        for l in range(wl.L):
+            dbf.matmul_hostio(wl.factors[l], xh[l], yh[l], workspace=ws)
+
+    one_step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        one_step()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(wl.tokens_per_step / (ms * 1e-3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": wl.L * T * M * 2, "d2h_bytes_per_step": wl.L * T * N * 2,
+            "ms_per_step": round(ms, 4), "path": "dbf_matmul_hostio (pinned host x and y)"}
+
+
+# ----------------------------------------------------------- CPU oracle timing
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        import numpy  # noqa: F401
+        info = threadpool_info()
+        return max([i.get("num_threads", 1) for i in info] or [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def time_oracle(seconds=10.0, min_calls=2):
+    """The fp64 oracle as it stands on the headline workload: calls per bounded time."""
+    from oracle import dbf_oracle as O
+    p = CFG.ADAPTER_4K.projections[0]
+    T = 16
+    f = G.make_factors(p.N, p.M, p.R, p.ell, p.seed, p.sign_mode, p.scale_mode)
+    xb = G.make_x(T, p.M, p.seed)
+    O.matmul(xb, f)  # warm
+    n = 0
+    t0 = time.perf_counter()
+    while n < min_calls or time.perf_counter() - t0 < seconds:
+        O.matmul(xb, f)
+        n += 1
+    el = time.perf_counter() - t0
+    return {"value": round(n * T / el, 2), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{n} oracle calls (fp64 numpy, factored route) on one N=M=4096 R=64 ell=1 factor set, "
+                      f"T={T} tokens each, {el:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import dbf_oracle as O
+    p = CFG.ADAPTER_4K.projections[0]
+    T = 16
+    f = G.make_factors(p.N, p.M, p.R, p.ell, p.seed, p.sign_mode, p.scale_mode)
+    xb = G.make_x(T, p.M, p.seed)
+    for _ in range(args.warmup):
+        O.matmul(xb, f)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.matmul(xb, f)
+    el = time.perf_counter() - t0
+    value = args.steps * T / el
+    cores = oracle_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "adapter4k: LoRDBA adapter branch N=M=4096 R=64 ell=1, T=16 decode tokens",
+                   "tokens_per_call": T, "calls_per_step": 1, "l2": "not applicable (CPU)"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} timed oracle calls (fp64 numpy) of the headline workload, "
+                                   f"one call per step"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------- main
+
+def workload_line(wl, ms_step, steps, peaks, extra=None):
+    ms_call = ms_step / wl.calls
+    d = {"workload": wl.key, "value": round(wl.tokens_per_step / (ms_step * 1e-3), 1), "unit": "tokens/s",
+         "ms_per_step": round(ms_step, 4), "us_per_call": round(ms_call * 1e3, 3), "calls_per_step": wl.calls,
+         "tokens_per_call": wl.T, "roofline": roofline_obj(wl, ms_call, peaks, measured_traffic(wl.key))}
+    if extra:
+        d.update(extra)
+    return d
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    rank, world, local = dist_env()
+    dist_mod = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        dist_mod = dist
+    else:
+        torch.cuda.set_device(0)
+
+    from double_binary_rank_packed_b300 import build
+    build.build()
+    from double_binary_rank_packed_b300 import dbf
+
+    peaks, peak_src = load_peaks()
+
+    # ---------------- headline: adapter4k, T = 16, streamed
+    p = CFG.ADAPTER_4K.projections[0]
+    head = DecodeWorkload(dbf, "adapter4k_T16", p, 16)
+    head.capture()
+    sampler = ClockSampler(local)
+    ms = time_steps(head, args.steps, args.warmup, dist_mod, sampler)
+    ms_max, tok_total = aggregate(ms, head.tokens_per_step * args.steps, dist_mod)
+    ms_step = ms_max / args.steps
+    value = tok_total / (ms_max * 1e-3)
+    ms_call = ms_step / head.calls
+    clocks = sampler.summary()
+    rl = roofline_obj(head, ms_call, peaks, measured_traffic(head.key))
+    rl["peak_source"] = peak_src
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16",
+        "arith": "fp16 tensor-core operands (+-1 signs, gamma*x, beta*u), fp32 accumulation, bf16 in/out",
+        "data": "synthetic",
+        "config": {"workload": "adapter4k: LoRDBA adapter branch N=M=4096 R=64 ell=1, T=16 decode tokens",
+                   "tokens_per_call": head.T, "calls_per_step": head.calls,
+                   "distinct_factor_sets_per_step": head.calls,
+                   "l2": "no flush: each step touches %.0f MB of distinct inputs (> 4x the 126 MB L2)"
+                         % (head.calls * call_footprint(head.N, head.M, head.R, head.ell, head.T,
+                                                        head.factors[0].B1w.shape[1],
+                                                        head.factors[0].B2w.shape[1]) / 1e6),
+                   "launch": "one CUDA graph per step, programmatic dependent launch between kernels",
+                   "parallelism": f"replicas x{world} (independent projections per rank)"},
+        "roofline": rl,
+        "clocks": clocks,
+        "gpu_launches": args.steps * head.calls * head.launches_per_call,
+    }
+
+    if rank == 0 and world == 1:
+        line["e2e"] = measure_e2e(dbf, head, max(3, min(args.steps, 10)))
+        line["cpu_baseline"] = time_oracle()
+    elif rank == 0:
+        line["e2e"] = measure_e2e(dbf, head, max(3, min(args.steps, 10)))
+
+    if world == 1 and not args.no_also:
+        also = []
+        wls = []
+        for T in (1, 4):
+            wls.append(DecodeWorkload(dbf, f"adapter4k_T{T}", p, T))
+        p3 = CFG.DBF_1P5.projections[0]
+        for T in (1, 8):
+            wls.append(DecodeWorkload(dbf, f"dbf1p5_T{T}", p3, T, outlier_scale=CFG.DBF_1P5.outlier_scale))
+        pt = CFG.TINY.projections[0]
+        wls.append(DecodeWorkload(dbf, "tiny_T8", pt, 8))
+        wls.append(SegmentedWorkload(dbf, "multiadapter_T256", CFG.MULTI_ADAPTER))
+        wls.append(PrefillWorkload(dbf, "dbfmlp_T2048", CFG.DBF_MLP.projections, 2048))
+        for wl in wls:
+            if args.only and wl.key != args.only:
+                continue
+            wl.capture()
+            s2 = ClockSampler(local)
+            ms_w = time_steps(wl, args.steps, args.warmup, None, s2)
+            d = workload_line(wl, ms_w / args.steps, args.steps, peaks)
+            d["clocks"] = s2.summary()
+            d["gpu_launches"] = args.steps * wl.calls * wl.launches_per_call
+            also.append(d)
+            del wl
+            torch.cuda.empty_cache()
+        line["also"] = also
+
+    if rank == 0:
+        print(json.dumps(line))
+    if dist_mod is not None:
+        dist_mod.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
