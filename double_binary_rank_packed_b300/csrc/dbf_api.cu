@@ -219,6 +219,10 @@ int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
 
 }  // namespace
 
+namespace dbfk {
+void set_last_error(const char *msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+}  // namespace dbfk
+
 extern "C" {
 
 const char *dbf_status_string(int code) {

@@ -92,4 +92,7 @@ cudaError_t launch_unpack(const uint32_t *words, int64_t rows, int64_t cols, int
                           cudaStream_t stream);
 cudaError_t launch_selftest_wait(int *status, uint64_t limit_ns, cudaStream_t stream);
 
+// Text returned by dbf_last_cuda_error() on this thread.
+void set_last_error(const char *msg);
+
 }  // namespace dbfk

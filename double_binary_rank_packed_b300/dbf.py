@@ -270,3 +270,29 @@ def check_status(stream=None) -> int:
 
 def selftest_bounded_wait(limit_us: int, stream=None) -> int:
     return int(_lib.dbf_selftest_bounded_wait(limit_us, _stream_handle(stream)))
+
+
+# ------------------------------------------------------- no-allocation variant
+
+_lib.dbf_matmul_decode_noalloc.restype = ctypes.c_int
+_lib.dbf_matmul_decode_noalloc.argtypes = [ctypes.POINTER(DbfFactors), ctypes.c_void_p, ctypes.c_int64,
+                                           ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+
+
+def matmul_decode_noalloc(f: PackedFactors, x: torch.Tensor, y: torch.Tensor | None = None,
+                          accumulate: bool = False, stream=None) -> torch.Tensor:
+    """Decode-path product with the library's static scratch (dbf_matmul_decode_noalloc).
+
+    For callers that cannot allocate device memory; needs no workspace.  The
+    output tensor is allocated here only when y is None.
+    """
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != f.M:
+        raise ValueError("x must be bf16 [T, M]")
+    x = x.contiguous()
+    T = x.shape[0]
+    if y is None:
+        y = torch.empty((T, f.N), dtype=torch.bfloat16, device=x.device)
+    rc = _lib.dbf_matmul_decode_noalloc(ctypes.byref(f.struct), _ptr(x), T, _ptr(y), int(bool(accumulate)),
+                                        _stream_handle(stream))
+    _check(rc, "dbf_matmul_decode_noalloc")
+    return y

@@ -180,6 +180,31 @@ int dbf_check_status(void *stream);
  */
 int dbf_selftest_bounded_wait(int64_t limit_us, void *stream);
 
+/*
+ * dbf_matmul_decode_noalloc: the decode-path dbf_matmul for callers that
+ * cannot allocate device memory -- code recording a CUDA graph (cudaMalloc
+ * cannot be captured), serving loops that must not take cudaMalloc's
+ * implicit device synchronisation, and runtimes whose device memory is a
+ * fixed, pre-planned arena.  The papers have no counterpart; this is a
+ * deployment variant of the same two decode kernels.
+ *   Arguments as dbf_matmul (f, x, T, y, accumulate, stream); no workspace.
+ *   Scratch: a 2 MiB static device array inside the library, held by every
+ *   GPU that loads the library until the process exits.  Calls needing more
+ *   than 2 MiB (ell * T * round_up(R, 64) * 2 bytes) are rejected with
+ *   DBF_ERR_WORKSPACE before any device work, with the reason in
+ *   dbf_last_cuda_error().
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, no allocation); make that first call before any
+ *   stream capture.
+ *   Every call shares the one array and the array keeps the last call's
+ *   contents; the kernels overwrite every element they read, so nothing
+ *   needs clearing, but calls that overlap on the GPU (concurrent streams,
+ *   or several host threads on one device) race on it: serialise them.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+int dbf_matmul_decode_noalloc(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
+                              int accumulate, void *stream);
+
 /* Human-readable text for a DBF_* code (static string). */
 const char *dbf_status_string(int code);
 
