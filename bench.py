@@ -112,6 +112,51 @@ def aggregate(local_ms: float, local_units: float, dist_mod=None):
 
 # ------------------------------------------------------------- clock sampling
 
+class _Nvml:
+    """Minimal NVML access through ctypes (libnvidia-ml ships with the driver)."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, index):
+        import ctypes
+        self.ct = ctypes
+        lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None:
+            raise OSError("libnvidia-ml not found")
+        self.lib = lib
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("nvmlDeviceGetHandleByIndex failed")
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn if fn is not None else lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _clock(self, fn):
+        v = self.ct.c_uint()
+        if fn(self.h, self.ct.c_int(self.NVML_CLOCK_SM), self.ct.byref(v)) != 0:
+            raise OSError("clock query failed")
+        return int(v.value)
+
+    def sm_mhz(self):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo)
+
+    def max_sm_mhz(self):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        if self.reasons_fn(self.h, self.ct.byref(v)) != 0:
+            raise OSError("reasons query failed")
+        return int(v.value)
+
+
 class ClockSampler:
     """Samples SM clock and throttle reasons through NVML while running."""
 
@@ -127,13 +172,11 @@ class ClockSampler:
         self.max_mhz = None
         self.period = period_s
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.nv = _Nvml(device_index)
+            self.max_mhz = self.nv.max_sm_mhz()
             self.ok = True
-        except Exception:
+        except Exception as e:  # no NVML: clocks reported as unavailable
+            self.err = repr(e)
             self.ok = False
         self._stop = threading.Event()
         self._t = None
@@ -141,10 +184,8 @@ class ClockSampler:
     def _run(self):
         while not self._stop.is_set():
             try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                get = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                    self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
-                mask = get(self.h)
+                self.samples.append(self.nv.sm_mhz())
+                mask = self.nv.reasons()
                 for name, bit in self.REASONS.items():
                     if mask & bit:
                         self.reasons.add(name)

@@ -106,6 +106,49 @@ size_t ws_for(const dbf_factors *f, int64_t T, int path) {
     return ws_prefill(f->N, f->M, f->R, f->ell, T);
 }
 
+constexpr int kFusedMaxR = 512;
+
+dbfk::FusedArgs fused_args(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate,
+                           const dbfk::FusedPlan &p) {
+    dbfk::FusedArgs a = {};
+    a.B1 = f->B1;
+    a.B2 = f->B2;
+    a.ldw1 = f->ldw1;
+    a.ldw2 = f->ldw2;
+    a.alpha = reinterpret_cast<const __half *>(f->alpha);
+    a.beta = reinterpret_cast<const __half *>(f->beta);
+    a.gamma = reinterpret_cast<const __half *>(f->gamma);
+    a.N = f->N;
+    a.M = f->M;
+    a.R = f->R;
+    a.ell = f->ell;
+    a.T = static_cast<int>(T);
+    a.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    a.accumulate = accumulate;
+    a.KS = p.KS;
+    a.RB2 = p.RB2;
+    a.Wc1 = p.Wc1;
+    a.status = status_ptr();
+    return a;
+}
+
+// one-launch decode for small R (uses no workspace); *done = false when the
+// shape needs the two-stage kernels instead
+int run_decode_fused(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate,
+                     cudaStream_t stream, bool *done) {
+    using namespace dbfk;
+    *done = false;
+    if (f->R > kFusedMaxR) return DBF_OK;
+    const int64_t cols = std::min<int64_t>(f->ell * T, 64);
+    FusedPlan p = plan_fused(f->N, f->M, f->R, f->ell, static_cast<int>(cols), num_sms(), 1, accumulate != 0);
+    if (p.CT == 0) return DBF_OK;
+    cudaError_t e = launch_decode_fused(false, p, fused_args(f, x, T, y, accumulate, p), 1, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "fused decode");
+    *done = true;
+    return DBF_OK;
+}
+
 // decode path: stage 1 (x -> V), stage 2 (V -> y)
 int run_decode(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *ws,
                cudaStream_t stream) {
@@ -289,7 +332,12 @@ int dbf_matmul_path(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
     if (!status_ptr()) return cuda_fail(cudaGetLastError(), "status word");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (path == DBF_PATH_DECODE) return run_decode(f, x, T, y, accumulate, workspace, s);
+    if (path == DBF_PATH_DECODE) {
+        bool done = false;
+        rc = run_decode_fused(f, x, T, y, accumulate, s, &done);
+        if (rc || done) return rc;
+        return run_decode(f, x, T, y, accumulate, workspace, s);
+    }
     return run_prefill(f, x, T, y, accumulate, workspace, s);
 }
 
@@ -360,6 +408,25 @@ int dbf_matmul_segmented(const dbf_factors *d_adapters, int32_t n_adapters, int3
     const int64_t mean_tok = ceil_div(T, S);
     const int64_t tok = std::min<int64_t>(T, std::max<int64_t>(2 * mean_tok, 4));
     const int64_t cols = std::min<int64_t>(ell * tok, 64);
+
+    if (R <= kFusedMaxR) {
+        FusedPlan p = plan_fused(N, M, R, ell, static_cast<int>(cols), num_sms(), S, accumulate != 0);
+        if (p.CT != 0) {
+            dbf_factors shape = {};
+            shape.N = N;
+            shape.M = M;
+            shape.R = R;
+            shape.ell = ell;
+            FusedArgs fa = fused_args(&shape, x, T, y, accumulate, p);
+            fa.seg_off = d_seg_offsets;
+            fa.seg_ad = d_seg_adapter;
+            fa.adapters = d_adapters;
+            fa.n_adapters = n_adapters;
+            cudaError_t e = launch_decode_fused(true, p, fa, S, s, true);
+            if (e != cudaSuccess) return cuda_fail(e, "segmented fused decode");
+            return DBF_OK;
+        }
+    }
 
     DecArgs a = {};
     a.ell = ell;

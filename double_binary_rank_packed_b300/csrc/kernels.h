@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -52,6 +54,38 @@ struct DecPlan {
 };
 
 DecPlan plan_decode_stage(int rows_cover, int Kw, int columns, int max_ct, int num_sms);
+
+// One-launch decode for small R: a cluster splits stage 1 over K, shares
+// the partial u through distributed shared memory, then each CTA computes
+// its slice of the N output rows.
+struct FusedArgs {
+    const uint32_t *B1, *B2;
+    int ldw1, ldw2;
+    const __half *alpha, *beta, *gamma;
+    int N, M, R, ell, T;
+    const __nv_bfloat16 *x;
+    __nv_bfloat16 *y;
+    int accumulate;
+    int KS;    // cluster size (stage-1 K split)
+    int RB2;   // stage-2 row blocks (16 rows) per CTA
+    int Wc1;   // stage-1 packed words per CTA
+    const int32_t *seg_off;
+    const int32_t *seg_ad;
+    const dbf_factors *adapters;
+    int n_adapters;
+    int *status;
+};
+
+struct FusedPlan {
+    int CT, KS, NQ, RB2, Wc1, grid_x;
+    size_t smem;
+};
+
+// problems: independent calls launched together (segments); the grid is
+// problems x grid_x CTAs.
+FusedPlan plan_fused(int N, int M, int R, int ell, int columns, int num_sms, int problems, bool accumulate);
+cudaError_t launch_decode_fused(bool segmented, const FusedPlan &plan, const FusedArgs &args, int grid_y,
+                                cudaStream_t stream, bool pdl);
 size_t decode_smem_bytes(int CT, int RB, int Wc);
 cudaError_t launch_decode_stage(int stage, bool segmented, const DecPlan &plan, const DecArgs &args,
                                 int grid_y, cudaStream_t stream, bool pdl);
