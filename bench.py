@@ -55,7 +55,13 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--only", default=None, help="run only this workload key (debugging)")
+    ap.add_argument("--only", default=None, help="run only this secondary workload key")
+    ap.add_argument("--workload", default="adapter4k_T16",
+                    help="workload timed for the main line (default: the headline adapter4k_T16)")
+    ap.add_argument("--max-calls", type=int, default=None,
+                    help="cap on calls per step (small profiling runs; breaks the > 4x L2 rule)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-io end-to-end leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
     return ap.parse_args(argv)
 
 
@@ -252,7 +258,8 @@ class DecodeWorkload:
         self.x = [x0] + [x0.clone() for _ in range(self.L - 1)]
         self.y = [torch.empty((T, proj.N), dtype=torch.bfloat16, device="cuda") for _ in range(self.L)]
         self.ws = dbf.new_workspace(dbf.workspace_bytes(base, T), "cuda")
-        self.launches_per_call = 2 if T <= dbf.decode_max_tokens() else 3
+        self.launches_per_call = dbf.launch_count(base, T)
+        self.fp_call = fp
         self.bytes_per_call = CFG.algorithmic_bytes(self.N, self.M, self.R, self.ell, T)
         self.flops_per_call = CFG.flops(self.N, self.M, self.R, self.ell, T)
         self.bound = "hbm"
@@ -261,6 +268,9 @@ class DecodeWorkload:
     def run_eager(self):
         for l in range(self.L):
             self.dbf.matmul(self.factors[l], self.x[l], self.y[l], workspace=self.ws)
+
+    def footprint_per_step(self):
+        return self.L * self.fp_call
 
     def capture(self):
         import torch
@@ -302,7 +312,7 @@ class PrefillWorkload:
             self.items.append((pf, x, y, ws, p))
             del f
         self.L = len(self.items)
-        self.launches_per_call = 3
+        self.launches_per_call = dbf.launch_count(self.items[0][0], T)
         self.bytes_per_call = sum(CFG.algorithmic_bytes(p.N, p.M, p.R, p.ell, T) for *_, p in self.items) / self.L
         self.flops_per_call = sum(CFG.flops(p.N, p.M, p.R, p.ell, T) for *_, p in self.items) / self.L
         self.bound = "tensor"
@@ -314,6 +324,10 @@ class PrefillWorkload:
 
     capture = DecodeWorkload.capture
     step = DecodeWorkload.step
+
+    def footprint_per_step(self):
+        return sum(call_footprint(p.N, p.M, p.R, p.ell, self.T, pf.B1w.shape[1], pf.B2w.shape[1])
+                   for pf, _, _, _, p in self.items)
 
     @property
     def calls(self):
@@ -352,7 +366,8 @@ class SegmentedWorkload:
         self.y = [torch.zeros((self.T, self.N), dtype=torch.bfloat16, device="cuda") for _ in range(self.L)]
         self.ws = dbf.new_workspace(dbf.segmented_workspace_bytes(self.N, self.M, self.R, self.ell, self.T, self.S),
                                     "cuda")
-        self.launches_per_call = 2
+        self.launches_per_call = dbf.segmented_launch_count(self.N, self.M, self.R, self.ell, self.T, self.S)
+        self.fp_call = fp
         # bytes: the sign bits and scales of every adapter the batch touches, plus x and y
         per_adapter = (self.R * (self.N + self.M)) // 8 + 2 * self.ell * (self.N + self.R + self.M)
         self.bytes_per_call = len(touched) * per_adapter + 2 * self.T * (self.M + self.N)
@@ -365,6 +380,9 @@ class SegmentedWorkload:
             ads, table = self.pools[l]
             self.dbf.matmul_segmented(table, len(ads), self.N, self.M, self.R, self.ell, self.x[l], self.off,
                                       self.ad, self.y[l], workspace=self.ws)
+
+    def footprint_per_step(self):
+        return self.L * self.fp_call
 
     capture = DecodeWorkload.capture
     step = DecodeWorkload.step
@@ -544,6 +562,37 @@ def workload_line(wl, ms_step, steps, peaks, extra=None):
     return d
 
 
+def make_workload(dbf, key, max_calls=None):
+    """Workload by key: adapter4k_T{1,4,16}, dbf1p5_T{1,8}, tiny_T{1,8}, multiadapter_T256, dbfmlp_T2048."""
+    cap = {} if max_calls is None else {"max_calls": max_calls}
+    name, _, tok = key.rpartition("_T")
+    T = int(tok)
+    if name == "adapter4k":
+        return DecodeWorkload(dbf, key, CFG.ADAPTER_4K.projections[0], T, **cap)
+    if name == "dbf1p5":
+        return DecodeWorkload(dbf, key, CFG.DBF_1P5.projections[0], T, outlier_scale=CFG.DBF_1P5.outlier_scale,
+                              **cap)
+    if name == "tiny":
+        return DecodeWorkload(dbf, key, CFG.TINY.projections[0], T, **cap)
+    if name == "multiadapter":
+        return SegmentedWorkload(dbf, key, CFG.MULTI_ADAPTER, **cap)
+    if name == "dbfmlp":
+        return PrefillWorkload(dbf, key, CFG.DBF_MLP.projections, T)
+    raise ValueError(f"unknown workload {key!r}")
+
+
+WORKLOAD_TITLES = {
+    "adapter4k": "adapter4k: LoRDBA adapter branch N=M=4096 R=64 ell=1, T={T} decode tokens",
+    "dbf1p5": "dbf1p5: DBF 1.5 bits/weight N=M=4096 R=3072 ell=1, 1% outlier columns x20, T={T} decode tokens",
+    "tiny": "tiny: N=M=256 R=32 ell=1, T={T} tokens",
+    "multiadapter": "multiadapter: 64 adapters N=M=4096 R=32 ell=2, T={T} routed decode tokens",
+    "dbfmlp": "dbfmlp: DBF MLP up 14336x4096 + down 4096x14336, R=5013 ell=2, T={T} prefill tokens",
+}
+
+SECONDARY = ["adapter4k_T1", "adapter4k_T4", "dbf1p5_T1", "dbf1p5_T8", "tiny_T8", "multiadapter_T256",
+             "dbfmlp_T2048"]
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.warmup < 3:
@@ -568,9 +617,8 @@ def main(argv=None):
 
     peaks, peak_src = load_peaks()
 
-    # ---------------- headline: adapter4k, T = 16, streamed
-    p = CFG.ADAPTER_4K.projections[0]
-    head = DecodeWorkload(dbf, "adapter4k_T16", p, 16)
+    # ---------------- main line (default: the headline adapter4k, T = 16), streamed
+    head = make_workload(dbf, args.workload, args.max_calls)
     head.capture()
     sampler = ClockSampler(local)
     ms = time_steps(head, args.steps, args.warmup, dist_mod, sampler)
@@ -581,20 +629,22 @@ def main(argv=None):
     clocks = sampler.summary()
     rl = roofline_obj(head, ms_call, peaks, measured_traffic(head.key))
     rl["peak_source"] = peak_src
+    rl["per"] = "call"
+    rl["us_per_call"] = round(ms_call * 1e3, 3)
 
+    name, _, tok = head.key.rpartition("_T")
+    footprint = head.footprint_per_step()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16",
         "arith": "fp16 tensor-core operands (+-1 signs, gamma*x, beta*u), fp32 accumulation, bf16 in/out",
         "data": "synthetic",
-        "config": {"workload": "adapter4k: LoRDBA adapter branch N=M=4096 R=64 ell=1, T=16 decode tokens",
+        "config": {"workload": WORKLOAD_TITLES[name].format(T=tok),
                    "tokens_per_call": head.T, "calls_per_step": head.calls,
                    "distinct_factor_sets_per_step": head.calls,
-                   "l2": "no flush: each step touches %.0f MB of distinct inputs (> 4x the 126 MB L2)"
-                         % (head.calls * call_footprint(head.N, head.M, head.R, head.ell, head.T,
-                                                        head.factors[0].B1w.shape[1],
-                                                        head.factors[0].B2w.shape[1]) / 1e6),
+                   "l2": ("no flush: each step touches %.0f MB of distinct inputs (%s 4x the 126 MB L2)"
+                          % (footprint / 1e6, ">" if footprint > 4 * L2_BYTES else "NOT >")),
                    "launch": "one CUDA graph per step, programmatic dependent launch between kernels",
                    "parallelism": f"replicas x{world} (independent projections per rank)"},
         "roofline": rl,
@@ -602,27 +652,17 @@ def main(argv=None):
         "gpu_launches": args.steps * head.calls * head.launches_per_call,
     }
 
-    if rank == 0 and world == 1:
+    if rank == 0 and not args.no_e2e and isinstance(head, DecodeWorkload):
         line["e2e"] = measure_e2e(dbf, head, max(3, min(args.steps, 10)))
+    if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = time_oracle()
-    elif rank == 0:
-        line["e2e"] = measure_e2e(dbf, head, max(3, min(args.steps, 10)))
 
     if world == 1 and not args.no_also:
         also = []
-        wls = []
-        for T in (1, 4):
-            wls.append(DecodeWorkload(dbf, f"adapter4k_T{T}", p, T))
-        p3 = CFG.DBF_1P5.projections[0]
-        for T in (1, 8):
-            wls.append(DecodeWorkload(dbf, f"dbf1p5_T{T}", p3, T, outlier_scale=CFG.DBF_1P5.outlier_scale))
-        pt = CFG.TINY.projections[0]
-        wls.append(DecodeWorkload(dbf, "tiny_T8", pt, 8))
-        wls.append(SegmentedWorkload(dbf, "multiadapter_T256", CFG.MULTI_ADAPTER))
-        wls.append(PrefillWorkload(dbf, "dbfmlp_T2048", CFG.DBF_MLP.projections, 2048))
-        for wl in wls:
-            if args.only and wl.key != args.only:
+        for key in SECONDARY:
+            if key == head.key or (args.only and key != args.only):
                 continue
+            wl = make_workload(dbf, key)
             wl.capture()
             s2 = ClockSampler(local)
             ms_w = time_steps(wl, args.steps, args.warmup, None, s2)

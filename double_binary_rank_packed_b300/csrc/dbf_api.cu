@@ -471,6 +471,29 @@ int dbf_matmul_segmented(const dbf_factors *d_adapters, int32_t n_adapters, int3
     return DBF_OK;
 }
 
+int dbf_launch_count(const dbf_factors *f, int64_t T, int path) {
+    if (check_factors(f) != DBF_OK || T <= 0) return 0;
+    if (path < DBF_PATH_AUTO || path > DBF_PATH_PREFILL) return 0;
+    path = resolve_path(path, T);
+    if (path == DBF_PATH_PREFILL) return 3;
+    if (f->R <= kFusedMaxR) {
+        const int64_t cols = std::min<int64_t>(f->ell * T, 64);
+        if (dbfk::plan_fused(f->N, f->M, f->R, f->ell, static_cast<int>(cols), num_sms(), 1, false).CT != 0) return 1;
+    }
+    return 2;
+}
+
+int dbf_segmented_launch_count(int32_t N, int32_t M, int32_t R, int32_t ell, int64_t T, int32_t S) {
+    if (check_dims(N, M, R, ell) != DBF_OK || T <= 0 || S <= 0) return 0;
+    if (R <= kFusedMaxR) {
+        const int64_t mean_tok = ceil_div(T, S);
+        const int64_t tok = std::min<int64_t>(T, std::max<int64_t>(2 * mean_tok, 4));
+        const int64_t cols = std::min<int64_t>(ell * tok, 64);
+        if (dbfk::plan_fused(N, M, R, ell, static_cast<int>(cols), num_sms(), S, false).CT != 0) return 1;
+    }
+    return 2;
+}
+
 int dbf_check_status(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "dbf_check_status sync");

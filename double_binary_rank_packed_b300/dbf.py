@@ -37,6 +37,7 @@ EXPORTED = (
     "dbf_decode_max_tokens", "dbf_matmul", "dbf_matmul_path", "dbf_hostio_workspace_bytes",
     "dbf_matmul_hostio", "dbf_segmented_workspace_bytes", "dbf_matmul_segmented",
     "dbf_check_status", "dbf_selftest_bounded_wait", "dbf_status_string", "dbf_last_cuda_error",
+    "dbf_launch_count", "dbf_segmented_launch_count",
 )
 
 
@@ -84,6 +85,8 @@ def _load():
         "dbf_selftest_bounded_wait": (ci, [i64, vp]),
         "dbf_status_string": (ctypes.c_char_p, [ci]),
         "dbf_last_cuda_error": (ctypes.c_char_p, []),
+        "dbf_launch_count": (ci, [fp, i64, ci]),
+        "dbf_segmented_launch_count": (ci, [i32, i32, i32, i32, i64, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -181,6 +184,16 @@ class PackedFactors:
 
 def workspace_bytes(f: PackedFactors, T: int, path: int = PATH_AUTO) -> int:
     return int(_lib.dbf_workspace_bytes_path(ctypes.byref(f.struct), T, path))
+
+
+def launch_count(f: PackedFactors, T: int, path: int = PATH_AUTO) -> int:
+    """Kernel launches of one matmul_path call (dbf_launch_count)."""
+    return int(_lib.dbf_launch_count(ctypes.byref(f.struct), T, path))
+
+
+def segmented_launch_count(N, M, R, ell, T, S) -> int:
+    """Kernel launches of one matmul_segmented call (dbf_segmented_launch_count)."""
+    return int(_lib.dbf_segmented_launch_count(N, M, R, ell, T, S))
 
 
 def decode_max_tokens() -> int:

@@ -165,6 +165,16 @@ int dbf_matmul_segmented(const dbf_factors *d_adapters, int32_t n_adapters,
                          void *stream);
 
 /*
+ * dbf_launch_count: number of kernel launches one dbf_matmul_path call makes
+ * for these factors, T and path (the fused decode kernel: 1; the two-stage
+ * decode kernels: 2; prefill: 3).  Host only, touches no device memory.
+ * Returns 0 for T <= 0 or invalid arguments.
+ * dbf_segmented_launch_count: the same for dbf_matmul_segmented.
+ */
+int dbf_launch_count(const dbf_factors *f, int64_t T, int path);
+int dbf_segmented_launch_count(int32_t N, int32_t M, int32_t R, int32_t ell, int64_t T, int32_t S);
+
+/*
  * dbf_check_status: synchronises `stream`, then returns and clears the device
  * status word of the current device (DBF_OK when no kernel recorded an
  * error).  A CUDA error from the synchronisation returns DBF_ERR_CUDA.
