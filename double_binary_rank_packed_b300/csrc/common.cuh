@@ -296,4 +296,25 @@ __host__ __device__ __forceinline__ int perm32_pos(int k) {
     return (k & ~31) | (2 * s + e);
 }
 
+// The K order of the decode kernels' activation operands: inside each group
+// of 8 consecutive k, position 2j + e (j = 0..3, e = 0..1) holds k = j + 4e.
+// For mma.m16n8k16 the lane with threadID_in_group c then finds all eight of
+// its B-fragment elements of a 32-k word in the 16 contiguous bytes at 8c,
+// as four fp16 pairs (k, k+4) = (8c+j, 8c+j+4), j = 0..3 (b0 and b1 of the
+// first k16 block are j = 0, 1; of the second, j = 2, 3).
+__host__ __device__ __forceinline__ int perm8_pos(int k) { return (k & ~7) | (2 * (k & 3)) | ((k >> 2) & 1); }
+
+// The matching A-fragment pairs of one packed sign word for the lane's
+// group c: bits 8c+j and 8c+j+4 -> fp16 pair j (+-1.0 each).  The byte is
+// spread so that bit j stays at j and bit j+4 moves to 16+j, then one
+// sign_pair per pair.
+__device__ __forceinline__ void sign_pairs8(uint32_t word, int c, uint32_t (&p)[4]) {
+    const uint32_t t = word >> (8 * c);
+    const uint32_t z = (t & 0xFu) | ((t << 12) & 0xF0000u);
+    p[0] = sign_pair(z, 15);
+    p[1] = sign_pair(z, 14);
+    p[2] = sign_pair(z, 13);
+    p[3] = sign_pair(z, 12);
+}
+
 }  // namespace dbfk

@@ -106,8 +106,6 @@ size_t ws_for(const dbf_factors *f, int64_t T, int path) {
     return ws_prefill(f->N, f->M, f->R, f->ell, T);
 }
 
-constexpr int kFusedMaxR = 512;
-
 dbfk::FusedArgs fused_args(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate,
                            const dbfk::FusedPlan &p) {
     dbfk::FusedArgs a = {};
@@ -126,81 +124,62 @@ dbfk::FusedArgs fused_args(const dbf_factors *f, const uint16_t *x, int64_t T, u
     a.x = reinterpret_cast<const __nv_bfloat16 *>(x);
     a.y = reinterpret_cast<__nv_bfloat16 *>(y);
     a.accumulate = accumulate;
-    a.KS = p.KS;
-    a.RB2 = p.RB2;
-    a.Wc1 = p.Wc1;
+    a.C = p.C;
+    a.RW = p.RW;
+    a.Wc = p.Wc;
     a.status = status_ptr();
     return a;
 }
 
-// one-launch decode for small R (uses no workspace); *done = false when the
-// shape needs the two-stage kernels instead
-int run_decode_fused(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate,
-                     cudaStream_t stream, bool *done) {
-    using namespace dbfk;
-    *done = false;
-    if (f->R > kFusedMaxR) return DBF_OK;
-    const int64_t cols = std::min<int64_t>(f->ell * T, 64);
-    FusedPlan p = plan_fused(f->N, f->M, f->R, f->ell, static_cast<int>(cols), num_sms(), 1, accumulate != 0);
-    if (p.CT == 0) return DBF_OK;
-    cudaError_t e = launch_decode_fused(false, p, fused_args(f, x, T, y, accumulate, p), 1, stream, true);
-    if (e != cudaSuccess) return cuda_fail(e, "fused decode");
-    *done = true;
-    return DBF_OK;
+// Columns (token x term) one decode launch covers per chunk.
+int64_t decode_columns(int64_t ell, int64_t tokens) { return std::min<int64_t>(ell * tokens, 64); }
+
+// Tokens one segment's share of a routed batch is planned for: about twice
+// the mean segment length.
+int64_t segment_tokens(int64_t T, int64_t S) {
+    const int64_t mean_tok = ceil_div(T, std::max<int64_t>(S, 1));
+    return std::min<int64_t>(T, std::max<int64_t>(2 * mean_tok, 4));
 }
 
-// decode path: stage 1 (x -> V), stage 2 (V -> y)
+dbfk::FusedPlan fused_plan_for(int N, int M, int R, int ell, int64_t tokens, int problems, bool accumulate) {
+    if (R > dbfk::kFusedMaxR) return dbfk::FusedPlan{};
+    return dbfk::plan_fused(N, M, R, ell, static_cast<int>(decode_columns(ell, tokens)), num_sms(), problems,
+                            accumulate);
+}
+
+int map_launch_error(cudaError_t e, const char *where) {
+    if (e == cudaErrorNotSupported) {
+        snprintf(g_last_error, sizeof(g_last_error), "%s: no decode tile plan fits this shape", where);
+        return DBF_ERR_UNSUPPORTED;
+    }
+    return cuda_fail(e, where);
+}
+
+// decode path: the one-launch fused kernel when R is small and its plan fits,
+// else the two stages (x -> V, V -> y) through the workspace
 int run_decode(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *ws,
                cudaStream_t stream) {
     using namespace dbfk;
-    const int ell = f->ell;
-    const int64_t cols = std::min<int64_t>(ell * T, 64);
-    DecArgs a = {};
-    a.ell = ell;
-    a.T = static_cast<int>(T);
-    a.x = reinterpret_cast<const __nv_bfloat16 *>(x);
-    a.ldx = f->M;
-    a.gamma = reinterpret_cast<const __half *>(f->gamma);
-    a.beta = reinterpret_cast<const __half *>(f->beta);
-    a.alpha = reinterpret_cast<const __half *>(f->alpha);
-    a.V = static_cast<__half *>(ws);
-    a.ldv = static_cast<int>(v_ld(f->R));
-    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
-    a.ldy = f->N;
-    a.accumulate = accumulate;
-    a.status = status_ptr();
-
-    // stage 1: rows of B2, K = M
-    DecArgs a1 = a;
-    a1.bits = f->B2;
-    a1.ldw = f->ldw2;
-    a1.rows = f->R;
-    a1.rows_cover = static_cast<int>(round_up(f->R, 32));
-    a1.K = f->M;
-    a1.Kw = static_cast<int>(ceil_div(f->M, 32));
-    DecPlan p1 = plan_decode_stage(a1.rows_cover, a1.Kw, static_cast<int>(cols), 8, num_sms());
-    a1.RB = p1.RB;
-    a1.KS = p1.KS;
-    a1.Wc = p1.Wc;
-    // stage 2: rows of B1, K = R
-    DecArgs a2 = a;
-    a2.bits = f->B1;
-    a2.ldw = f->ldw1;
-    a2.rows = f->N;
-    a2.rows_cover = f->N;
-    a2.K = f->R;
-    a2.Kw = static_cast<int>(ceil_div(f->R, 32));
-    DecPlan p2 = plan_decode_stage(a2.rows_cover, a2.Kw, static_cast<int>(cols), p1.CT, num_sms());
-    p2.CT = p1.CT;  // both stages use the same column chunking
-    a2.RB = p2.RB;
-    a2.KS = p2.KS;
-    a2.Wc = p2.Wc;
-    if (p1.CT == 0 || p2.CT == 0) return DBF_ERR_UNSUPPORTED;
-    cudaError_t e = launch_decode_stage(1, false, p1, a1, 1, stream, true);
-    if (e != cudaSuccess) return cuda_fail(e, "decode stage 1");
-    e = launch_decode_stage(2, false, p2, a2, 1, stream, true);
-    if (e != cudaSuccess) return cuda_fail(e, "decode stage 2");
-    return DBF_OK;
+    const FusedPlan fp = fused_plan_for(f->N, f->M, f->R, f->ell, T, 1, accumulate != 0);
+    if (fp.CT != 0) {
+        cudaError_t e = launch_decode_fused(false, fp, fused_args(f, x, T, y, accumulate, fp), 1, stream, true);
+        return e == cudaSuccess ? DBF_OK : cuda_fail(e, "fused decode");
+    }
+    DecodeCall c = {};
+    c.f = f;
+    c.N = f->N;
+    c.M = f->M;
+    c.R = f->R;
+    c.ell = f->ell;
+    c.T = static_cast<int>(T);
+    c.tokens_per_problem = static_cast<int>(T);
+    c.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    c.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    c.accumulate = accumulate;
+    c.status = status_ptr();
+    cudaError_t e = launch_decode_two_stage(c, static_cast<__half *>(ws), static_cast<int>(v_ld(f->R)), num_sms(),
+                                            stream);
+    return e == cudaSuccess ? DBF_OK : map_launch_error(e, "decode");
 }
 
 int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *ws,
@@ -332,12 +311,7 @@ int dbf_matmul_path(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
     if (!status_ptr()) return cuda_fail(cudaGetLastError(), "status word");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (path == DBF_PATH_DECODE) {
-        bool done = false;
-        rc = run_decode_fused(f, x, T, y, accumulate, s, &done);
-        if (rc || done) return rc;
-        return run_decode(f, x, T, y, accumulate, workspace, s);
-    }
+    if (path == DBF_PATH_DECODE) return run_decode(f, x, T, y, accumulate, workspace, s);
     return run_prefill(f, x, T, y, accumulate, workspace, s);
 }
 
@@ -404,71 +378,41 @@ int dbf_matmul_segmented(const dbf_factors *d_adapters, int32_t n_adapters, int3
     if (!status_ptr()) return cuda_fail(cudaGetLastError(), "status word");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // columns per chunk sized for about twice the mean segment length
-    const int64_t mean_tok = ceil_div(T, S);
-    const int64_t tok = std::min<int64_t>(T, std::max<int64_t>(2 * mean_tok, 4));
-    const int64_t cols = std::min<int64_t>(ell * tok, 64);
-
-    if (R <= kFusedMaxR) {
-        FusedPlan p = plan_fused(N, M, R, ell, static_cast<int>(cols), num_sms(), S, accumulate != 0);
-        if (p.CT != 0) {
-            dbf_factors shape = {};
-            shape.N = N;
-            shape.M = M;
-            shape.R = R;
-            shape.ell = ell;
-            FusedArgs fa = fused_args(&shape, x, T, y, accumulate, p);
-            fa.seg_off = d_seg_offsets;
-            fa.seg_ad = d_seg_adapter;
-            fa.adapters = d_adapters;
-            fa.n_adapters = n_adapters;
-            cudaError_t e = launch_decode_fused(true, p, fa, S, s, true);
-            if (e != cudaSuccess) return cuda_fail(e, "segmented fused decode");
-            return DBF_OK;
-        }
+    const int64_t tok = segment_tokens(T, S);
+    FusedPlan p = fused_plan_for(N, M, R, ell, tok, S, accumulate != 0);
+    if (p.CT != 0) {
+        dbf_factors shape = {};
+        shape.N = N;
+        shape.M = M;
+        shape.R = R;
+        shape.ell = ell;
+        FusedArgs fa = fused_args(&shape, x, T, y, accumulate, p);
+        fa.seg_off = d_seg_offsets;
+        fa.seg_ad = d_seg_adapter;
+        fa.adapters = d_adapters;
+        fa.n_adapters = n_adapters;
+        cudaError_t e = launch_decode_fused(true, p, fa, S, s, true);
+        return e == cudaSuccess ? DBF_OK : cuda_fail(e, "segmented fused decode");
     }
-
-    DecArgs a = {};
-    a.ell = ell;
-    a.T = static_cast<int>(T);
-    a.x = reinterpret_cast<const __nv_bfloat16 *>(x);
-    a.ldx = M;
-    a.V = static_cast<__half *>(workspace);
-    a.ldv = static_cast<int>(v_ld(R));
-    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
-    a.ldy = N;
-    a.accumulate = accumulate;
-    a.seg_off = d_seg_offsets;
-    a.seg_ad = d_seg_adapter;
-    a.adapters = d_adapters;
-    a.n_adapters = n_adapters;
-    a.status = status_ptr();
-
-    DecArgs a1 = a;
-    a1.rows = R;
-    a1.rows_cover = static_cast<int>(round_up(R, 32));
-    a1.K = M;
-    a1.Kw = static_cast<int>(ceil_div(M, 32));
-    DecPlan p1 = plan_decode_stage(a1.rows_cover, a1.Kw, static_cast<int>(cols), 8, num_sms() / std::max(1, S));
-    a1.RB = p1.RB;
-    a1.KS = p1.KS;
-    a1.Wc = p1.Wc;
-    DecArgs a2 = a;
-    a2.rows = N;
-    a2.rows_cover = N;
-    a2.K = R;
-    a2.Kw = static_cast<int>(ceil_div(R, 32));
-    DecPlan p2 = plan_decode_stage(a2.rows_cover, a2.Kw, static_cast<int>(cols), p1.CT, num_sms() / std::max(1, S));
-    p2.CT = p1.CT;
-    a2.RB = p2.RB;
-    a2.KS = p2.KS;
-    a2.Wc = p2.Wc;
-    if (p1.CT == 0 || p2.CT == 0) return DBF_ERR_UNSUPPORTED;
-    cudaError_t e = launch_decode_stage(1, true, p1, a1, S, s, true);
-    if (e != cudaSuccess) return cuda_fail(e, "segmented stage 1");
-    e = launch_decode_stage(2, true, p2, a2, S, s, true);
-    if (e != cudaSuccess) return cuda_fail(e, "segmented stage 2");
-    return DBF_OK;
+    DecodeCall c = {};
+    c.N = N;
+    c.M = M;
+    c.R = R;
+    c.ell = ell;
+    c.T = static_cast<int>(T);
+    c.tokens_per_problem = static_cast<int>(tok);
+    c.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    c.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    c.accumulate = accumulate;
+    c.seg_off = d_seg_offsets;
+    c.seg_ad = d_seg_adapter;
+    c.adapters = d_adapters;
+    c.n_adapters = n_adapters;
+    c.S = S;
+    c.status = status_ptr();
+    cudaError_t e = launch_decode_two_stage(c, static_cast<__half *>(workspace), static_cast<int>(v_ld(R)), num_sms(),
+                                            s);
+    return e == cudaSuccess ? DBF_OK : map_launch_error(e, "segmented decode");
 }
 
 int dbf_launch_count(const dbf_factors *f, int64_t T, int path) {
@@ -476,22 +420,12 @@ int dbf_launch_count(const dbf_factors *f, int64_t T, int path) {
     if (path < DBF_PATH_AUTO || path > DBF_PATH_PREFILL) return 0;
     path = resolve_path(path, T);
     if (path == DBF_PATH_PREFILL) return 3;
-    if (f->R <= kFusedMaxR) {
-        const int64_t cols = std::min<int64_t>(f->ell * T, 64);
-        if (dbfk::plan_fused(f->N, f->M, f->R, f->ell, static_cast<int>(cols), num_sms(), 1, false).CT != 0) return 1;
-    }
-    return 2;
+    return fused_plan_for(f->N, f->M, f->R, f->ell, T, 1, false).CT != 0 ? 1 : 2;
 }
 
 int dbf_segmented_launch_count(int32_t N, int32_t M, int32_t R, int32_t ell, int64_t T, int32_t S) {
     if (check_dims(N, M, R, ell) != DBF_OK || T <= 0 || S <= 0) return 0;
-    if (R <= kFusedMaxR) {
-        const int64_t mean_tok = ceil_div(T, S);
-        const int64_t tok = std::min<int64_t>(T, std::max<int64_t>(2 * mean_tok, 4));
-        const int64_t cols = std::min<int64_t>(ell * tok, 64);
-        if (dbfk::plan_fused(N, M, R, ell, static_cast<int>(cols), num_sms(), S, false).CT != 0) return 1;
-    }
-    return 2;
+    return fused_plan_for(N, M, R, ell, segment_tokens(T, S), S, false).CT != 0 ? 1 : 2;
 }
 
 int dbf_check_status(void *stream) {

@@ -4,29 +4,37 @@
 // them; DBF page, section 2, "Cálculo en la inferencia": the order
 // gamma -> B2 -> beta -> B1 -> alpha).
 //
-// The sign contraction runs on the tensor cores with mma.sync m16n8k16:
+// At decode sizes a call moves a few hundred KB to a few MB, which HBM
+// delivers in well under a microsecond; what a call costs is its chain of
+// dependent latencies.  The kernels are laid out for that:
+//   * every input no earlier kernel writes (packed signs, scales) is
+//     prefetched with cp.async before griddepcontrol.wait, so it overlaps the
+//     previous kernel under programmatic dependent launch;
+//   * after the wait a CTA issues all its activation loads at once, and every
+//     later phase is spread over all threads (one or two iterations each);
+//   * partial sums leave the tensor-core fragments straight into the shared
+//     memory of the CTA that needs them (distributed shared memory inside a
+//     thread-block cluster), followed by one cluster barrier.
+//
+// The sign contraction runs on mma.sync m16n8k16 (fp16 in, fp32 accumulate):
 // packed sign words are unpacked in registers straight into the A fragment
-// (one shift + one LOP3 per fp16 pair, see sign_pair), the activations (the
-// ell*T columns) are the B operand, loaded with ldmatrix from shared memory in
-// the permuted K order sign_pair expects.  A CUDA-core add/subtract needs
-// about T+2 instructions per sign bit; this costs about one per bit for any
-// T <= 64 columns.
+// (one shift + one LOP3 per fp16 pair, see sign_pair); the activation columns
+// (token t, term i -> column t*ell + i) are the B operand, read with ldmatrix
+// from shared memory in the permuted K order sign_pair expects.
 //
 // Two kernel shapes:
-//   dec_fused_kernel  (R small, the adapter case): one launch per call.  A
-//       thread-block cluster splits stage 1 over K; every CTA pushes its
-//       partial u into every CTA of the cluster (distributed shared memory),
-//       each sums the partials in rank order, forms the fp16 v = beta*u
-//       locally, and runs stage 2 for its own slice of the N output rows.
-//       Every cluster recomputes stage 1 (R*M bits, small next to the call
-//       when R is small); no intermediate goes through global memory.
-//   dec_stage_kernel  (any R): one launch per stage; stage 1 writes V (fp16)
-//       to the workspace, stage 2 reads it.  CTAs own 16*RB weight rows and
-//       a K-slice; KS CTAs of a cluster split K and reduce through DSMEM.
-// Both prefetch every input that no earlier kernel writes (packed signs and
-// scales) with cp.async before griddepcontrol.wait, so that after the
-// dependency resolves a call waits for one more memory latency (x or V).
+//   dec_fused_kernel  (R <= 256, the adapter case): one launch per call.  The
+//       CTAs of a cluster split stage 1 over M; every CTA pushes its partial u
+//       into every CTA of the cluster, each sums them in rank order, forms the
+//       fp16 v = beta*u itself and runs stage 2 for its own slice of the N
+//       output rows.  Every cluster recomputes stage 1 (R*M bits, small next
+//       to the call when R is small); no intermediate goes through HBM.
+//   dec_stage_kernel  (any R): one launch per stage.  Stage 1 writes V (fp16)
+//       to the workspace, stage 2 reads it.  A CTA owns 16*RB weight rows and a
+//       K slice; the KS CTAs of a cluster split K and push their partials to
+//       the CTA that owns each 32-row group.
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -46,8 +54,6 @@ __host__ __device__ inline int ldws_for(int W) {
     if ((s & 7) == 0) s += 4;
     return s;
 }
-
-__host__ __device__ inline int lda_for(int W) { return 32 * W + 8; }  // halves; +16 B kills ldmatrix conflicts
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
@@ -84,6 +90,27 @@ __device__ __forceinline__ void copy_rows_async(void *dst, int dst_stride, const
     }
 }
 
+// As copy_rows_async, for data an earlier kernel may have written (x, V, the
+// old y): 16-byte cp.async.cg (through L2 only) when aligned, else plain
+// coherent loads and stores.
+__device__ __forceinline__ void copy_rows_dep(void *dst, int dst_stride, const void *src, size_t src_stride,
+                                              int nrows, int row_bytes, int tid, int nthr) {
+    if (nrows <= 0 || row_bytes <= 0) return;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+    const uintptr_t all = d | s | static_cast<uintptr_t>(dst_stride) | static_cast<uintptr_t>(src_stride) |
+                          static_cast<uintptr_t>(row_bytes);
+    if ((all & 15) == 0) {
+        copy_rows_async(dst, dst_stride, src, src_stride, nrows, row_bytes, tid, nthr);
+        return;
+    }
+    const int q = row_bytes >> 1;
+    for (int e = tid; e < nrows * q; e += nthr) {
+        const int r = e / q, c = e - r * q;
+        *reinterpret_cast<uint16_t *>(static_cast<char *>(dst) + r * dst_stride + 2 * c) =
+            *reinterpret_cast<const uint16_t *>(static_cast<const char *>(src) + r * src_stride + 2 * c);
+    }
+}
+
 // Zero nrows x row_bytes (row_bytes a multiple of 4) of shared memory.
 __device__ __forceinline__ void zero_rows(void *dst, int dst_stride, int nrows, int row_bytes, int tid, int nthr) {
     const int q = row_bytes >> 2;
@@ -93,145 +120,485 @@ __device__ __forceinline__ void zero_rows(void *dst, int dst_stride, int nrows, 
     }
 }
 
-// One warp: 16 weight rows (rowA points at the lane's row g) x words
-// [wb, we) x CT column tiles of 8 activation rows.
-template <int CT>
-__device__ __forceinline__ void mma_rows(const uint32_t *__restrict__ rowA, int ldws, uint32_t act_base, int lda_s,
-                                         int wb, int we, float (&acc)[CT][4], int lane) {
-    const int c = lane & 3;
-    const uint32_t sh0 = 15 - c, sh1 = 11 - c, sh2 = 7 - c, sh3 = 3 - c;
-    const uint32_t *rowB = rowA + 8 * ldws;
-#pragma unroll 2
-    for (int j = wb; j < we; ++j) {
-        const uint32_t wa = rowA[j], wv = rowB[j];
-        const uint32_t a00 = sign_pair(wa, sh0), a01 = sign_pair(wv, sh0);
-        const uint32_t a02 = sign_pair(wa, sh1), a03 = sign_pair(wv, sh1);
-        const uint32_t a10 = sign_pair(wa, sh2), a11 = sign_pair(wv, sh2);
-        const uint32_t a12 = sign_pair(wa, sh3), a13 = sign_pair(wv, sh3);
-#pragma unroll
-        for (int ct = 0; ct < CT; ++ct) {
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(act_base + static_cast<uint32_t>((ct * 8 * lda_s + 32 * j) * 2), b0, b1, b2, b3);
-            mma_16816(acc[ct], a00, a01, a02, a03, b0, b1);
-            mma_16816(acc[ct], a10, a11, a12, a13, b2, b3);
-        }
-    }
-}
-
-// Accumulator fragments (16 rows x 8*CT columns) -> shared-memory tile.
-template <int CT>
-__device__ __forceinline__ void store_tile(float *tile, int ld, const float (&acc)[CT][4], int lane) {
-    const int g = lane >> 2, c = lane & 3;
-#pragma unroll
-    for (int ct = 0; ct < CT; ++ct) {
-        const int col = ct * 8 + 2 * c;
-        *reinterpret_cast<float2 *>(tile + g * ld + col) = make_float2(acc[ct][0], acc[ct][1]);
-        *reinterpret_cast<float2 *>(tile + (g + 8) * ld + col) = make_float2(acc[ct][2], acc[ct][3]);
-    }
-}
-
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// x rows of a token chunk -> activation rows t*ell+i in logical K order:
-// act[t*ell+i][32g + 2s + e] = fp16(gamma_i[k] * x[t][k]), k = 32g + s + 16e
-// (g, k local to this CTA's K slice).  gam_s holds gamma for the slice in
-// physical order, zero past kvalid.  One piece = 8 consecutive k and the 8 k
-// sixteen further on, which become 16 consecutive logical positions; x is
-// read straight from global memory (16-byte loads when vec).
-__device__ __forceinline__ void load_x_act(__half *act, int lda, const __nv_bfloat16 *x, size_t ldx, int ntok,
-                                           const __half *gam_s, int ldg, int ell, int Wslice, int kvalid, bool vec,
-                                           int tid, int nthr) {
-    const int npieces = ntok * Wslice * 2;
-    for (int p = tid; p < npieces; p += nthr) {
-        const int q = p & 1;
-        const int gt = p >> 1;
-        const int t = gt / Wslice;
-        const int g = gt - t * Wslice;
-        const int kl = 32 * g + 8 * q;  // local physical k of the first element
-        const __nv_bfloat16 *xr = x + size_t(t) * ldx;
-        float xa[8], xb[8];
-        if (vec && kl + 24 <= kvalid) {
-            const uint4 va = *reinterpret_cast<const uint4 *>(xr + kl);
-            const uint4 vb = *reinterpret_cast<const uint4 *>(xr + kl + 16);
-            xa[0] = bf16lo(va.x); xa[1] = bf16hi(va.x); xa[2] = bf16lo(va.y); xa[3] = bf16hi(va.y);
-            xa[4] = bf16lo(va.z); xa[5] = bf16hi(va.z); xa[6] = bf16lo(va.w); xa[7] = bf16hi(va.w);
-            xb[0] = bf16lo(vb.x); xb[1] = bf16hi(vb.x); xb[2] = bf16lo(vb.y); xb[3] = bf16hi(vb.y);
-            xb[4] = bf16lo(vb.z); xb[5] = bf16hi(vb.z); xb[6] = bf16lo(vb.w); xb[7] = bf16hi(vb.w);
+// Two m16n8k16 MMAs (k 0..15 and 16..31 of one packed word) for rows g and
+// g+8 of a 16-row block: pa / pv are the sign pairs of the two rows, b the
+// lane's four activation pairs (see perm8_pos and sign_pairs8).
+__device__ __forceinline__ void mma_word8(float (&acc)[4], const uint32_t (&pa)[4], const uint32_t (&pv)[4],
+                                          const uint32_t (&b)[4]) {
+    mma_16816(acc, pa[0], pv[0], pa[1], pv[1], b[0], b[1]);
+    mma_16816(acc, pa[2], pv[2], pa[3], pv[3], b[2], b[3]);
+}
+
+// 8 bf16 of x (k0 .. k0+7 of one row, zero at k >= kmax) with plain
+// coherent loads: x is written by an earlier kernel.
+__device__ __forceinline__ uint4 load_x8(const __nv_bfloat16 *row, int k0, int kmax, bool vec) {
+    if (vec && k0 + 8 <= kmax) return *reinterpret_cast<const uint4 *>(row + k0);
+    const uint16_t *r16 = reinterpret_cast<const uint16_t *>(row);
+    uint16_t v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = (k0 + j < kmax) ? r16[k0 + j] : uint16_t(0);
+    return make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16), v[4] | (uint32_t(v[5]) << 16),
+                      v[6] | (uint32_t(v[7]) << 16));
+}
+
+// The lane's four B pairs of one word from 8 bf16 x (physical k 8c..8c+7)
+// and the matching 8 fp16 gamma: pair j = fp16(gamma*x) at (8c+j, 8c+j+4).
+__device__ __forceinline__ void x_pairs(const uint4 &xv, const uint4 &gv, uint32_t (&b)[4]) {
+    const float2 g01 = __half22float2(*reinterpret_cast<const __half2 *>(&gv.x));
+    const float2 g23 = __half22float2(*reinterpret_cast<const __half2 *>(&gv.y));
+    const float2 g45 = __half22float2(*reinterpret_cast<const __half2 *>(&gv.z));
+    const float2 g67 = __half22float2(*reinterpret_cast<const __half2 *>(&gv.w));
+    __half2 h;
+    h = __floats2half2_rn(bf16lo(xv.x) * g01.x, bf16lo(xv.z) * g45.x);
+    b[0] = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2half2_rn(bf16hi(xv.x) * g01.y, bf16hi(xv.z) * g45.y);
+    b[1] = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2half2_rn(bf16lo(xv.y) * g23.x, bf16lo(xv.w) * g67.x);
+    b[2] = *reinterpret_cast<uint32_t *>(&h);
+    h = __floats2half2_rn(bf16hi(xv.y) * g23.y, bf16hi(xv.w) * g67.y);
+    b[3] = *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <int CT>
+__device__ __forceinline__ void zero_acc(float (&acc)[CT][4]) {
+#pragma unroll
+    for (int ct = 0; ct < CT; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
+}
+
+// Fragment (16 rows x 8*CT columns) -> 32-bit shared-memory address `base`
+// (row stride ld floats) of the CTA `rank` of the cluster (or of this CTA when
+// remote is false).
+template <int CT>
+__device__ __forceinline__ void put_frag(uint32_t base, int ld, const float (&acc)[CT][4], int lane, bool remote,
+                                         uint32_t rank) {
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int ct = 0; ct < CT; ++ct) {
+        const uint32_t a0 = base + 4u * static_cast<uint32_t>(g * ld + ct * 8 + 2 * c);
+        const uint32_t a1 = a0 + 4u * static_cast<uint32_t>(8 * ld);
+        if (remote) {
+            asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(mapa_shared(a0, rank)), "f"(acc[ct][0]),
+                         "f"(acc[ct][1])
+                         : "memory");
+            asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(mapa_shared(a1, rank)), "f"(acc[ct][2]),
+                         "f"(acc[ct][3])
+                         : "memory");
         } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                xa[j] = (kl + j < kvalid) ? __bfloat162float(xr[kl + j]) : 0.f;
-                xb[j] = (kl + 16 + j < kvalid) ? __bfloat162float(xr[kl + 16 + j]) : 0.f;
-            }
+            asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a0), "f"(acc[ct][0]), "f"(acc[ct][1]) : "memory");
+            asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a1), "f"(acc[ct][2]), "f"(acc[ct][3]) : "memory");
         }
+    }
+}
+
+__device__ __forceinline__ void add4(float4 &u, const float4 &o) {
+    u.x += o.x;
+    u.y += o.y;
+    u.z += o.z;
+    u.w += o.w;
+}
+
+__device__ __forceinline__ void push_float4(uint32_t addr, const float4 &u, uint32_t rank) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(mapa_shared(addr, rank)), "f"(u.x),
+                 "f"(u.y), "f"(u.z), "f"(u.w)
+                 : "memory");
+}
+
+// Words a warp streams per batch: every activation load of a batch is in
+// flight before the first conversion.
+template <int CT>
+__host__ __device__ constexpr int words_per_batch() {
+    return CT >= 8 ? 1 : (CT >= 4 ? 2 : 4);
+}
+
+// Stage-2 tile (RW rows x columns, fp32) -> y[t][n] = bf16(sum_i alpha_i[n]
+// w[t*ell+i][n] (+ y_in)), pairs of adjacent n per thread.
+__device__ __forceinline__ void epilogue_tile(const float *tile, int ldt, const __half *alp, int lda_al, int ell,
+                                              int ntok, int nrows, int row_base, __nv_bfloat16 *y, size_t ldy,
+                                              const __nv_bfloat16 *yst, int ldyst, bool accumulate, bool pairs_ok,
+                                              int tid) {
+    const int np = (nrows + 1) >> 1;  // row pairs
+    for (int e = tid; e < ntok * np; e += kThreads) {
+        const int t = e / np, p = e - t * np;
+        const int n = 2 * p;
+        float s0 = 0.f, s1 = 0.f;
         for (int i = 0; i < ell; ++i) {
-            const __half *gi = gam_s + i * ldg + kl;
-            uint32_t out[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const __half2 h = __floats2half2_rn(__half2float(gi[j]) * xa[j], __half2float(gi[16 + j]) * xb[j]);
-                out[j] = *reinterpret_cast<const uint32_t *>(&h);
-            }
-            uint4 *dst = reinterpret_cast<uint4 *>(act + (t * ell + i) * lda + 32 * g + 16 * q);
-            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-            dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+            s0 += __half2float(alp[i * lda_al + n]) * tile[n * ldt + t * ell + i];
+            s1 += __half2float(alp[i * lda_al + n + 1]) * tile[(n + 1) * ldt + t * ell + i];
+        }
+        if (accumulate) {
+            s0 += __bfloat162float(yst[t * ldyst + n]);
+            if (n + 1 < nrows) s1 += __bfloat162float(yst[t * ldyst + n + 1]);
+        }
+        __nv_bfloat16 *yp = y + size_t(t) * ldy + row_base + n;
+        if (pairs_ok && n + 1 < nrows) {
+            *reinterpret_cast<__nv_bfloat162 *>(yp) = __floats2bfloat162_rn(s0, s1);
+        } else {
+            yp[0] = __float2bfloat16_rn(s0);
+            if (n + 1 < nrows) yp[1] = __float2bfloat16_rn(s1);
         }
     }
 }
 
-// gamma of a K slice -> shared memory (physical order), zero past kvalid.
-__device__ __forceinline__ void load_gamma(__half *gam_s, int ldg, const __half *gamma, int K, int k0, int ell,
-                                           int kvalid, int klen, int tid, int nthr) {
-    if (kvalid > 0) copy_rows_async(gam_s, ldg * 2, gamma + k0, size_t(K) * 2, ell, kvalid * 2, tid, nthr);
-    const int tail = klen - kvalid;
-    if (tail > 0) {
-        for (int e = tid; e < ell * tail; e += nthr) {
-            const int i = e / tail;
-            gam_s[i * ldg + kvalid + (e - i * tail)] = __float2half_rn(0.f);
-        }
-    }
-}
+// ============================================================ fused kernel
 
-// ============================================================ two-stage kernel
-
-struct StageSmem {
-    size_t act, gam, bits, sc, yst, red, total;
+struct FusedSmem {
+    size_t gam, b2, beta, b1, alp, red, slots, vs, yst, tile, total;
 };
 
-__host__ __device__ inline StageSmem stage_smem(int CPAD, int RB, int Wc, int ell, bool stage1, bool acc) {
-    StageSmem L;
+__host__ __device__ inline int fused_g1(int R, int RBW) { return ((R + 15) / 16 + RBW - 1) / RBW; }
+__host__ __device__ inline int fused_kp(int G1) { return G1 >= kWarps ? 1 : kWarps / G1; }
+
+__host__ __device__ inline FusedSmem fused_smem(int CPAD, int RBW, int Wc, int R, int RW, int ell, int C, bool acc) {
+    const int G1 = fused_g1(R, RBW), R1 = 16 * RBW * G1, R2 = (R + 31) & ~31, Kw2 = R2 / 32;
+    const int KP = fused_kp(G1);
+    FusedSmem L;
     size_t o = 0;
-    L.act = o;
-    o += align16(size_t(CPAD) * lda_for(Wc) * 2);
     L.gam = o;
-    if (stage1) o += align16(size_t(ell) * 32 * Wc * 2);
-    L.bits = o;
-    o += align16(size_t(16) * RB * ldws_for(Wc) * 4);
-    L.sc = o;
-    o += align16(size_t(ell) * 16 * RB * 2);
-    L.yst = o;
-    if (!stage1 && acc) o += align16(size_t(CPAD) * 16 * RB * 2);
+    o += align16(size_t(ell) * 32 * Wc * 2);
+    L.b2 = o;
+    o += align16(size_t(R1) * ldws_for(Wc) * 4);
+    L.beta = o;
+    o += align16(size_t(ell) * R2 * 2);
+    L.b1 = o;
+    o += align16(size_t(RW) * ldws_for(Kw2) * 4);
+    L.alp = o;
+    o += align16(size_t(ell) * RW * 2);
     L.red = o;
-    o += size_t(kWarps) * 16 * (CPAD + 4) * 4;
+    o += align16(size_t(KP) * R1 * CPAD * 4);
+    L.slots = o;
+    o += align16(size_t(C) * R1 * CPAD * 4);
+    L.vs = o;
+    o += align16(size_t(CPAD) * (R2 + 8) * 2);
+    L.yst = o;
+    if (acc) o += align16(size_t(CPAD) * RW * 2);
+    L.tile = o;
+    if (ell == 3) o += size_t(RW) * (CPAD + 4) * 4;
     L.total = o;
     return L;
 }
 
-template <int CT, int STAGE, bool SEG>
-__global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
+template <int CT, int RBW, bool SEG>
+__global__ void __launch_bounds__(kThreads) dec_fused_kernel(const FusedArgs a) {
     constexpr int CPAD = 8 * CT;
-    constexpr int RED_LD = CPAD + 4;
+    constexpr int C4 = CPAD / 4;
+    constexpr int NWB = words_per_batch<CT>();
     extern __shared__ __align__(128) unsigned char smem[];
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int KS = a.KS, RB = a.RB, Wc = a.Wc;
-    const int kc = (KS > 1) ? static_cast<int>(cluster_ctarank()) : 0;
-    const int row0 = (blockIdx.x / KS) * RB * 16;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, c = lane & 3;
+    const int C = a.C;
+    const int rank = (C > 1) ? static_cast<int>(cluster_ctarank()) : 0;
     const int ell = a.ell;
-    const int rows_cta = 16 * RB;
+    const int N = a.N, M = a.M, R = a.R;
 
-    // ---- which factors and which tokens
+    const uint32_t *B1 = a.B1, *B2 = a.B2;
+    int ldw1 = a.ldw1, ldw2 = a.ldw2;
+    const __half *alpha = a.alpha, *beta = a.beta, *gamma = a.gamma;
+    int t0 = 0, Tseg = a.T;
+    if constexpr (SEG) {
+        pdl_wait();  // the routing table may come from the previous kernel
+        const int s = blockIdx.y;
+        const int o0 = a.seg_off[s], o1 = a.seg_off[s + 1], ad = a.seg_ad[s];
+        if (o0 < 0 || o1 < o0 || o1 > a.T || ad < 0 || ad >= a.n_adapters) {
+            if (tid == 0 && blockIdx.x == 0) record_status(a.status, DBF_ERR_DEVICE_ARG);
+            return;  // uniform over the cluster: every CTA of it reads the same entry
+        }
+        t0 = o0;
+        Tseg = o1 - o0;
+        const dbf_factors f = a.adapters[ad];
+        B1 = f.B1;
+        B2 = f.B2;
+        ldw1 = f.ldw1;
+        ldw2 = f.ldw2;
+        alpha = reinterpret_cast<const __half *>(f.alpha);
+        beta = reinterpret_cast<const __half *>(f.beta);
+        gamma = reinterpret_cast<const __half *>(f.gamma);
+        if (Tseg == 0) return;
+    }
+
+    const int G1 = fused_g1(R, RBW);
+    const int R1 = 16 * RBW * G1, R2 = (R + 31) & ~31;
+    const int Kw1 = (M + 31) >> 5, Kw2 = R2 >> 5;
+    const int KP = fused_kp(G1);
+    const int Wc = a.Wc, RW = a.RW;
+    const bool acc_mode = a.accumulate != 0;
+    const FusedSmem L = fused_smem(CPAD, RBW, Wc, R, RW, ell, C, acc_mode);
+    __half *gam_s = reinterpret_cast<__half *>(smem + L.gam);
+    uint32_t *b2_s = reinterpret_cast<uint32_t *>(smem + L.b2);
+    __half *beta_s = reinterpret_cast<__half *>(smem + L.beta);
+    uint32_t *b1_s = reinterpret_cast<uint32_t *>(smem + L.b1);
+    __half *alp_s = reinterpret_cast<__half *>(smem + L.alp);
+    float *red = reinterpret_cast<float *>(smem + L.red);
+    float *slots = reinterpret_cast<float *>(smem + L.slots);
+    __half *vs = reinterpret_cast<__half *>(smem + L.vs);
+    __nv_bfloat16 *yst = reinterpret_cast<__nv_bfloat16 *>(smem + L.yst);
+    float *tile = reinterpret_cast<float *>(smem + L.tile);
+
+    const int ldb2 = ldws_for(Wc), ldb1 = ldws_for(Kw2);
+    const int ldv = R2 + 8, ldt = CPAD + 4;
+    const int w0 = rank * Wc;
+    const int Wslice = max(0, min(Wc, Kw1 - w0));
+    const int kvalid = max(0, min(32 * Wslice, M - 32 * w0));
+    const int row_base = blockIdx.x * RW;  // first stage-2 output row of this CTA
+    const int nrows2 = max(0, min(RW, N - row_base));
+
+    // ---- 1. inputs no earlier kernel writes: signs and scales
+    copy_rows_async(b2_s, ldb2 * 4, B2 + w0, size_t(ldw2) * 4, R, Wslice * 4, tid, kThreads);
+    zero_rows(b2_s + R * ldb2, ldb2 * 4, R1 - R, Wslice * 4, tid, kThreads);
+    if (kvalid > 0) copy_rows_async(gam_s, 64 * Wc, gamma + 32 * w0, size_t(M) * 2, ell, kvalid * 2, tid, kThreads);
+    for (int e = tid; e < ell * (32 * Wc - kvalid); e += kThreads) {
+        const int i = e / (32 * Wc - kvalid);
+        gam_s[i * 32 * Wc + kvalid + (e - i * (32 * Wc - kvalid))] = __float2half_rn(0.f);
+    }
+    copy_rows_async(beta_s, R2 * 2, beta, size_t(R) * 2, ell, R * 2, tid, kThreads);
+    for (int e = tid; e < ell * (R2 - R); e += kThreads) {
+        const int i = e / (R2 - R);
+        beta_s[i * R2 + R + (e - i * (R2 - R))] = __float2half_rn(0.f);
+    }
+    copy_rows_async(b1_s, ldb1 * 4, B1 + size_t(row_base) * ldw1, size_t(ldw1) * 4, nrows2, Kw2 * 4, tid, kThreads);
+    zero_rows(b1_s + nrows2 * ldb1, ldb1 * 4, RW - nrows2, Kw2 * 4, tid, kThreads);
+    copy_rows_async(alp_s, RW * 2, alpha + row_base, size_t(N) * 2, ell, nrows2 * 2, tid, kThreads);
+    cp_async_commit();
+    if (C > 1) cluster_arrive_relaxed();  // matched by the wait before the first push
+    pdl_trigger();
+    if constexpr (!SEG) pdl_wait();
+
+    // this warp's stage-1 item: row group gr, K part kp, words [wb, we) of the slice
+    const bool has1 = warp < G1 * KP;
+    const int gr = warp % G1, kp = warp / G1;
+    const int Wp = (Wslice + KP - 1) / KP;
+    const int wb = min(Wslice, kp * Wp), we = has1 ? min(Wslice, wb + Wp) : wb;
+    // the lane's activation column in each column tile: token, term
+    int ctok[CT], cterm[CT];
+#pragma unroll
+    for (int ct = 0; ct < CT; ++ct) {
+        const int col = 8 * ct + g;
+        ctok[ct] = col / ell;
+        cterm[ct] = col - ctok[ct] * ell;
+    }
+    // the thread's columns in the reduction phases (the stride is a multiple of C4)
+    const int c4 = tid % C4;
+    int term4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) term4[j] = (4 * c4 + j) % ell;
+
+    const int tpc = CPAD / ell;  // whole tokens per column chunk
+    const int nchunks = (Tseg + tpc - 1) / tpc;
+    const bool xvec = ((M & 7) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0);
+    const bool pairs_ok = ((N & 1) == 0);
+    const uint32_t red_addr = smem_u32(red), slots_addr = smem_u32(slots), tile_addr = smem_u32(tile);
+    const int RB2 = RW / 16;
+
+    for (int chunk = 0; chunk < nchunks; ++chunk) {
+        const int tc0 = chunk * tpc;
+        const int ntok = min(tpc, Tseg - tc0);
+        const int ncol = ntok * ell;
+        if (chunk > 0 && C > 1) cluster_sync_all();  // peers finished reading the previous chunk's slots
+        const __nv_bfloat16 *xc = a.x + size_t(t0 + tc0) * M;
+
+        // ---- 2. old y by cp.async; the first batch of x straight into registers
+        if (acc_mode)
+            copy_rows_dep(yst, RW * 2, a.y + size_t(t0 + tc0) * N + row_base, size_t(N) * 2, ntok, nrows2 * 2,
+                          tid, kThreads);
+        cp_async_commit();
+        uint4 xr[NWB][CT];
+        auto load_batch = [&](int wbat) {
+#pragma unroll
+            for (int w = 0; w < NWB; ++w)
+#pragma unroll
+                for (int ct = 0; ct < CT; ++ct) {
+                    const int col = 8 * ct + g;
+                    if (wbat + w < we && col < ncol)
+                        xr[w][ct] = load_x8(xc + size_t(ctok[ct]) * M, 32 * (w0 + wbat + w) + 8 * c, M, xvec);
+                    else
+                        xr[w][ct] = make_uint4(0u, 0u, 0u, 0u);
+                }
+        };
+        load_batch(wb);
+        cp_async_wait_all();
+        __syncthreads();  // signs, scales and the old y are in shared memory
+        if (chunk == 0 && C > 1) cluster_wait();  // every CTA of the cluster has started
+
+        // ---- 3. stage 1 on this warp's words: x pairs from registers, signs from shared memory
+        if (has1) {
+            float acc[RBW][CT][4];
+#pragma unroll
+            for (int rb = 0; rb < RBW; ++rb) zero_acc<CT>(acc[rb]);
+            for (int wbat = wb; wbat < we; wbat += NWB) {
+                if (wbat != wb) load_batch(wbat);
+#pragma unroll
+                for (int w = 0; w < NWB; ++w) {
+                    const int wl = wbat + w;
+                    if (wl >= we) break;
+                    uint32_t bx[CT][4];
+#pragma unroll
+                    for (int ct = 0; ct < CT; ++ct) {
+                        const uint4 gv = *reinterpret_cast<const uint4 *>(gam_s + cterm[ct] * 32 * Wc + 32 * wl + 8 * c);
+                        x_pairs(xr[w][ct], gv, bx[ct]);
+                    }
+#pragma unroll
+                    for (int rb = 0; rb < RBW; ++rb) {
+                        const int r0 = 16 * (gr * RBW + rb) + g;
+                        uint32_t pa[4], pv[4];
+                        sign_pairs8(b2_s[r0 * ldb2 + wl], c, pa);
+                        sign_pairs8(b2_s[(r0 + 8) * ldb2 + wl], c, pv);
+#pragma unroll
+                        for (int ct = 0; ct < CT; ++ct) mma_word8(acc[rb][ct], pa, pv, bx[ct]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int rb = 0; rb < RBW; ++rb)
+                put_frag<CT>(red_addr + 4u * static_cast<uint32_t>((kp * R1 + 16 * (gr * RBW + rb)) * CPAD), CPAD,
+                             acc[rb], lane, false, 0);
+        }
+        __syncthreads();
+
+        // ---- 4. sum the K parts, push the CTA's partial u into slot `rank` of every CTA
+        for (int e = tid; e < R1 * C4; e += kThreads) {
+            const int r = e / C4;
+            float4 u = *reinterpret_cast<const float4 *>(red + r * CPAD + 4 * c4);
+            for (int q = 1; q < KP; ++q) add4(u, *reinterpret_cast<const float4 *>(red + (q * R1 + r) * CPAD + 4 * c4));
+            const uint32_t off = 4u * static_cast<uint32_t>((rank * R1 + r) * CPAD + 4 * c4);
+            if (C > 1) {
+                for (int q = 0; q < C; ++q) push_float4(slots_addr + off, u, static_cast<uint32_t>(q));
+            } else {
+                *reinterpret_cast<float4 *>(slots + off / 4) = u;
+            }
+        }
+        if (C > 1)
+            cluster_sync_all();  // every slot of every CTA is filled
+        else
+            __syncthreads();
+
+        // ---- 5. u = sum of the slots in rank order, v = beta * u (fp16, perm8 order)
+        for (int e = tid; e < R2 * C4; e += kThreads) {
+            const int r = e / C4;
+            float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < R1)
+                for (int q = 0; q < C; ++q) add4(u, *reinterpret_cast<const float4 *>(slots + (q * R1 + r) * CPAD + 4 * c4));
+            const float uu[4] = {u.x, u.y, u.z, u.w};
+            const int pos = perm8_pos(r);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                vs[(4 * c4 + j) * ldv + pos] = __float2half_rn(__half2float(beta_s[term4[j] * R2 + r]) * uu[j]);
+        }
+        __syncthreads();
+
+        // ---- 6. stage 2 per (row block, column tile); y straight from the fragment
+        for (int it = warp; it < RB2 * CT; it += kWarps) {
+            const int rb2 = it % RB2, ct = it / RB2;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const int n0 = 16 * rb2 + g;
+            for (int w = 0; w < Kw2; ++w) {
+                const uint4 bv = *reinterpret_cast<const uint4 *>(vs + (8 * ct + g) * ldv + 32 * w + 8 * c);
+                const uint32_t b[4] = {bv.x, bv.y, bv.z, bv.w};
+                uint32_t pa[4], pv[4];
+                sign_pairs8(b1_s[n0 * ldb1 + w], c, pa);
+                sign_pairs8(b1_s[(n0 + 8) * ldb1 + w], c, pv);
+                mma_word8(d, pa, pv, b);
+            }
+            if (ell == 3) {
+                float dd[1][4] = {{d[0], d[1], d[2], d[3]}};
+                put_frag<1>(tile_addr + 4u * static_cast<uint32_t>(16 * rb2 * ldt + 8 * ct), ldt, dd, lane, false, 0);
+                continue;
+            }
+            // rows n0 (d[0], d[1]) and n0 + 8 (d[2], d[3]); columns 8ct + 2c, 8ct + 2c + 1
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int nl = n0 + 8 * hh;
+                const float d0 = d[2 * hh], d1 = d[2 * hh + 1];
+                const bool row_ok = nl < nrows2;
+                __nv_bfloat16 *yrow = a.y + size_t(t0 + tc0) * N + row_base + nl;
+                if (ell == 1) {
+                    const float al = row_ok ? __half2float(alp_s[nl]) : 0.f;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = 8 * ct + 2 * c + e;
+                        if (row_ok && t < ntok) {
+                            float o = al * (e ? d1 : d0);
+                            if (acc_mode) o += __bfloat162float(yst[t * RW + nl]);
+                            yrow[size_t(t) * N] = __float2bfloat16_rn(o);
+                        }
+                    }
+                } else if (ell == 2) {
+                    const int t = 4 * ct + c;
+                    if (row_ok && t < ntok) {
+                        float o = __half2float(alp_s[nl]) * d0 + __half2float(alp_s[RW + nl]) * d1;
+                        if (acc_mode) o += __bfloat162float(yst[t * RW + nl]);
+                        yrow[size_t(t) * N] = __float2bfloat16_rn(o);
+                    }
+                } else {  // ell == 4: terms 0,1 in lane c even, 2,3 in lane c odd
+                    const int i0 = 2 * (c & 1);
+                    float o = row_ok ? __half2float(alp_s[i0 * RW + nl]) * d0 + __half2float(alp_s[(i0 + 1) * RW + nl]) * d1
+                                     : 0.f;
+                    o += __shfl_xor_sync(0xffffffffu, o, 1);
+                    const int t = 2 * ct + (c >> 1);
+                    if ((c & 1) == 0 && row_ok && t < ntok) {
+                        if (acc_mode) o += __bfloat162float(yst[t * RW + nl]);
+                        yrow[size_t(t) * N] = __float2bfloat16_rn(o);
+                    }
+                }
+            }
+        }
+        if (ell == 3) {
+            __syncthreads();
+            epilogue_tile(tile, ldt, alp_s, RW, ell, ntok, nrows2, row_base, a.y + size_t(t0 + tc0) * N, size_t(N), yst,
+                          RW, acc_mode, pairs_ok, tid);
+        }
+        __syncthreads();  // vs / red / slots / yst / tile are reused by the next chunk
+    }
+}
+
+// ============================================================== stage kernel
+//
+// One stage of the two-stage decode.  A CTA owns 16*RBW weight rows
+// [row0, row0 + 16*RBW) and one K slice (the KS CTAs of a cluster split the
+// packed words); its 8 warps split the slice again.  Warp partials are summed
+// in shared memory; with KS > 1 each CTA then pushes the rows owned by rank q
+// (16*RBW/KS consecutive rows) into slot `rank` of CTA q, which sums the KS
+// slots and writes the outputs of its rows.
+
+struct StageSmem {
+    size_t gam, bits, sc, yst, red, slots, total;
+};
+
+__host__ __device__ inline StageSmem stage_smem(int CPAD, int RBW, int KS, int Wc, int ell, bool stage1, bool acc) {
+    const int RWS = 16 * RBW;
+    StageSmem L;
+    size_t o = 0;
+    L.gam = o;
+    if (stage1) o += align16(size_t(ell) * 32 * Wc * 2);
+    L.bits = o;
+    o += align16(size_t(RWS) * ldws_for(Wc) * 4);
+    L.sc = o;
+    o += align16(size_t(ell) * RWS * 2);
+    L.yst = o;
+    if (!stage1 && acc) o += align16(size_t(CPAD) * RWS * 2);
+    L.red = o;
+    o += align16(size_t(kWarps) * RWS * CPAD * 4);
+    L.slots = o;
+    if (KS > 1) o += align16(size_t(KS) * (RWS / KS) * CPAD * 4);
+    L.total = o;
+    return L;
+}
+
+template <int CT, int RBW, int STAGE, bool SEG>
+__global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
+    constexpr int CPAD = 8 * CT;
+    constexpr int C4 = CPAD / 4;
+    constexpr int RWS = 16 * RBW;
+    constexpr int NWB = words_per_batch<CT>();
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, c = lane & 3;
+    const int KS = a.KS, Wc = a.Wc;
+    const int rank = (KS > 1) ? static_cast<int>(cluster_ctarank()) : 0;
+    const int row0 = (blockIdx.x / KS) * RWS;
+    const int ell = a.ell;
+
     const uint32_t *bits = a.bits;
     int ldw = a.ldw;
     const __half *scale_in = (STAGE == 1) ? a.gamma : nullptr;
@@ -242,7 +609,7 @@ __global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
         const int s = blockIdx.y;
         const int o0 = a.seg_off[s], o1 = a.seg_off[s + 1], ad = a.seg_ad[s];
         if (o0 < 0 || o1 < o0 || o1 > a.T || ad < 0 || ad >= a.n_adapters) {
-            if (tid == 0 && kc == 0) record_status(a.status, DBF_ERR_DEVICE_ARG);
+            if (tid == 0 && blockIdx.x == 0) record_status(a.status, DBF_ERR_DEVICE_ARG);
             return;  // uniform over the cluster: every CTA of it reads the same entry
         }
         t0 = o0;
@@ -261,375 +628,216 @@ __global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
         if (Tseg == 0) return;
     }
 
-    const StageSmem L = stage_smem(CPAD, RB, Wc, ell, STAGE == 1, a.accumulate != 0);
-    const int w0 = kc * Wc;
+    const StageSmem L = stage_smem(CPAD, RBW, KS, Wc, ell, STAGE == 1, a.accumulate != 0);
+    const int w0 = rank * Wc;
     const int Wslice = max(0, min(Wc, a.Kw - w0));
-    const int lda_s = lda_for(Wc);
+    const int kvalid = max(0, min(32 * Wslice, a.K - 32 * w0));
     const int ldws = ldws_for(Wc);
-    const int kvalid = max(0, min(32 * Wslice, a.K - 32 * w0));  // valid elements of this K slice
-    const int nr = max(0, min(rows_cta, a.rows - row0));          // weight rows that exist
-    __half *act_s = reinterpret_cast<__half *>(smem + L.act);
+    const int nr = max(0, min(RWS, a.rows - row0));  // weight rows that exist
+    const int ROWN = RWS / KS;                       // rows each CTA of the cluster finishes
     __half *gam_s = reinterpret_cast<__half *>(smem + L.gam);
     uint32_t *bits_s = reinterpret_cast<uint32_t *>(smem + L.bits);
     __half *sc_s = reinterpret_cast<__half *>(smem + L.sc);
     __nv_bfloat16 *yst = reinterpret_cast<__nv_bfloat16 *>(smem + L.yst);
-    float *red_s = reinterpret_cast<float *>(smem + L.red);
+    float *red = reinterpret_cast<float *>(smem + L.red);
+    float *slots = reinterpret_cast<float *>(smem + L.slots);
 
     // ---- 1. inputs no earlier kernel writes: packed signs and scales
     copy_rows_async(bits_s, ldws * 4, bits + size_t(row0) * ldw + w0, size_t(ldw) * 4, nr, Wslice * 4, tid,
                     kThreads);
-    zero_rows(bits_s + nr * ldws, ldws * 4, rows_cta - nr, Wslice * 4, tid, kThreads);
-    // output-side scale of this CTA's rows: beta (stage 1) or alpha (stage 2)
-    copy_rows_async(sc_s, rows_cta * 2, scale_out + row0, size_t(a.rows) * 2, ell, nr * 2, tid, kThreads);
-    if (STAGE == 1) load_gamma(gam_s, 32 * Wc, scale_in, a.K, 32 * w0, ell, kvalid, 32 * Wslice, tid, kThreads);
-    cp_async_commit();
-    pdl_trigger();
-    if constexpr (!SEG) pdl_wait();
-
-    const int tpc = CPAD / ell;  // whole tokens per column chunk
-    const int nchunks = (Tseg + tpc - 1) / tpc;
-    const bool xvec = ((a.ldx & 7) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0);
-    const uint32_t act_base =
-        smem_u32(act_s) + static_cast<uint32_t>(((lane & 7) * lda_s + 8 * (lane >> 3)) * 2);
-
-    for (int chunk = 0; chunk < nchunks; ++chunk) {
-        const int tc0 = chunk * tpc;
-        const int ntok = min(tpc, Tseg - tc0);
-        const int ncol = ntok * ell;
-
-        // ---- 2. activations (written by the previous kernel) -> shared memory
-        if constexpr (STAGE == 2) {
-            copy_rows_async(act_s, lda_s * 2, a.V + size_t(t0 + tc0) * ell * a.ldv + 32 * w0, size_t(a.ldv) * 2,
-                            ncol, Wslice * 64, tid, kThreads);
-            if (a.accumulate)
-                copy_rows_async(yst, rows_cta * 2, a.y + size_t(t0 + tc0) * a.ldy + row0, size_t(a.ldy) * 2, ntok,
-                                nr * 2, tid, kThreads);
-        }
-        cp_async_commit();
-        zero_rows(act_s + ncol * lda_s, lda_s * 2, CPAD - ncol, Wslice * 64, tid, kThreads);
-        cp_async_wait_all();
-        __syncthreads();  // gamma in place (stage 1), V / y staged (stage 2)
-        if constexpr (STAGE == 1) {
-            load_x_act(act_s, lda_s, a.x + size_t(t0 + tc0) * a.ldx + 32 * w0, size_t(a.ldx), ntok, gam_s, 32 * Wc,
-                       ell, Wslice, kvalid, xvec, tid, kThreads);
-            __syncthreads();
-        }
-
-        // ---- 3. tensor-core sign contraction
-        const int KP = kWarps / RB;
-        const int rb = warp % RB, kp = warp / RB;
-        const int Wp = (Wslice + KP - 1) / KP;
-        const int wb = min(Wslice, kp * Wp), we = min(Wslice, wb + Wp);
-        float acc[CT][4];
-#pragma unroll
-        for (int ct = 0; ct < CT; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
-        mma_rows<CT>(bits_s + (rb * 16 + (lane >> 2)) * ldws, ldws, act_base, lda_s, wb, we, acc, lane);
-
-        // ---- 4. per-warp partials -> shared memory, then fixed-order sum over K parts
-        store_tile<CT>(red_s + warp * 16 * RED_LD, RED_LD, acc, lane);
-        __syncthreads();
-        if (KP > 1) {
-            for (int e = tid; e < RB * 16 * RED_LD; e += kThreads) {
-                const int r = e / (16 * RED_LD), off = e - r * 16 * RED_LD;
-                float s = red_s[r * 16 * RED_LD + off];
-                for (int p = 1; p < KP; ++p) s += red_s[(p * RB + r) * 16 * RED_LD + off];
-                red_s[r * 16 * RED_LD + off] = s;
-            }
-            __syncthreads();
-        }
-
-        // ---- 5. cluster reduction (fixed order of ranks) and epilogue
-        if (KS > 1) cluster_sync_all();
-        const int per = (rows_cta + KS - 1) / KS;
-        const int rbeg = kc * per, rend = min(rows_cta, rbeg + per);
-        const int nrr = max(0, rend - rbeg);
-        const uint32_t red_addr = smem_u32(red_s);
-
-        auto reduced = [&](int rl, int col) -> float {
-            const int off = rl * RED_LD + col;
-            if (KS == 1) return red_s[off];
-            float s = 0.f;
-            for (int q = 0; q < KS; ++q) s += ld_dsmem_f32(mapa_shared(red_addr + 4u * off, q));
-            return s;
-        };
-
-        if constexpr (STAGE == 1) {
-            // V[(t0+tc0)*ell + col][perm(r)] = fp16(beta_i[r] * u), zero for r >= R
-            const size_t vrow0 = size_t(t0 + tc0) * ell;
-            for (int e = tid; e < ncol * nrr; e += kThreads) {
-                const int col = e / nrr, rl = rbeg + (e - col * nrr);
-                const int r = row0 + rl;
-                if (r >= a.rows_cover) continue;
-                const float u = reduced(rl, col);
-                const int i = col % ell;
-                const float v = (r < a.rows) ? __half2float(sc_s[i * rows_cta + rl]) * u : 0.f;
-                a.V[(vrow0 + col) * a.ldv + perm32_pos(r)] = __float2half_rn(v);
-            }
-        } else {
-            // y[t][n] = bf16(sum_i alpha_i[n] * w[t*ell+i] (+ y))
-            for (int e = tid; e < ntok * nrr; e += kThreads) {
-                const int t = e / nrr, rl = rbeg + (e - t * nrr);
-                const int n = row0 + rl;
-                if (n >= a.rows) continue;
-                float s = 0.f;
-                for (int i = 0; i < ell; ++i) s += __half2float(sc_s[i * rows_cta + rl]) * reduced(rl, t * ell + i);
-                if (a.accumulate) s += __bfloat162float(yst[t * rows_cta + rl]);
-                a.y[size_t(t0 + tc0 + t) * a.ldy + n] = __float2bfloat16_rn(s);
-            }
-        }
-        if (KS > 1) cluster_sync_all();  // peers may still read our partials
-        __syncthreads();                 // act_s / red_s are reused by the next chunk
+    zero_rows(bits_s + nr * ldws, ldws * 4, RWS - nr, Wslice * 4, tid, kThreads);
+    copy_rows_async(sc_s, RWS * 2, scale_out + row0, size_t(a.rows) * 2, ell, nr * 2, tid, kThreads);
+    for (int e = tid; e < ell * (RWS - nr); e += kThreads) {
+        const int i = e / (RWS - nr);
+        sc_s[i * RWS + nr + (e - i * (RWS - nr))] = __float2half_rn(0.f);
     }
-}
-
-// ============================================================== fused kernel
-
-constexpr int kFusedThreads = 512;
-constexpr int kFusedWarps = kFusedThreads / 32;
-
-struct FusedSmem {
-    size_t act1, gam, b2, red1, slots, act2, beta, b1, alp, yst, tile, total;
-};
-
-__host__ __device__ inline int fused_kp1(int RB1) { return RB1 >= kFusedWarps ? 1 : kFusedWarps / RB1; }
-
-__host__ __device__ inline FusedSmem fused_smem(int CPAD, int Wc1, int R1, int Kw2, int RW, int ell, int KS,
-                                                bool acc) {
-    FusedSmem L;
-    const int RB1 = R1 / 16;
-    const int KP1 = fused_kp1(RB1);
-    size_t o = 0;
-    L.act1 = o;
-    o += align16(size_t(CPAD) * lda_for(Wc1) * 2);
-    L.gam = o;
-    o += align16(size_t(ell) * 32 * Wc1 * 2);
-    L.b2 = o;
-    o += align16(size_t(R1) * ldws_for(Wc1) * 4);
-    L.red1 = o;
-    o += align16(size_t(RB1) * KP1 * 16 * (CPAD + 4) * 4);
-    L.slots = o;
-    o += align16(size_t(KS) * R1 * CPAD * 4);
-    L.act2 = o;
-    o += align16(size_t(CPAD) * lda_for(Kw2) * 2);
-    L.beta = o;
-    o += align16(size_t(ell) * R1 * 2);
-    L.b1 = o;
-    o += align16(size_t(RW) * ldws_for(Kw2) * 4);
-    L.alp = o;
-    o += align16(size_t(ell) * RW * 2);
-    L.yst = o;
-    if (acc) o += align16(size_t(CPAD) * RW * 2);
-    L.tile = o;
-    o += size_t(kFusedWarps) * 16 * (CPAD + 4) * 4;
-    L.total = o;
-    return L;
-}
-
-template <int CT, bool SEG>
-__global__ void __launch_bounds__(kFusedThreads) dec_fused_kernel(const FusedArgs a) {
-    constexpr int CPAD = 8 * CT;
-    constexpr int RED_LD = CPAD + 4;
-    extern __shared__ __align__(128) unsigned char smem[];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int KS = a.KS;
-    const int kc = (KS > 1) ? static_cast<int>(cluster_ctarank()) : 0;
-    const int ell = a.ell;
-    const int N = a.N, M = a.M, R = a.R;
-    const int R1 = (R + 31) & ~31;  // stage-1 rows covered (activation positions up to round_up(R, 32))
-    const int Kw1 = (M + 31) / 32, Kw2 = R1 / 32;
-    const int Wc1 = a.Wc1;
-    const int RW = 16 * a.RB2;
-    const int row_base = blockIdx.x * RW;  // first stage-2 output row of this CTA
-
-    const uint32_t *B1 = a.B1, *B2 = a.B2;
-    int ldw1 = a.ldw1, ldw2 = a.ldw2;
-    const __half *alpha = a.alpha, *beta = a.beta, *gamma = a.gamma;
-    int t0 = 0, Tseg = a.T;
-    if constexpr (SEG) {
-        pdl_wait();
-        const int s = blockIdx.y;
-        const int o0 = a.seg_off[s], o1 = a.seg_off[s + 1], ad = a.seg_ad[s];
-        if (o0 < 0 || o1 < o0 || o1 > a.T || ad < 0 || ad >= a.n_adapters) {
-            if (tid == 0 && blockIdx.x == 0) record_status(a.status, DBF_ERR_DEVICE_ARG);
-            return;  // uniform over the cluster
+    if (STAGE == 1) {
+        if (kvalid > 0)
+            copy_rows_async(gam_s, 64 * Wc, scale_in + 32 * w0, size_t(a.K) * 2, ell, kvalid * 2, tid, kThreads);
+        for (int e = tid; e < ell * (32 * Wc - kvalid); e += kThreads) {
+            const int i = e / (32 * Wc - kvalid);
+            gam_s[i * 32 * Wc + kvalid + (e - i * (32 * Wc - kvalid))] = __float2half_rn(0.f);
         }
-        t0 = o0;
-        Tseg = o1 - o0;
-        const dbf_factors f = a.adapters[ad];
-        B1 = f.B1;
-        B2 = f.B2;
-        ldw1 = f.ldw1;
-        ldw2 = f.ldw2;
-        alpha = reinterpret_cast<const __half *>(f.alpha);
-        beta = reinterpret_cast<const __half *>(f.beta);
-        gamma = reinterpret_cast<const __half *>(f.gamma);
-        if (Tseg == 0) return;
     }
-
-    const FusedSmem L = fused_smem(CPAD, Wc1, R1, Kw2, RW, ell, KS, a.accumulate != 0);
-    __half *act1 = reinterpret_cast<__half *>(smem + L.act1);
-    __half *gam_s = reinterpret_cast<__half *>(smem + L.gam);
-    uint32_t *b2_s = reinterpret_cast<uint32_t *>(smem + L.b2);
-    float *red1 = reinterpret_cast<float *>(smem + L.red1);
-    float *slots = reinterpret_cast<float *>(smem + L.slots);
-    __half *act2 = reinterpret_cast<__half *>(smem + L.act2);
-    __half *beta_s = reinterpret_cast<__half *>(smem + L.beta);
-    uint32_t *b1_s = reinterpret_cast<uint32_t *>(smem + L.b1);
-    __half *alp_s = reinterpret_cast<__half *>(smem + L.alp);
-    __nv_bfloat16 *yst = reinterpret_cast<__nv_bfloat16 *>(smem + L.yst);
-    float *tiles = reinterpret_cast<float *>(smem + L.tile);
-
-    const int lda1 = lda_for(Wc1), lda2 = lda_for(Kw2);
-    const int ldb2 = ldws_for(Wc1), ldb1 = ldws_for(Kw2);
-    const int w0 = kc * Wc1;
-    const int Wslice = max(0, min(Wc1, Kw1 - w0));
-    const int kvalid = max(0, min(32 * Wslice, M - 32 * w0));
-    const int nrows2 = max(0, min(RW, N - row_base));
-
-    // ---- 1. inputs no earlier kernel writes: signs and scales
-    copy_rows_async(b2_s, ldb2 * 4, B2 + w0, size_t(ldw2) * 4, R, Wslice * 4, tid, kFusedThreads);
-    zero_rows(b2_s + R * ldb2, ldb2 * 4, R1 - R, Wslice * 4, tid, kFusedThreads);
-    load_gamma(gam_s, 32 * Wc1, gamma, M, 32 * w0, ell, kvalid, 32 * Wslice, tid, kFusedThreads);
-    copy_rows_async(beta_s, R1 * 2, beta, size_t(R) * 2, ell, R * 2, tid, kFusedThreads);
-    copy_rows_async(b1_s, ldb1 * 4, B1 + size_t(row_base) * ldw1, size_t(ldw1) * 4, nrows2, Kw2 * 4, tid,
-                    kFusedThreads);
-    zero_rows(b1_s + nrows2 * ldb1, ldb1 * 4, RW - nrows2, Kw2 * 4, tid, kFusedThreads);
-    copy_rows_async(alp_s, RW * 2, alpha + row_base, size_t(N) * 2, ell, nrows2 * 2, tid, kFusedThreads);
     cp_async_commit();
     if (KS > 1) cluster_arrive_relaxed();  // matched by the wait before the first push
     pdl_trigger();
     if constexpr (!SEG) pdl_wait();
 
-    const int tpc = CPAD / ell;
+    // this warp's words of the slice
+    const int Wp = (Wslice + kWarps - 1) / kWarps;
+    const int wb = min(Wslice, warp * Wp), we = min(Wslice, wb + Wp);
+    int ctok[CT], cterm[CT];
+#pragma unroll
+    for (int ct = 0; ct < CT; ++ct) {
+        const int col = 8 * ct + g;
+        ctok[ct] = col / ell;
+        cterm[ct] = col - ctok[ct] * ell;
+    }
+    const int tpc = CPAD / ell;  // whole tokens per column chunk
     const int nchunks = (Tseg + tpc - 1) / tpc;
-    const int RB1 = R1 / 16;
-    const int KP1 = fused_kp1(RB1);
-    const int items1 = RB1 * KP1;
-    const bool xvec = ((M & 7) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0);
-    const uint32_t act1_base = smem_u32(act1) + static_cast<uint32_t>(((lane & 7) * lda1 + 8 * (lane >> 3)) * 2);
-    const uint32_t act2_base = smem_u32(act2) + static_cast<uint32_t>(((lane & 7) * lda2 + 8 * (lane >> 3)) * 2);
-    const uint32_t slots_addr = smem_u32(slots);
+    const bool xvec = ((a.ldx & 7) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0);
+    const uint32_t red_addr = smem_u32(red), slots_addr = smem_u32(slots);
+    const int c4 = tid % C4;
+    const int nsl = (KS > 1) ? KS : kWarps;      // partial slices summed in the epilogue
+    const float *part = (KS > 1) ? slots : red;  // [nsl][rows][CPAD]
+    const int prows = (KS > 1) ? ROWN : RWS;     // rows per slice
+    const int rown0 = (KS > 1) ? rank * ROWN : 0;
+    const bool pairs_ok = ((a.ldy & 1) == 0);
 
     for (int chunk = 0; chunk < nchunks; ++chunk) {
         const int tc0 = chunk * tpc;
         const int ntok = min(tpc, Tseg - tc0);
         const int ncol = ntok * ell;
-        if (chunk > 0 && KS > 1) cluster_sync_all();  // peers finished reading the previous chunk's slots
+        if (chunk > 0 && KS > 1) cluster_sync_all();  // owners finished reading the previous chunk's slots
 
-        // ---- 2. activations (and the old y of this CTA's rows)
-        if (a.accumulate)
-            copy_rows_async(yst, RW * 2, a.y + size_t(t0 + tc0) * N + row_base, size_t(N) * 2, ntok, nrows2 * 2,
-                            tid, kFusedThreads);
+        // ---- 2. the first batch of activations straight into registers
+        if (STAGE == 2 && a.accumulate)
+            copy_rows_dep(yst, RWS * 2, a.y + size_t(t0 + tc0) * a.ldy + row0, size_t(a.ldy) * 2, ntok, nr * 2, tid,
+                          kThreads);
         cp_async_commit();
-        zero_rows(act1 + ncol * lda1, lda1 * 2, CPAD - ncol, Wslice * 64, tid, kFusedThreads);
-        cp_async_wait_all();  // gamma must be in place for the conversion
-        __syncthreads();
-        load_x_act(act1, lda1, a.x + size_t(t0 + tc0) * M + 32 * w0, size_t(M), ntok, gam_s, 32 * Wc1, ell, Wslice,
-                   kvalid, xvec, tid, kFusedThreads);
-        __syncthreads();
-
-        // ---- 3. stage 1 on this CTA's K slice: items (row block, K part)
-        for (int it = warp; it < items1; it += kFusedWarps) {
-            const int rb = it % RB1, kp = it / RB1;
-            const int Wp = (Wslice + KP1 - 1) / KP1;
-            const int wb = min(Wslice, kp * Wp), we = min(Wslice, wb + Wp);
-            float acc[CT][4];
+        uint4 xr[NWB][CT];
+        auto load_batch = [&](int wbat) {
 #pragma unroll
-            for (int ct = 0; ct < CT; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
-            mma_rows<CT>(b2_s + (rb * 16 + (lane >> 2)) * ldb2, ldb2, act1_base, lda1, wb, we, acc, lane);
-            store_tile<CT>(red1 + it * 16 * RED_LD, RED_LD, acc, lane);
-        }
-        __syncthreads();
-
-        // ---- 4. sum the K parts (fixed order) and push this CTA's partial u
-        //         into slot kc of every CTA of the cluster
+            for (int w = 0; w < NWB; ++w)
+#pragma unroll
+                for (int ct = 0; ct < CT; ++ct) {
+                    const int col = 8 * ct + g;
+                    if (wbat + w < we && col < ncol) {
+                        if constexpr (STAGE == 1) {
+                            xr[w][ct] = load_x8(a.x + size_t(t0 + tc0 + ctok[ct]) * a.ldx,
+                                                32 * (w0 + wbat + w) + 8 * c, a.K, xvec);
+                        } else {
+                            xr[w][ct] = *reinterpret_cast<const uint4 *>(
+                                a.V + (size_t(t0 + tc0) * ell + col) * a.ldv + 32 * (w0 + wbat + w) + 8 * c);
+                        }
+                    } else {
+                        xr[w][ct] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+        };
+        load_batch(wb);
+        cp_async_wait_all();
+        __syncthreads();  // signs and scales are in shared memory
         if (chunk == 0 && KS > 1) cluster_wait();  // every CTA of the cluster has started
-        {
-            constexpr int C4 = CPAD / 4;
-            for (int e = tid; e < R1 * C4; e += kFusedThreads) {
-                const int r = e / C4, c4 = e - r * C4;
-                const int rb = r >> 4, r16 = r & 15;
-                float4 s = *reinterpret_cast<const float4 *>(red1 + (rb * 16 + r16) * RED_LD + 4 * c4);
-                for (int p = 1; p < KP1; ++p) {
-                    const float4 o =
-                        *reinterpret_cast<const float4 *>(red1 + ((p * RB1 + rb) * 16 + r16) * RED_LD + 4 * c4);
-                    s.x += o.x;
-                    s.y += o.y;
-                    s.z += o.z;
-                    s.w += o.w;
-                }
-                if (KS == 1) {
-                    *reinterpret_cast<float4 *>(slots + (r * CPAD + 4 * c4)) = s;
-                } else {
-                    const uint32_t off = 4u * static_cast<uint32_t>((kc * R1 + r) * CPAD + 4 * c4);
-                    for (int q = 0; q < KS; ++q)
-                        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                         mapa_shared(slots_addr + off, q)),
-                                     "f"(s.x), "f"(s.y), "f"(s.z), "f"(s.w)
-                                     : "memory");
-                }
-            }
-        }
-        if (KS > 1)
-            cluster_sync_all();  // every slot of every CTA is filled
-        else
-            __syncthreads();
 
-        // ---- 5. u = sum over ranks (fixed order), v = beta * u as fp16 in activation order
+        // ---- 3. tensor-core sign contraction over this warp's words
         {
-            constexpr int C4 = CPAD / 4;
-            for (int e = tid; e < R1 * C4; e += kFusedThreads) {
-                const int r = e / C4, c4 = e - r * C4;
-                float4 u = *reinterpret_cast<const float4 *>(slots + (r * CPAD + 4 * c4));
-                for (int q = 1; q < KS; ++q) {
-                    const float4 o = *reinterpret_cast<const float4 *>(slots + ((q * R1 + r) * CPAD + 4 * c4));
-                    u.x += o.x;
-                    u.y += o.y;
-                    u.z += o.z;
-                    u.w += o.w;
-                }
-                const float uu[4] = {u.x, u.y, u.z, u.w};
-                const int pos = perm32_pos(r);
+            float acc[RBW][CT][4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int col = 4 * c4 + j;
-                    const int i = col % ell;
-                    const float v = (r < R && col < ncol) ? __half2float(beta_s[i * R1 + r]) * uu[j] : 0.f;
-                    act2[col * lda2 + pos] = __float2half_rn(v);
+            for (int rb = 0; rb < RBW; ++rb) zero_acc<CT>(acc[rb]);
+            for (int wbat = wb; wbat < we; wbat += NWB) {
+                if (wbat != wb) load_batch(wbat);
+#pragma unroll
+                for (int w = 0; w < NWB; ++w) {
+                    const int wl = wbat + w;
+                    if (wl >= we) break;
+                    uint32_t bx[CT][4];
+#pragma unroll
+                    for (int ct = 0; ct < CT; ++ct) {
+                        if constexpr (STAGE == 1) {
+                            const uint4 gv =
+                                *reinterpret_cast<const uint4 *>(gam_s + cterm[ct] * 32 * Wc + 32 * wl + 8 * c);
+                            x_pairs(xr[w][ct], gv, bx[ct]);
+                        } else {
+                            bx[ct][0] = xr[w][ct].x;
+                            bx[ct][1] = xr[w][ct].y;
+                            bx[ct][2] = xr[w][ct].z;
+                            bx[ct][3] = xr[w][ct].w;
+                        }
+                    }
+#pragma unroll
+                    for (int rb = 0; rb < RBW; ++rb) {
+                        const int r0 = 16 * rb + g;
+                        uint32_t pa[4], pv[4];
+                        sign_pairs8(bits_s[r0 * ldws + wl], c, pa);
+                        sign_pairs8(bits_s[(r0 + 8) * ldws + wl], c, pv);
+#pragma unroll
+                        for (int ct = 0; ct < CT; ++ct) mma_word8(acc[rb][ct], pa, pv, bx[ct]);
+                    }
                 }
             }
+#pragma unroll
+            for (int rb = 0; rb < RBW; ++rb)
+                put_frag<CT>(red_addr + 4u * static_cast<uint32_t>((warp * RWS + 16 * rb) * CPAD), CPAD, acc[rb], lane,
+                             false, 0);
         }
         __syncthreads();
 
-        // ---- 6. stage 2 on this CTA's output rows, epilogue per warp
-        float *tile = tiles + warp * 16 * RED_LD;
-        for (int rb2 = warp; rb2 * 16 < nrows2; rb2 += kFusedWarps) {
-            float acc[CT][4];
-#pragma unroll
-            for (int ct = 0; ct < CT; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
-            mma_rows<CT>(b1_s + (rb2 * 16 + (lane >> 2)) * ldb1, ldb1, act2_base, lda2, 0, Kw2, acc, lane);
-            store_tile<CT>(tile, RED_LD, acc, lane);
-            __syncwarp();
-            for (int e = lane; e < ntok * 16; e += 32) {
-                const int t = e >> 4, r16 = e & 15;
-                const int rl = rb2 * 16 + r16;
-                if (rl >= nrows2) continue;
-                float s = 0.f;
-                for (int i = 0; i < ell; ++i) s += __half2float(alp_s[i * RW + rl]) * tile[r16 * RED_LD + t * ell + i];
-                if (a.accumulate) s += __bfloat162float(yst[t * RW + rl]);
-                a.y[size_t(t0 + tc0 + t) * N + row_base + rl] = __float2bfloat16_rn(s);
+        // ---- 4. cluster: sum the warp partials, push each owner's rows into its slot `rank`
+        if (KS > 1) {
+            for (int e = tid; e < RWS * C4; e += kThreads) {
+                const int r = e / C4;
+                float4 u = *reinterpret_cast<const float4 *>(red + r * CPAD + 4 * c4);
+                for (int q = 1; q < kWarps; ++q)
+                    add4(u, *reinterpret_cast<const float4 *>(red + (q * RWS + r) * CPAD + 4 * c4));
+                const int owner = r / ROWN, rl = r - owner * ROWN;
+                push_float4(slots_addr + 4u * static_cast<uint32_t>((rank * ROWN + rl) * CPAD + 4 * c4), u,
+                            static_cast<uint32_t>(owner));
             }
-            __syncwarp();
+            cluster_sync_all();
         }
-        __syncthreads();  // act1 / act2 / red1 are reused by the next chunk
+
+        // ---- 5. epilogue of this CTA's rows [rown0, rown0 + prows)
+        if constexpr (STAGE == 1) {
+            // V[(t0+tc0)*ell + col][perm8(r)]: pairs (r, r+4) of each 8-row group
+            const size_t vrow0 = size_t(t0 + tc0) * ell;
+            const int npairs = prows / 2;
+            for (int e = tid; e < ncol * npairs; e += kThreads) {
+                const int col = e / npairs, p = e - col * npairs;
+                const int rl = 8 * (p >> 2) + (p & 3);  // row inside the owned range, first of the pair
+                const int r = row0 + rown0 + rl;
+                if (r >= a.rows_out) continue;
+                float u0 = 0.f, u1 = 0.f;
+                for (int q = 0; q < nsl; ++q) {
+                    const float *b = part + size_t(q) * prows * CPAD;
+                    u0 += b[rl * CPAD + col];
+                    u1 += b[(rl + 4) * CPAD + col];
+                }
+                const int i = col % ell;
+                const float v0 = __half2float(sc_s[i * RWS + rown0 + rl]) * u0;
+                const float v1 = __half2float(sc_s[i * RWS + rown0 + rl + 4]) * u1;
+                *reinterpret_cast<__half2 *>(a.V + (vrow0 + col) * a.ldv + (r & ~7) + 2 * (r & 3)) =
+                    __floats2half2_rn(v0, v1);
+            }
+        } else {
+            // y[t][n], n pairs (n, n+1)
+            const int npairs = prows / 2;
+            for (int e = tid; e < ntok * npairs; e += kThreads) {
+                const int t = e / npairs, p = e - t * npairs;
+                const int rl = 2 * p;
+                const int n = row0 + rown0 + rl;
+                if (n >= a.rows) continue;
+                float s0 = 0.f, s1 = 0.f;
+                for (int q = 0; q < nsl; ++q) {
+                    const float *b = part + size_t(q) * prows * CPAD;
+                    for (int i = 0; i < ell; ++i) {
+                        s0 += __half2float(sc_s[i * RWS + rown0 + rl]) * b[rl * CPAD + t * ell + i];
+                        s1 += __half2float(sc_s[i * RWS + rown0 + rl + 1]) * b[(rl + 1) * CPAD + t * ell + i];
+                    }
+                }
+                const bool two = n + 1 < a.rows;
+                if (a.accumulate) {
+                    s0 += __bfloat162float(yst[t * RWS + rown0 + rl]);
+                    if (two) s1 += __bfloat162float(yst[t * RWS + rown0 + rl + 1]);
+                }
+                __nv_bfloat16 *yp = a.y + size_t(t0 + tc0 + t) * a.ldy + n;
+                if (pairs_ok && two) {
+                    *reinterpret_cast<__nv_bfloat162 *>(yp) = __floats2bfloat162_rn(s0, s1);
+                } else {
+                    yp[0] = __float2bfloat16_rn(s0);
+                    if (two) yp[1] = __float2bfloat16_rn(s1);
+                }
+            }
+        }
+        __syncthreads();  // red / slots / yst are reused by the next chunk
     }
 }
 
 // ================================================================ launchers
 
 template <typename Kern, typename Args>
-cudaError_t launch_ex(Kern kern, int &configured_smem, int grid_x, int grid_y, int threads, size_t smem, int KS,
+cudaError_t launch_ex(Kern kern, int &configured_smem, int grid_x, int grid_y, size_t smem, int cluster,
                       const Args &args, cudaStream_t stream, bool pdl) {
     if (smem > 48 * 1024 && static_cast<int>(smem) > configured_smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -638,14 +846,14 @@ cudaError_t launch_ex(Kern kern, int &configured_smem, int grid_x, int grid_y, i
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x, grid_y, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (KS > 1) {
+    if (cluster > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = KS;
+        attr[na].val.clusterDim.x = cluster;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -660,39 +868,62 @@ cudaError_t launch_ex(Kern kern, int &configured_smem, int grid_x, int grid_y, i
     return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
-template <int CT, int STAGE, bool SEG>
+template <int CT, int RBW, int STAGE, bool SEG>
 cudaError_t launch_stage_one(const DecPlan &plan, const DecArgs &args, int grid_y, cudaStream_t stream, bool pdl) {
     static int configured = 0;
-    return launch_ex(dec_stage_kernel<CT, STAGE, SEG>, configured, plan.grid_x, grid_y, kThreads, plan.smem, plan.KS,
-                     args, stream, pdl);
+    return launch_ex(dec_stage_kernel<CT, RBW, STAGE, SEG>, configured, plan.grid_x, grid_y, plan.smem, plan.KS, args,
+                     stream, pdl);
+}
+
+template <int CT, int STAGE, bool SEG>
+cudaError_t launch_stage_rbw(const DecPlan &plan, const DecArgs &args, int grid_y, cudaStream_t stream, bool pdl) {
+    switch (plan.RBW) {
+        case 2: return launch_stage_one<CT, 2, STAGE, SEG>(plan, args, grid_y, stream, pdl);
+        case 4: return launch_stage_one<CT, 4, STAGE, SEG>(plan, args, grid_y, stream, pdl);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <int STAGE, bool SEG>
 cudaError_t launch_stage_ct(const DecPlan &plan, const DecArgs &args, int grid_y, cudaStream_t stream, bool pdl) {
     switch (plan.CT) {
-        case 1: return launch_stage_one<1, STAGE, SEG>(plan, args, grid_y, stream, pdl);
-        case 2: return launch_stage_one<2, STAGE, SEG>(plan, args, grid_y, stream, pdl);
-        case 4: return launch_stage_one<4, STAGE, SEG>(plan, args, grid_y, stream, pdl);
-        case 8: return launch_stage_one<8, STAGE, SEG>(plan, args, grid_y, stream, pdl);
+        case 1: return launch_stage_rbw<1, STAGE, SEG>(plan, args, grid_y, stream, pdl);
+        case 2: return launch_stage_rbw<2, STAGE, SEG>(plan, args, grid_y, stream, pdl);
+        case 4: return launch_stage_rbw<4, STAGE, SEG>(plan, args, grid_y, stream, pdl);
+        case 8: return plan.RBW == 2 ? launch_stage_one<8, 2, STAGE, SEG>(plan, args, grid_y, stream, pdl)
+                                     : cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <int CT, bool SEG>
+template <int CT, int RBW, bool SEG>
 cudaError_t launch_fused_one(const FusedPlan &plan, const FusedArgs &args, int grid_y, cudaStream_t stream,
                              bool pdl) {
     static int configured = 0;
-    return launch_ex(dec_fused_kernel<CT, SEG>, configured, plan.grid_x, grid_y, kFusedThreads, plan.smem, plan.KS,
-                     args, stream, pdl);
+    return launch_ex(dec_fused_kernel<CT, RBW, SEG>, configured, plan.grid_x, grid_y, plan.smem, plan.C, args, stream,
+                     pdl);
+}
+
+template <int CT, bool SEG>
+cudaError_t launch_fused_rbw(const FusedPlan &plan, const FusedArgs &args, int grid_y, cudaStream_t stream, bool pdl) {
+    switch (plan.RBW) {
+        case 1: return launch_fused_one<CT, 1, SEG>(plan, args, grid_y, stream, pdl);
+        case 2: return launch_fused_one<CT, 2, SEG>(plan, args, grid_y, stream, pdl);
+        case 4: return launch_fused_one<CT, 4, SEG>(plan, args, grid_y, stream, pdl);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <bool SEG>
 cudaError_t launch_fused_ct(const FusedPlan &plan, const FusedArgs &args, int grid_y, cudaStream_t stream, bool pdl) {
     switch (plan.CT) {
-        case 1: return launch_fused_one<1, SEG>(plan, args, grid_y, stream, pdl);
-        case 2: return launch_fused_one<2, SEG>(plan, args, grid_y, stream, pdl);
-        case 4: return launch_fused_one<4, SEG>(plan, args, grid_y, stream, pdl);
-        case 8: return launch_fused_one<8, SEG>(plan, args, grid_y, stream, pdl);
+        case 1: return launch_fused_rbw<1, SEG>(plan, args, grid_y, stream, pdl);
+        case 2: return launch_fused_rbw<2, SEG>(plan, args, grid_y, stream, pdl);
+        case 4: return launch_fused_rbw<4, SEG>(plan, args, grid_y, stream, pdl);
+        case 8:
+            if (plan.RBW == 1) return launch_fused_one<8, 1, SEG>(plan, args, grid_y, stream, pdl);
+            if (plan.RBW == 2) return launch_fused_one<8, 2, SEG>(plan, args, grid_y, stream, pdl);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -703,48 +934,47 @@ int ct_for(int columns, int max_ct) {
     return ct;
 }
 
-}  // namespace
+constexpr size_t kSmemCap = 200 * 1024;
 
-size_t decode_smem_bytes(int CT, int RB, int Wc) {
-    // upper bound over both stages, any ell <= 4, with or without accumulate
-    size_t m = 0;
-    for (int ell = 1; ell <= 4; ++ell)
-        m = std::max(m, std::max(stage_smem(8 * CT, RB, Wc, ell, true, true).total,
-                                 stage_smem(8 * CT, RB, Wc, ell, false, true).total));
-    return m;
+int occupancy_for(size_t smem) {
+    int occ = static_cast<int>(std::min<size_t>(size_t(228 * 1024) / (smem + 1024), 8));
+    return occ < 1 ? 1 : occ;
 }
 
-// Choose rows per CTA (RB), cluster split of K (KS) and column tiles (CT)
-// for one stage.  The cost model counts, per SM, the unpack work (one
-// instruction per sign bit, 128 lanes per clock), the activation fill, and
-// a fixed per-CTA cost.
-DecPlan plan_decode_stage(int rows_cover, int Kw, int columns, int max_ct, int num_sms) {
+}  // namespace
+
+// Stage plan: 16*RBW rows per CTA, cluster split of K (KS), column tiles CT.
+// Latency model (clocks) of the slowest SM: per wave a fixed cost (launch,
+// the activation round trip, barriers) plus the words each warp streams;
+// a cluster exchange costs a barrier and the pushes.
+DecPlan plan_decode_stage(int rows_cover, int Kw, int columns, int max_ct, int num_sms, int ell, bool stage1) {
     DecPlan best = {};
     const int ct = ct_for(columns, max_ct);
-    const int nb = (rows_cover + 15) / 16;
-    const size_t smem_cap = 200 * 1024;
+    const int cpad = 8 * ct;
     double best_cost = 1e300;
-    for (int KS = 1; KS <= 8; KS *= 2) {
-        if (KS > Kw) break;
-        const int Wc = (Kw + KS - 1) / KS;
-        for (int RB = 1; RB <= 8; RB *= 2) {
-            if (RB > 1 && (RB / 2) * 16 >= rows_cover) break;
-            const size_t smem = decode_smem_bytes(ct, RB, Wc);
-            if (smem > smem_cap) continue;
-            const int groups = (nb + RB - 1) / RB;
+    for (int RBW = 2; RBW <= 4; RBW *= 2) {
+        if (ct >= 8 && RBW > 2) break;
+        for (int KS = 1; KS <= 8; KS *= 2) {
+            if (KS > 1 && (KS > Kw || 16 * RBW / KS < 8)) break;
+            const int Wc = (Kw + KS - 1) / KS;
+            const size_t smem = stage_smem(cpad, RBW, KS, Wc, ell, stage1, true).total;
+            if (smem > kSmemCap) continue;
+            const int groups = (rows_cover + 16 * RBW - 1) / (16 * RBW);
             const int ctas = groups * KS;
-            int occ = static_cast<int>(std::min<size_t>(size_t(228 * 1024) / (smem + 1024), 8));
-            if (occ < 1) occ = 1;
-            const double per_sm = double(ctas) / num_sms;
-            const double waves = std::ceil(per_sm / occ);
-            const double unpack = 4.0 * RB * Wc;                 // clocks of sign unpack per CTA
-            const double fill = double(ct * 8) * Wc * 0.75;      // activation fill per CTA
-            const double fixed = 900.0 + (KS > 1 ? 500.0 : 0.0);  // launch, syncs, epilogue
-            const double cost = std::ceil(per_sm) * (unpack + fill) + waves * fixed;
+            const int occ = occupancy_for(smem);
+            const double waves = std::ceil(double(ctas) / (double(num_sms) * occ));
+            const double per_sm = std::ceil(double(ctas) / num_sms);
+            const int Wp = (Wc + kWarps - 1) / kWarps;
+            const int nwb = ct >= 8 ? 1 : (ct >= 4 ? 2 : 4);
+            const double batches = std::ceil(double(Wp) / nwb);
+            const double warp_work = Wp * (60.0 * ct + 30.0 * RBW + 12.0 * RBW * ct);
+            const double epi = double(16 * RBW / KS) * cpad * 8.0 / kThreads * 20.0;
+            const double cost = waves * 1500.0 + per_sm * (warp_work + epi) + (batches - 1.0) * 700.0 +
+                                (KS > 1 ? 900.0 : 0.0);
             if (cost < best_cost) {
                 best_cost = cost;
                 best.CT = ct;
-                best.RB = RB;
+                best.RBW = RBW;
                 best.KS = KS;
                 best.Wc = Wc;
                 best.grid_x = ctas;
@@ -755,43 +985,46 @@ DecPlan plan_decode_stage(int rows_cover, int Kw, int columns, int max_ct, int n
     return best;
 }
 
-// Fused plan: cluster size KS (stage-1 K split), clusters per problem NQ and
-// stage-2 row blocks per CTA RB2.  One 512-thread CTA fits an SM, so the
-// grid of problems x NQ x KS CTAs runs in ceil(total / num_sms) waves; the
-// cost is waves x the clocks of one CTA (stage-1 and stage-2 unpack, the
-// activation fill, the bytes it streams at ~24 B/clk, the cluster exchange).
+// Fused plan: cluster size C (stage-1 split of M), stage-2 rows per CTA RW.
+// Same latency model: waves, the stage-1 words per warp, the stage-2 items
+// per warp, the cluster exchange.
 FusedPlan plan_fused(int N, int M, int R, int ell, int columns, int num_sms, int problems, bool accumulate) {
     FusedPlan best = {};
+    if (R > kFusedMaxR) return best;
     const int ct = ct_for(columns, 8);
-    const int R1 = (R + 31) & ~31;
-    const int Kw1 = (M + 31) / 32, Kw2 = R1 / 32;
-    const size_t smem_cap = 200 * 1024;
-    double best_cost = 1e300;
+    const int cpad = 8 * ct;
+    const int RB1 = (R + 15) / 16;
+    int RBW = RB1 >= 4 ? 4 : (RB1 >= 2 ? 2 : 1);
+    if (ct >= 8 && RBW > 2) RBW = 2;
+    const int G1 = fused_g1(R, RBW), KP = fused_kp(G1);
+    const int R2 = (R + 31) & ~31, Kw1 = (M + 31) / 32, Kw2 = R2 / 32;
     if (problems < 1) problems = 1;
-    for (int KS = 1; KS <= 8; KS *= 2) {
-        if (KS > Kw1) break;
-        const int Wc1 = (Kw1 + KS - 1) / KS;
-        for (int NQ = 1; NQ * KS <= std::max(num_sms, KS); NQ *= 2) {
-            const int ctas = NQ * KS;
-            const int RB2 = std::max(1, (N + 16 * ctas - 1) / (16 * ctas));
-            const int RW = 16 * RB2;
-            const size_t smem = fused_smem(8 * ct, Wc1, R1, Kw2, RW, ell, KS, accumulate).total;
-            if (smem > smem_cap) continue;
-            const double s1 = 4.0 * (R1 / 16) * Wc1 + double(ct * 8) * Wc1 * 0.75;
-            const double s2 = 4.0 * RB2 * Kw2 + 2.0 * RB2 * ct * 8;
-            const double bytes = double(R1) * Wc1 * 4 + double(RW) * Kw2 * 4 + 2.0 * ell * (32.0 * Wc1 + RW);
-            const double mem = bytes / 24.0;
-            const double xch = KS > 1 ? 600.0 + double(R1) * ct * 8 / 64.0 : 0.0;
-            const double waves = std::ceil(double(problems) * ctas / num_sms);
-            const double cost = waves * (s1 + s2 + mem + xch + 2000.0);
+    double best_cost = 1e300;
+    for (int C = 1; C <= 8; C *= 2) {
+        if (C > 1 && C > Kw1) break;
+        const int Wc = (Kw1 + C - 1) / C;
+        const int Wp = (Wc + KP - 1) / KP;
+        for (int RW = 16; RW <= 256; RW *= 2) {
+            const int used = (N + RW - 1) / RW;          // CTAs that own output rows
+            const int grid = ((used + C - 1) / C) * C;   // whole clusters
+            const size_t smem = fused_smem(cpad, RBW, Wc, R, RW, ell, C, accumulate).total;
+            if (smem > kSmemCap) continue;
+            const int occ = occupancy_for(smem);
+            const double waves = std::ceil(double(problems) * grid / (double(num_sms) * occ));
+            const double per_sm = std::ceil(double(problems) * grid / num_sms);
+            const int nwb = ct >= 8 ? 1 : (ct >= 4 ? 2 : 4);
+            const double s1 = Wp * (60.0 * ct + 30.0 * RBW + 12.0 * RBW * ct) + std::ceil(double(Wp) / nwb - 1.0) * 700.0;
+            const double s2 = std::ceil(double(RW / 16) * ct / kWarps) * Kw2 * 40.0;
+            const double red = double(16 * RBW * G1) * cpad / kThreads * (KP + 2.0 * C) * 8.0;
+            const double cost = waves * (1500.0 + (C > 1 ? 900.0 : 0.0)) + per_sm * (s1 + s2 + red);
             if (cost < best_cost) {
                 best_cost = cost;
                 best.CT = ct;
-                best.KS = KS;
-                best.NQ = NQ;
-                best.RB2 = RB2;
-                best.Wc1 = Wc1;
-                best.grid_x = ctas;
+                best.RBW = RBW;
+                best.C = C;
+                best.RW = RW;
+                best.Wc = Wc;
+                best.grid_x = grid;
                 best.smem = smem;
             }
         }
@@ -812,6 +1045,68 @@ cudaError_t launch_decode_fused(bool segmented, const FusedPlan &plan, const Fus
                                 cudaStream_t stream, bool pdl) {
     return segmented ? launch_fused_ct<true>(plan, args, grid_y, stream, pdl)
                      : launch_fused_ct<false>(plan, args, grid_y, stream, pdl);
+}
+
+// Both decode stages of one call (or of a routed batch when seg_off is set):
+// stage 1 writes V = beta * (B2 (gamma * x)) to `V` (fp16, [ell*T][ldv]),
+// stage 2 reads it.
+cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int num_sms, cudaStream_t stream) {
+    const int ell = c.ell;
+    const int64_t cols = std::min<int64_t>(int64_t(ell) * c.tokens_per_problem, 64);
+    const int problems = std::max(1, c.S);
+    const int sms_per_problem = std::max(1, num_sms / problems);
+    DecArgs a = {};
+    a.ell = ell;
+    a.T = c.T;
+    a.x = c.x;
+    a.ldx = c.M;
+    a.V = V;
+    a.ldv = ldv;
+    a.y = c.y;
+    a.ldy = c.N;
+    a.accumulate = c.accumulate;
+    a.seg_off = c.seg_off;
+    a.seg_ad = c.seg_ad;
+    a.adapters = c.adapters;
+    a.n_adapters = c.n_adapters;
+    a.status = c.status;
+    const bool seg = c.seg_off != nullptr;
+
+    DecArgs a1 = a;
+    if (!seg) {
+        a1.bits = c.f->B2;
+        a1.ldw = c.f->ldw2;
+        a1.gamma = reinterpret_cast<const __half *>(c.f->gamma);
+        a1.beta = reinterpret_cast<const __half *>(c.f->beta);
+    }
+    a1.rows = c.R;
+    a1.rows_out = (c.R + 31) & ~31;
+    a1.K = c.M;
+    a1.Kw = (c.M + 31) / 32;
+    DecPlan p1 = plan_decode_stage(a1.rows_out, a1.Kw, static_cast<int>(cols), 8, sms_per_problem, ell, true);
+    a1.KS = p1.KS;
+    a1.Wc = p1.Wc;
+
+    DecArgs a2 = a;
+    if (!seg) {
+        a2.bits = c.f->B1;
+        a2.ldw = c.f->ldw1;
+        a2.alpha = reinterpret_cast<const __half *>(c.f->alpha);
+    }
+    a2.rows = c.N;
+    a2.rows_out = c.N;
+    a2.K = c.R;
+    a2.Kw = (c.R + 31) / 32;
+    DecPlan p2 = plan_decode_stage(c.N, a2.Kw, static_cast<int>(cols), p1.CT, sms_per_problem, ell, false);
+    p2.CT = p1.CT;  // both stages use the same column chunking
+    if (p2.smem == 0 || p1.smem == 0) return cudaErrorNotSupported;
+    if (p2.CT >= 8 && p2.RBW > 2) return cudaErrorNotSupported;
+    p2.smem = stage_smem(8 * p2.CT, p2.RBW, p2.KS, p2.Wc, ell, false, c.accumulate != 0).total;
+    a2.KS = p2.KS;
+    a2.Wc = p2.Wc;
+    cudaError_t e = launch_decode_stage(1, seg, p1, a1, problems, stream, true);
+    if (e != cudaSuccess) return e;
+    return launch_decode_stage(2, seg, p2, a2, problems, stream, true);
 }
 
 }  // namespace dbfk

@@ -13,19 +13,23 @@ namespace dbfk {
 
 // ----------------------------------------------------------- decode path
 
+// Largest R the one-launch fused decode kernel takes (it recomputes stage 1
+// in every cluster; the plan also checks its shared memory).
+constexpr int kFusedMaxR = 256;
+
 // Arguments of one decode stage launch.  Stage 1 contracts x (scaled by
 // gamma) with B2 and writes V = beta * u in fp16 (activation order); stage 2
 // contracts V with B1 and writes y = sum_i alpha_i * w_i in bf16.
 struct DecArgs {
     const uint32_t *bits;   // packed weights of this stage (B2 or B1)
     int ldw;                // words per packed row
-    int rows;               // weight rows (R or N)
-    int rows_cover;         // rows the launch covers (stage 1: round_up(R, 32))
+    int rows;               // weight rows that exist (R or N)
+    int rows_out;           // rows the launch writes (stage 1: round_up(R, 32); stage 2: N)
     int Kw;                 // packed words per row that hold data (ceil(K/32))
     int K;                  // contraction length (M or R)
     int ell;
-    int T;                  // tokens (plain mode)
-    const __nv_bfloat16 *x; // stage 1 input [T][M]
+    int T;                  // tokens of the call (all segments in segmented mode)
+    const __nv_bfloat16 *x; // stage 1 input [T][ldx]
     int ldx;
     const __half *gamma;    // [ell][M]
     const __half *beta;     // [ell][R]
@@ -35,7 +39,6 @@ struct DecArgs {
     __nv_bfloat16 *y;       // [T][ldy]
     int ldy;
     int accumulate;
-    int RB;                 // 16-row blocks per CTA (1, 2, 4 or 8)
     int KS;                 // CTAs per cluster along K
     int Wc;                 // packed words per CTA K-slice
     // multi-adapter mode
@@ -47,15 +50,16 @@ struct DecArgs {
 };
 
 struct DecPlan {
-    int CT;          // n8 column tiles (columns per chunk = 8*CT)
-    int RB, KS, Wc;
+    int CT;          // n8 column tiles (columns per chunk = 8*CT); 0 = no plan
+    int RBW;         // 16-row blocks per CTA (2 or 4)
+    int KS, Wc;
     int grid_x;
     size_t smem;
 };
 
-DecPlan plan_decode_stage(int rows_cover, int Kw, int columns, int max_ct, int num_sms);
+DecPlan plan_decode_stage(int rows_cover, int Kw, int columns, int max_ct, int num_sms, int ell, bool stage1);
 
-// One-launch decode for small R: a cluster splits stage 1 over K, shares
+// One-launch decode for small R: a cluster splits stage 1 over M, shares
 // the partial u through distributed shared memory, then each CTA computes
 // its slice of the N output rows.
 struct FusedArgs {
@@ -66,9 +70,9 @@ struct FusedArgs {
     const __nv_bfloat16 *x;
     __nv_bfloat16 *y;
     int accumulate;
-    int KS;    // cluster size (stage-1 K split)
-    int RB2;   // stage-2 row blocks (16 rows) per CTA
-    int Wc1;   // stage-1 packed words per CTA
+    int C;     // cluster size (stage-1 split of M)
+    int Wc;    // stage-1 packed words per CTA
+    int RW;    // stage-2 output rows per CTA (multiple of 16)
     const int32_t *seg_off;
     const int32_t *seg_ad;
     const dbf_factors *adapters;
@@ -77,7 +81,7 @@ struct FusedArgs {
 };
 
 struct FusedPlan {
-    int CT, KS, NQ, RB2, Wc1, grid_x;
+    int CT, RBW, C, RW, Wc, grid_x;  // CT = 0: no plan; RBW: stage-1 16-row blocks per warp
     size_t smem;
 };
 
@@ -86,9 +90,30 @@ struct FusedPlan {
 FusedPlan plan_fused(int N, int M, int R, int ell, int columns, int num_sms, int problems, bool accumulate);
 cudaError_t launch_decode_fused(bool segmented, const FusedPlan &plan, const FusedArgs &args, int grid_y,
                                 cudaStream_t stream, bool pdl);
-size_t decode_smem_bytes(int CT, int RB, int Wc);
 cudaError_t launch_decode_stage(int stage, bool segmented, const DecPlan &plan, const DecArgs &args,
                                 int grid_y, cudaStream_t stream, bool pdl);
+
+// One decode call (f set, seg_off null) or a routed batch of S segments
+// (f null; seg_off, seg_ad, adapters set) for the two-stage kernels.
+struct DecodeCall {
+    const dbf_factors *f;        // host copy of the factors (single call)
+    int N, M, R, ell;
+    int T;                       // tokens in x / y
+    int tokens_per_problem;      // tokens one launch problem covers (T, or about twice the mean segment)
+    const __nv_bfloat16 *x;
+    __nv_bfloat16 *y;
+    int accumulate;
+    const int32_t *seg_off;
+    const int32_t *seg_ad;
+    const dbf_factors *adapters;
+    int n_adapters;
+    int S;
+    int *status;
+};
+
+// Both stages; V is device scratch of ell*T rows x ldv halves.  Returns
+// cudaErrorNotSupported when no tile plan fits the shape.
+cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------- prefill path
 

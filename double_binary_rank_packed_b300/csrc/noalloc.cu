@@ -87,9 +87,7 @@ extern "C" int dbf_matmul_decode_noalloc(const dbf_factors *f, const uint16_t *x
         return DBF_ERR_CUDA;
     }
 
-    // the same two decode launches as dbf_matmul's decode path, with V in the static array
-    const int ell = f->ell;
-    const int64_t cols = std::min<int64_t>(ell * T, 64);
+    // the two-stage decode kernels of dbf_matmul's decode path, with V in the static array
     int sms = 148;
     {
         int dev = 0;
@@ -97,48 +95,24 @@ extern "C" int dbf_matmul_decode_noalloc(const dbf_factors *f, const uint16_t *x
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 148;
     }
-    DecArgs a = {};
-    a.ell = ell;
-    a.T = static_cast<int>(T);
-    a.x = reinterpret_cast<const __nv_bfloat16 *>(x);
-    a.ldx = f->M;
-    a.gamma = reinterpret_cast<const __half *>(f->gamma);
-    a.beta = reinterpret_cast<const __half *>(f->beta);
-    a.alpha = reinterpret_cast<const __half *>(f->alpha);
-    a.V = static_cast<__half *>(scratch);
-    a.ldv = static_cast<int>(ldv);
-    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
-    a.ldy = f->N;
-    a.accumulate = accumulate;
-    a.status = nullptr;
-
-    DecArgs a1 = a;
-    a1.bits = f->B2;
-    a1.ldw = f->ldw2;
-    a1.rows = f->R;
-    a1.rows_cover = static_cast<int>(round_up(f->R, 32));
-    a1.K = f->M;
-    a1.Kw = static_cast<int>(ceil_div(f->M, 32));
-    DecPlan p1 = plan_decode_stage(a1.rows_cover, a1.Kw, static_cast<int>(cols), 8, sms);
-    a1.RB = p1.RB;
-    a1.KS = p1.KS;
-    a1.Wc = p1.Wc;
-    DecArgs a2 = a;
-    a2.bits = f->B1;
-    a2.ldw = f->ldw1;
-    a2.rows = f->N;
-    a2.rows_cover = f->N;
-    a2.K = f->R;
-    a2.Kw = static_cast<int>(ceil_div(f->R, 32));
-    DecPlan p2 = plan_decode_stage(a2.rows_cover, a2.Kw, static_cast<int>(cols), p1.CT, sms);
-    p2.CT = p1.CT;
-    a2.RB = p2.RB;
-    a2.KS = p2.KS;
-    a2.Wc = p2.Wc;
-    if (p1.CT == 0 || p2.CT == 0) return DBF_ERR_UNSUPPORTED;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    err = launch_decode_stage(1, false, p1, a1, 1, s, true);
-    if (err == cudaSuccess) err = launch_decode_stage(2, false, p2, a2, 1, s, true);
+    DecodeCall c = {};
+    c.f = f;
+    c.N = f->N;
+    c.M = f->M;
+    c.R = f->R;
+    c.ell = f->ell;
+    c.T = static_cast<int>(T);
+    c.tokens_per_problem = static_cast<int>(T);
+    c.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    c.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    c.accumulate = accumulate;
+    c.status = nullptr;
+    err = launch_decode_two_stage(c, static_cast<__half *>(scratch), static_cast<int>(ldv), sms,
+                                  static_cast<cudaStream_t>(stream));
+    if (err == cudaErrorNotSupported) {
+        set_last_error("dbf_matmul_decode_noalloc: no decode tile plan fits this shape");
+        return DBF_ERR_UNSUPPORTED;
+    }
     if (err != cudaSuccess) {
         char msg[200];
         snprintf(msg, sizeof(msg), "dbf_matmul_decode_noalloc: %s", cudaGetErrorString(err));
