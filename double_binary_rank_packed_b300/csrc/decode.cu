@@ -200,17 +200,11 @@ __device__ __forceinline__ void add4(float4 &u, const float4 &o) {
     u.w += o.w;
 }
 
-__device__ __forceinline__ void push_float4(uint32_t addr, const float4 &u, uint32_t rank) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(mapa_shared(addr, rank)), "f"(u.x),
-                 "f"(u.y), "f"(u.z), "f"(u.w)
-                 : "memory");
-}
-
 // Words a warp streams per batch: every activation load of a batch is in
 // flight before the first conversion.
 template <int CT>
 __host__ __device__ constexpr int words_per_batch() {
-    return CT >= 8 ? 1 : (CT >= 4 ? 2 : 4);
+    return CT >= 4 ? 1 : (CT >= 2 ? 2 : 4);
 }
 
 // Stage-2 tile (RW rows x columns, fp32) -> y[t][n] = bf16(sum_i alpha_i[n]
@@ -269,7 +263,7 @@ __host__ __device__ inline FusedSmem fused_smem(int CPAD, int RBW, int Wc, int R
     L.red = o;
     o += align16(size_t(KP) * R1 * CPAD * 4);
     L.slots = o;
-    o += align16(size_t(C) * R1 * CPAD * 4);
+    o += align16(size_t(C) * R1 * CPAD * 4);  // slot q: the partial u of cluster rank q
     L.vs = o;
     o += align16(size_t(CPAD) * (R2 + 8) * 2);
     L.yst = o;
@@ -281,7 +275,7 @@ __host__ __device__ inline FusedSmem fused_smem(int CPAD, int RBW, int Wc, int R
 }
 
 template <int CT, int RBW, bool SEG>
-__global__ void __launch_bounds__(kThreads) dec_fused_kernel(const FusedArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs a) {
     constexpr int CPAD = 8 * CT;
     constexpr int C4 = CPAD / 4;
     constexpr int NWB = words_per_batch<CT>();
@@ -461,11 +455,15 @@ __global__ void __launch_bounds__(kThreads) dec_fused_kernel(const FusedArgs a) 
             const int r = e / C4;
             float4 u = *reinterpret_cast<const float4 *>(red + r * CPAD + 4 * c4);
             for (int q = 1; q < KP; ++q) add4(u, *reinterpret_cast<const float4 *>(red + (q * R1 + r) * CPAD + 4 * c4));
-            const uint32_t off = 4u * static_cast<uint32_t>((rank * R1 + r) * CPAD + 4 * c4);
+            const uint32_t off = slots_addr + 4u * static_cast<uint32_t>((rank * R1 + r) * CPAD + 4 * c4);
             if (C > 1) {
-                for (int q = 0; q < C; ++q) push_float4(slots_addr + off, u, static_cast<uint32_t>(q));
+                for (int q = 0; q < C; ++q)
+                    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     mapa_shared(off, static_cast<uint32_t>(q))),
+                                 "f"(u.x), "f"(u.y), "f"(u.z), "f"(u.w)
+                                 : "memory");
             } else {
-                *reinterpret_cast<float4 *>(slots + off / 4) = u;
+                *reinterpret_cast<float4 *>(slots + r * CPAD + 4 * c4) = u;
             }
         }
         if (C > 1)
@@ -579,14 +577,14 @@ __host__ __device__ inline StageSmem stage_smem(int CPAD, int RBW, int KS, int W
     if (!stage1 && acc) o += align16(size_t(CPAD) * RWS * 2);
     L.red = o;
     o += align16(size_t(kWarps) * RWS * CPAD * 4);
-    L.slots = o;
-    if (KS > 1) o += align16(size_t(KS) * (RWS / KS) * CPAD * 4);
+    L.slots = o;  // KS > 1: this CTA's partial [RWS][CPAD], then the sums of its own rows [RWS/KS][CPAD]
+    if (KS > 1) o += align16(size_t(RWS) * CPAD * 4) + align16(size_t(RWS / KS) * CPAD * 4);
     L.total = o;
     return L;
 }
 
 template <int CT, int RBW, int STAGE, bool SEG>
-__global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) dec_stage_kernel(const DecArgs a) {
     constexpr int CPAD = 8 * CT;
     constexpr int C4 = CPAD / 4;
     constexpr int RWS = 16 * RBW;
@@ -660,7 +658,6 @@ __global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
         }
     }
     cp_async_commit();
-    if (KS > 1) cluster_arrive_relaxed();  // matched by the wait before the first push
     pdl_trigger();
     if constexpr (!SEG) pdl_wait();
 
@@ -677,10 +674,13 @@ __global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
     const int tpc = CPAD / ell;  // whole tokens per column chunk
     const int nchunks = (Tseg + tpc - 1) / tpc;
     const bool xvec = ((a.ldx & 7) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0);
-    const uint32_t red_addr = smem_u32(red), slots_addr = smem_u32(slots);
+    const uint32_t red_addr = smem_u32(red);
+    float *mine = slots;                                               // KS > 1: this CTA's partial
+    float *sums = slots + (align16(size_t(RWS) * CPAD * 4) / 4);       // KS > 1: sums of the owned rows
+    const uint32_t mine_addr = smem_u32(mine);
     const int c4 = tid % C4;
-    const int nsl = (KS > 1) ? KS : kWarps;      // partial slices summed in the epilogue
-    const float *part = (KS > 1) ? slots : red;  // [nsl][rows][CPAD]
+    const int nsl = (KS > 1) ? 1 : kWarps;       // partial slices summed in the epilogue
+    const float *part = (KS > 1) ? sums : red;   // [nsl][rows][CPAD]
     const int prows = (KS > 1) ? ROWN : RWS;     // rows per slice
     const int rown0 = (KS > 1) ? rank * ROWN : 0;
     const bool pairs_ok = ((a.ldy & 1) == 0);
@@ -689,7 +689,7 @@ __global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
         const int tc0 = chunk * tpc;
         const int ntok = min(tpc, Tseg - tc0);
         const int ncol = ntok * ell;
-        if (chunk > 0 && KS > 1) cluster_sync_all();  // owners finished reading the previous chunk's slots
+        if (chunk > 0 && KS > 1) cluster_wait_acquire();  // peers finished reading the previous chunk's partial
 
         // ---- 2. the first batch of activations straight into registers
         if (STAGE == 2 && a.accumulate)
@@ -719,7 +719,6 @@ __global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
         load_batch(wb);
         cp_async_wait_all();
         __syncthreads();  // signs and scales are in shared memory
-        if (chunk == 0 && KS > 1) cluster_wait();  // every CTA of the cluster has started
 
         // ---- 3. tensor-core sign contraction over this warp's words
         {
@@ -764,18 +763,33 @@ __global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
         }
         __syncthreads();
 
-        // ---- 4. cluster: sum the warp partials, push each owner's rows into its slot `rank`
+        // ---- 4. cluster: sum the warp partials into this CTA's partial; after the
+        //         barrier each CTA sums its own rows over the partials of all
+        //         CTAs of the cluster (loads from distributed shared memory)
         if (KS > 1) {
             for (int e = tid; e < RWS * C4; e += kThreads) {
                 const int r = e / C4;
                 float4 u = *reinterpret_cast<const float4 *>(red + r * CPAD + 4 * c4);
                 for (int q = 1; q < kWarps; ++q)
                     add4(u, *reinterpret_cast<const float4 *>(red + (q * RWS + r) * CPAD + 4 * c4));
-                const int owner = r / ROWN, rl = r - owner * ROWN;
-                push_float4(slots_addr + 4u * static_cast<uint32_t>((rank * ROWN + rl) * CPAD + 4 * c4), u,
-                            static_cast<uint32_t>(owner));
+                *reinterpret_cast<float4 *>(mine + r * CPAD + 4 * c4) = u;
             }
             cluster_sync_all();
+            for (int e = tid; e < ROWN * C4; e += kThreads) {
+                const int rl = e / C4;
+                const uint32_t off = mine_addr + 4u * static_cast<uint32_t>((rown0 + rl) * CPAD + 4 * c4);
+                float4 part4[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < KS) part4[q] = ld_dsmem_f32x4(mapa_shared(off, static_cast<uint32_t>(q)));
+                float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < KS) add4(u, part4[q]);
+                *reinterpret_cast<float4 *>(sums + rl * CPAD + 4 * c4) = u;
+            }
+            cluster_arrive_release();  // this CTA is done reading its peers' partials
+            __syncthreads();
         }
 
         // ---- 5. epilogue of this CTA's rows [rown0, rown0 + prows)
@@ -832,6 +846,7 @@ __global__ void __launch_bounds__(kThreads) dec_stage_kernel(const DecArgs a) {
         }
         __syncthreads();  // red / slots / yst are reused by the next chunk
     }
+    if (KS > 1) cluster_wait_acquire();  // peers may read this CTA's partial until they arrive
 }
 
 // ================================================================ launchers
@@ -889,7 +904,8 @@ cudaError_t launch_stage_ct(const DecPlan &plan, const DecArgs &args, int grid_y
     switch (plan.CT) {
         case 1: return launch_stage_rbw<1, STAGE, SEG>(plan, args, grid_y, stream, pdl);
         case 2: return launch_stage_rbw<2, STAGE, SEG>(plan, args, grid_y, stream, pdl);
-        case 4: return launch_stage_rbw<4, STAGE, SEG>(plan, args, grid_y, stream, pdl);
+        case 4: return plan.RBW == 2 ? launch_stage_one<4, 2, STAGE, SEG>(plan, args, grid_y, stream, pdl)
+                                     : cudaErrorInvalidValue;
         case 8: return plan.RBW == 2 ? launch_stage_one<8, 2, STAGE, SEG>(plan, args, grid_y, stream, pdl)
                                      : cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
@@ -919,11 +935,12 @@ cudaError_t launch_fused_ct(const FusedPlan &plan, const FusedArgs &args, int gr
     switch (plan.CT) {
         case 1: return launch_fused_rbw<1, SEG>(plan, args, grid_y, stream, pdl);
         case 2: return launch_fused_rbw<2, SEG>(plan, args, grid_y, stream, pdl);
-        case 4: return launch_fused_rbw<4, SEG>(plan, args, grid_y, stream, pdl);
-        case 8:
-            if (plan.RBW == 1) return launch_fused_one<8, 1, SEG>(plan, args, grid_y, stream, pdl);
-            if (plan.RBW == 2) return launch_fused_one<8, 2, SEG>(plan, args, grid_y, stream, pdl);
+        case 4:
+            if (plan.RBW == 1) return launch_fused_one<4, 1, SEG>(plan, args, grid_y, stream, pdl);
+            if (plan.RBW == 2) return launch_fused_one<4, 2, SEG>(plan, args, grid_y, stream, pdl);
             return cudaErrorInvalidValue;
+        case 8: return plan.RBW == 1 ? launch_fused_one<8, 1, SEG>(plan, args, grid_y, stream, pdl)
+                                     : cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -936,8 +953,9 @@ int ct_for(int columns, int max_ct) {
 
 constexpr size_t kSmemCap = 200 * 1024;
 
+// CTAs per SM: shared memory, and the registers of __launch_bounds__(kThreads, 2)
 int occupancy_for(size_t smem) {
-    int occ = static_cast<int>(std::min<size_t>(size_t(228 * 1024) / (smem + 1024), 8));
+    int occ = static_cast<int>(std::min<size_t>(size_t(228 * 1024) / (smem + 1024), 2));
     return occ < 1 ? 1 : occ;
 }
 
@@ -953,7 +971,7 @@ DecPlan plan_decode_stage(int rows_cover, int Kw, int columns, int max_ct, int n
     const int cpad = 8 * ct;
     double best_cost = 1e300;
     for (int RBW = 2; RBW <= 4; RBW *= 2) {
-        if (ct >= 8 && RBW > 2) break;
+        if (ct >= 4 && RBW > 2) break;  // accumulators of RBW x CT fragments stay in registers
         for (int KS = 1; KS <= 8; KS *= 2) {
             if (KS > 1 && (KS > Kw || 16 * RBW / KS < 8)) break;
             const int Wc = (Kw + KS - 1) / KS;
@@ -965,7 +983,7 @@ DecPlan plan_decode_stage(int rows_cover, int Kw, int columns, int max_ct, int n
             const double waves = std::ceil(double(ctas) / (double(num_sms) * occ));
             const double per_sm = std::ceil(double(ctas) / num_sms);
             const int Wp = (Wc + kWarps - 1) / kWarps;
-            const int nwb = ct >= 8 ? 1 : (ct >= 4 ? 2 : 4);
+            const int nwb = ct >= 4 ? 1 : (ct >= 2 ? 2 : 4);
             const double batches = std::ceil(double(Wp) / nwb);
             const double warp_work = Wp * (60.0 * ct + 30.0 * RBW + 12.0 * RBW * ct);
             const double epi = double(16 * RBW / KS) * cpad * 8.0 / kThreads * 20.0;
@@ -995,7 +1013,8 @@ FusedPlan plan_fused(int N, int M, int R, int ell, int columns, int num_sms, int
     const int cpad = 8 * ct;
     const int RB1 = (R + 15) / 16;
     int RBW = RB1 >= 4 ? 4 : (RB1 >= 2 ? 2 : 1);
-    if (ct >= 8 && RBW > 2) RBW = 2;
+    if (ct >= 4 && RBW > 2) RBW = 2;  // accumulators of RBW x CT fragments stay in registers
+    if (ct >= 8) RBW = 1;
     const int G1 = fused_g1(R, RBW), KP = fused_kp(G1);
     const int R2 = (R + 31) & ~31, Kw1 = (M + 31) / 32, Kw2 = R2 / 32;
     if (problems < 1) problems = 1;
@@ -1012,11 +1031,14 @@ FusedPlan plan_fused(int N, int M, int R, int ell, int columns, int num_sms, int
             const int occ = occupancy_for(smem);
             const double waves = std::ceil(double(problems) * grid / (double(num_sms) * occ));
             const double per_sm = std::ceil(double(problems) * grid / num_sms);
-            const int nwb = ct >= 8 ? 1 : (ct >= 4 ? 2 : 4);
+            const int nwb = ct >= 4 ? 1 : (ct >= 2 ? 2 : 4);
             const double s1 = Wp * (60.0 * ct + 30.0 * RBW + 12.0 * RBW * ct) + std::ceil(double(Wp) / nwb - 1.0) * 700.0;
             const double s2 = std::ceil(double(RW / 16) * ct / kWarps) * Kw2 * 40.0;
             const double red = double(16 * RBW * G1) * cpad / kThreads * (KP + 2.0 * C) * 8.0;
-            const double cost = waves * (1500.0 + (C > 1 ? 900.0 : 0.0)) + per_sm * (s1 + s2 + red);
+            // measured on B300: every CTA costs about 400 clocks of launch and
+            // prologue on its SM, so fewer, fatter CTAs win until stage 2 dominates
+            const double cost = waves * (1500.0 + (C > 1 ? 900.0 : 0.0)) + per_sm * (s1 + s2 + red) +
+                                400.0 * double(problems) * grid / num_sms;
             if (cost < best_cost) {
                 best_cost = cost;
                 best.CT = ct;
