@@ -187,7 +187,8 @@ int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
     using namespace dbfk;
     const int ell = f->ell;
     const int64_t C = ell * T;
-    if (C > (int64_t(1) << 30)) return DBF_ERR_UNSUPPORTED;
+    // activation tiles are the second grid dimension (at most 65535 of them)
+    if (ceil_div(C, prefill_bn(ell)) > 65535) return DBF_ERR_UNSUPPORTED;
     const int ldxs = static_cast<int>(xs_ld(f->M));
     const int ldv = static_cast<int>(v_ld(f->R));
     __half *xs = static_cast<__half *>(ws);

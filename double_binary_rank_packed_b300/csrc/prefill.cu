@@ -64,8 +64,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
     constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int col0 = blockIdx.x * BN;   // first activation row (token*ell + term)
-    const int row0 = blockIdx.y * 128;  // first weight row
+    // weight row blocks vary fastest across the grid: the CTAs resident at one
+    // time share a few activation tiles, which stay in L2 while every row
+    // block of the weights consumes them
+    const int row0 = blockIdx.x * 128;  // first weight row
+    const int col0 = blockIdx.y * BN;   // first activation row (token*ell + term)
     const int nk = a.nk;
 
     if (threadIdx.x == 0) {
@@ -319,28 +322,77 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
 }
 
 // x [T][M] bf16 -> X' [T*ell + i][ldxs] fp16 in activation order, zero past M.
+// One thread per (token, 32-group g, half q): the 8 k at 32g + 8q and the 8
+// at 32g + 8q + 16 become the 16 consecutive logical positions 32g + 16q ..
+// (see perm32_pos), written as two 16-byte stores per term.  16-byte loads
+// of x and gamma when M is a multiple of 8, element loads otherwise.
 __global__ void pf_prologue_kernel(const __nv_bfloat16 *__restrict__ x, int T, int M, int ldx,
                                    const __half *__restrict__ gamma, int ell, __half *__restrict__ xs, int ldxs) {
     pdl_trigger();
     pdl_wait();
     const int groups = ldxs / 32;
-    const int64_t total = static_cast<int64_t>(T) * groups * 16;
+    const bool vec = ((M & 7) == 0) && ((ldx & 7) == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(gamma) & 15) == 0);
+    const int64_t total = static_cast<int64_t>(T) * groups * 2;
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int s = static_cast<int>(e & 15);
-        const int64_t tg = e >> 4;
+        const int q = static_cast<int>(e & 1);
+        const int64_t tg = e >> 1;
         const int g = static_cast<int>(tg % groups);
         const int t = static_cast<int>(tg / groups);
-        const int k = 32 * g + s;
+        const int k0 = 32 * g + 8 * q;  // first physical k of the low half; the high half is k0 + 16
         const __nv_bfloat16 *xr = x + static_cast<size_t>(t) * ldx;
-        const float xlo = (k < M) ? __bfloat162float(xr[k]) : 0.f;
-        const float xhi = (k + 16 < M) ? __bfloat162float(xr[k + 16]) : 0.f;
+        float xa[8], xb[8];
+        if (vec && k0 + 24 <= M) {
+            const uint4 va = *reinterpret_cast<const uint4 *>(xr + k0);
+            const uint4 vb = *reinterpret_cast<const uint4 *>(xr + k0 + 16);
+            const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                xa[2 * j] = __uint_as_float(wa[j] << 16);
+                xa[2 * j + 1] = __uint_as_float(wa[j] & 0xFFFF0000u);
+                xb[2 * j] = __uint_as_float(wb[j] << 16);
+                xb[2 * j + 1] = __uint_as_float(wb[j] & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                xa[j] = (k0 + j < M) ? __bfloat162float(xr[k0 + j]) : 0.f;
+                xb[j] = (k0 + 16 + j < M) ? __bfloat162float(xr[k0 + 16 + j]) : 0.f;
+            }
+        }
         for (int i = 0; i < ell; ++i) {
             const __half *gi = gamma + static_cast<size_t>(i) * M;
-            const float glo = (k < M) ? __half2float(gi[k]) : 0.f;
-            const float ghi = (k + 16 < M) ? __half2float(gi[k + 16]) : 0.f;
-            *reinterpret_cast<__half2 *>(xs + (static_cast<size_t>(t) * ell + i) * ldxs + 32 * g + 2 * s) =
-                __floats2half2_rn(glo * xlo, ghi * xhi);
+            float ga[8], gb[8];
+            if (vec && k0 + 24 <= M) {
+                const uint4 ua = *reinterpret_cast<const uint4 *>(gi + k0);
+                const uint4 ub = *reinterpret_cast<const uint4 *>(gi + k0 + 16);
+                const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&wa[j]));
+                    const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&wb[j]));
+                    ga[2 * j] = fa.x;
+                    ga[2 * j + 1] = fa.y;
+                    gb[2 * j] = fb.x;
+                    gb[2 * j + 1] = fb.y;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    ga[j] = (k0 + j < M) ? __half2float(gi[k0 + j]) : 0.f;
+                    gb[j] = (k0 + 16 + j < M) ? __half2float(gi[k0 + 16 + j]) : 0.f;
+                }
+            }
+            uint32_t out[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const __half2 h = __floats2half2_rn(ga[j] * xa[j], gb[j] * xb[j]);
+                out[j] = *reinterpret_cast<const uint32_t *>(&h);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(xs + (static_cast<size_t>(t) * ell + i) * ldxs + 32 * g + 16 * q);
+            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
         }
     }
 }
@@ -356,7 +408,7 @@ cudaError_t launch_gemm_t(const CUtensorMap &map, const PfArgs &a, cudaStream_t 
     }
     const int rows_cover = (STAGE == 1) ? a.rows_store : a.rows;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((a.C + BN - 1) / BN, (rows_cover + 127) / 128, 1);
+    cfg.gridDim = dim3((rows_cover + 127) / 128, (a.C + BN - 1) / BN, 1);
     cfg.blockDim = dim3(kPfThreads, 1, 1);
     cfg.dynamicSmemBytes = PfSmem<BN>::kBytes;
     cfg.stream = stream;
@@ -385,7 +437,7 @@ int prefill_bn(int ell) { return ell == 3 ? 240 : 256; }
 
 cudaError_t launch_prefill_prologue(const __nv_bfloat16 *x, int T, int M, int ldx, const __half *gamma, int ell,
                                     __half *xs, int ldxs, cudaStream_t stream, bool pdl) {
-    const int64_t total = static_cast<int64_t>(T) * (ldxs / 32) * 16;
+    const int64_t total = static_cast<int64_t>(T) * (ldxs / 32) * 2;
     int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 148 * 16));
     if (blocks < 1) blocks = 1;
     cudaLaunchConfig_t cfg = {};
