@@ -43,7 +43,6 @@ from workloads import generators as G  # noqa: E402
 METRIC = "tokens/s + % roofline: HBM GB/s (decode T≤16), tensor-pipe util (T=2048)"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-KERNEL_SOURCES = ["decode.cu", "prefill.cu", "misc.cu", "common.cuh", "dbf_api.cu", "kernels.h"]
 
 
 # --------------------------------------------------------------------- setup
@@ -81,25 +80,26 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def sources_hash(files):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in files:
         with open(os.path.join(ROOT, "double_binary_rank_packed_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(workload_key):
-    """DRAM bytes per call from a committed ncu summary, if taken on the current kernels."""
+    """DRAM bytes per launch of the workload's dominant kernel, from the committed ncu
+    summary (profiles/dram_traffic.json), or None when the kernel sources changed since."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh)
     e = d.get(workload_key)
-    if not e or e.get("kernel_hash") != kernel_source_hash():
+    if not e or sources_hash(e["sources"]) != e.get("sources_hash"):
         return None
-    return e.get("dram_bytes_per_call")
+    return e.get("dram_bytes_per_launch")
 
 
 def aggregate(local_ms: float, local_units: float, dist_mod=None):
