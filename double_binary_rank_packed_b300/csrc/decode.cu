@@ -243,6 +243,18 @@ struct FusedSmem {
 };
 
 __host__ __device__ inline int fused_g1(int R, int RBW) { return ((R + 15) / 16 + RBW - 1) / RBW; }
+
+// Exchange of the fused kernel.  All-to-all: every CTA pushes its whole
+// partial u into every CTA of the cluster, one barrier.  Reduce-scatter +
+// broadcast: every row of the partial goes to the CTA that owns it, the owner
+// finishes v for its rows and broadcasts it, two barriers.  Measured on B300
+// the second barrier costs more than the all-to-all traffic it saves until a
+// chunk has 32 or more columns; the scatter also needs every CTA to own a
+// whole number of 8-row groups of v.
+__host__ __device__ inline bool fused_scatter(int C, int R, int CPAD) {
+    const int R2 = (R + 31) & ~31;
+    return CPAD >= 32 && C > 1 && R2 % (8 * C) == 0;
+}
 __host__ __device__ inline int fused_kp(int G1) { return G1 >= kWarps ? 1 : kWarps / G1; }
 
 __host__ __device__ inline FusedSmem fused_smem(int CPAD, int RBW, int Wc, int R, int RW, int ell, int C, bool acc) {
@@ -262,8 +274,8 @@ __host__ __device__ inline FusedSmem fused_smem(int CPAD, int RBW, int Wc, int R
     o += align16(size_t(ell) * RW * 2);
     L.red = o;
     o += align16(size_t(KP) * R1 * CPAD * 4);
-    L.slots = o;
-    o += align16(size_t(C) * R1 * CPAD * 4);  // slot q: the partial u of cluster rank q
+    L.slots = o;  // all-to-all: slot q = partial u of rank q; scatter: [C][R2/C][CPAD] of the owned rows
+    o += align16(fused_scatter(C, R, CPAD) ? size_t(C) * (R2 / C) * CPAD * 4 : size_t(C) * R1 * CPAD * 4);
     L.vs = o;
     o += align16(size_t(CPAD) * (R2 + 8) * 2);
     L.yst = o;
@@ -383,7 +395,10 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
     const bool xvec = ((M & 7) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0);
     const bool pairs_ok = ((N & 1) == 0);
     const uint32_t red_addr = smem_u32(red), slots_addr = smem_u32(slots), tile_addr = smem_u32(tile);
+    const uint32_t vs_addr = smem_u32(vs);
     const int RB2 = RW / 16;
+    const bool scatter = fused_scatter(C, R, CPAD);
+    const int RO = R2 / C;  // rows of v each CTA of the cluster finishes (scatter mode)
 
     for (int chunk = 0; chunk < nchunks; ++chunk) {
         const int tc0 = chunk * tpc;
@@ -450,40 +465,88 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
         }
         __syncthreads();
 
-        // ---- 4. sum the K parts, push the CTA's partial u into slot `rank` of every CTA
-        for (int e = tid; e < R1 * C4; e += kThreads) {
-            const int r = e / C4;
-            float4 u = *reinterpret_cast<const float4 *>(red + r * CPAD + 4 * c4);
-            for (int q = 1; q < KP; ++q) add4(u, *reinterpret_cast<const float4 *>(red + (q * R1 + r) * CPAD + 4 * c4));
-            const uint32_t off = slots_addr + 4u * static_cast<uint32_t>((rank * R1 + r) * CPAD + 4 * c4);
-            if (C > 1) {
-                for (int q = 0; q < C; ++q)
-                    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     mapa_shared(off, static_cast<uint32_t>(q))),
-                                 "f"(u.x), "f"(u.y), "f"(u.z), "f"(u.w)
-                                 : "memory");
-            } else {
-                *reinterpret_cast<float4 *>(slots + r * CPAD + 4 * c4) = u;
+        if (scatter) {
+            // ---- 4. sum the K parts; each row of the partial u goes to the CTA
+            //         that owns it (slot `rank` of owner r / RO)
+            const int rows_x = min(R1, R2);  // rows of u stage 2 reads (owner ranks < C)
+            for (int e = tid; e < rows_x * C4; e += kThreads) {
+                const int r = e / C4;
+                float4 u = *reinterpret_cast<const float4 *>(red + r * CPAD + 4 * c4);
+                for (int q = 1; q < KP; ++q)
+                    add4(u, *reinterpret_cast<const float4 *>(red + (q * R1 + r) * CPAD + 4 * c4));
+                const int owner = r / RO, rl = r - owner * RO;
+                asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(mapa_shared(
+                                 slots_addr + 4u * static_cast<uint32_t>((rank * RO + rl) * CPAD + 4 * c4),
+                                 static_cast<uint32_t>(owner))),
+                             "f"(u.x), "f"(u.y), "f"(u.z), "f"(u.w)
+                             : "memory");
             }
-        }
-        if (C > 1)
-            cluster_sync_all();  // every slot of every CTA is filled
-        else
-            __syncthreads();
+            cluster_sync_all();  // every owner holds the partials of its rows
 
-        // ---- 5. u = sum of the slots in rank order, v = beta * u (fp16, perm8 order)
-        for (int e = tid; e < R2 * C4; e += kThreads) {
-            const int r = e / C4;
-            float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < R1)
-                for (int q = 0; q < C; ++q) add4(u, *reinterpret_cast<const float4 *>(slots + (q * R1 + r) * CPAD + 4 * c4));
-            const float uu[4] = {u.x, u.y, u.z, u.w};
-            const int pos = perm8_pos(r);
+            // ---- 5. owner: u of its RO rows = sum over ranks (rank order), v =
+            //         beta * u (fp16) staged in perm8 order, then broadcast in
+            //         16-byte pieces into v of every CTA of the cluster
+            __half *stage = reinterpret_cast<__half *>(red);  // [CPAD][RO], free after step 4
+            for (int e = tid; e < CPAD * RO; e += kThreads) {
+                const int col = e / RO, rl = e - col * RO;
+                const int r = rank * RO + rl;
+                float u = 0.f;
+                if (r < R1)
+                    for (int q = 0; q < C; ++q) u += slots[(q * RO + rl) * CPAD + col];
+                const float v = __half2float(beta_s[(col % ell) * R2 + r]) * u;
+                stage[col * RO + (perm8_pos(r) - rank * RO)] = __float2half_rn(v);
+            }
+            __syncthreads();
+            const int pieces = CPAD * (RO / 8);
+            for (int e = tid; e < pieces * C; e += kThreads) {
+                const int q = e / pieces, pc = e - q * pieces;
+                const int col = pc / (RO / 8), k8 = pc - col * (RO / 8);
+                const uint4 val = *reinterpret_cast<const uint4 *>(stage + col * RO + 8 * k8);
+                const uint32_t dst = vs_addr + 2u * static_cast<uint32_t>(col * ldv + rank * RO + 8 * k8);
+                asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 mapa_shared(dst, static_cast<uint32_t>(q))),
+                             "r"(val.x), "r"(val.y), "r"(val.z), "r"(val.w)
+                             : "memory");
+            }
+            cluster_sync_all();  // v of every CTA is complete
+        } else {
+            // ---- 4. sum the K parts, push the CTA's partial u into slot `rank` of every CTA
+            for (int e = tid; e < R1 * C4; e += kThreads) {
+                const int r = e / C4;
+                float4 u = *reinterpret_cast<const float4 *>(red + r * CPAD + 4 * c4);
+                for (int q = 1; q < KP; ++q)
+                    add4(u, *reinterpret_cast<const float4 *>(red + (q * R1 + r) * CPAD + 4 * c4));
+                const uint32_t off = slots_addr + 4u * static_cast<uint32_t>((rank * R1 + r) * CPAD + 4 * c4);
+                if (C > 1) {
+                    for (int q = 0; q < C; ++q)
+                        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         mapa_shared(off, static_cast<uint32_t>(q))),
+                                     "f"(u.x), "f"(u.y), "f"(u.z), "f"(u.w)
+                                     : "memory");
+                } else {
+                    *reinterpret_cast<float4 *>(slots + r * CPAD + 4 * c4) = u;
+                }
+            }
+            if (C > 1)
+                cluster_sync_all();  // every slot of every CTA is filled
+            else
+                __syncthreads();
+
+            // ---- 5. u = sum of the slots in rank order, v = beta * u (fp16, perm8 order)
+            for (int e = tid; e < R2 * C4; e += kThreads) {
+                const int r = e / C4;
+                float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r < R1)
+                    for (int q = 0; q < C; ++q)
+                        add4(u, *reinterpret_cast<const float4 *>(slots + (q * R1 + r) * CPAD + 4 * c4));
+                const float uu[4] = {u.x, u.y, u.z, u.w};
+                const int pos = perm8_pos(r);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                vs[(4 * c4 + j) * ldv + pos] = __float2half_rn(__half2float(beta_s[term4[j] * R2 + r]) * uu[j]);
+                for (int j = 0; j < 4; ++j)
+                    vs[(4 * c4 + j) * ldv + pos] = __float2half_rn(__half2float(beta_s[term4[j] * R2 + r]) * uu[j]);
+            }
+            __syncthreads();
         }
-        __syncthreads();
 
         // ---- 6. stage 2 per (row block, column tile); y straight from the fragment
         for (int it = warp; it < RB2 * CT; it += kWarps) {
@@ -1023,7 +1086,7 @@ FusedPlan plan_fused(int N, int M, int R, int ell, int columns, int num_sms, int
         if (C > 1 && C > Kw1) break;
         const int Wc = (Kw1 + C - 1) / C;
         const int Wp = (Wc + KP - 1) / KP;
-        for (int RW = 16; RW <= 256; RW *= 2) {
+        for (int RW = 16; RW <= 1024; RW *= 2) {
             const int used = (N + RW - 1) / RW;          // CTAs that own output rows
             const int grid = ((used + C - 1) / C) * C;   // whole clusters
             const size_t smem = fused_smem(cpad, RBW, Wc, R, RW, ell, C, accumulate).total;

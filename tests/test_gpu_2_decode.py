@@ -72,7 +72,10 @@ def test_dbf_1p5_bits(cuda_lib, T):
 
 @pytest.mark.parametrize("N,M,R,ell,T,pad", [
     (257, 257, 33, 1, 3, 0), (300, 200, 77, 2, 5, 3), (130, 1000, 50, 3, 7, 0), (64, 96, 1, 4, 16, 1),
-    (33, 31, 640, 1, 2, 4), (512, 4100, 96, 2, 9, 0), (16, 16, 16, 1, 1, 0)])
+    (33, 31, 640, 1, 2, 4), (512, 4100, 96, 2, 9, 0), (16, 16, 16, 1, 1, 0),
+    # cluster exchange variants of the fused kernel (rows of u past round_up(R, 32), 8-row ownership)
+    (1024, 2048, 130, 2, 12, 0), (2048, 4096, 96, 2, 12, 0), (4096, 8192, 256, 1, 3, 0), (3000, 4096, 64, 1, 16, 1),
+    (4096, 4096, 64, 2, 16, 0)])
 def test_odd_shapes(cuda_lib, N, M, R, ell, T, pad):
     f = G.make_factors(N, M, R, ell, N + M + R)
     xb = G.make_x(T, M, N + M + R)
