@@ -208,6 +208,44 @@ def y_sampled(x64: np.ndarray, f, tokens, outputs) -> np.ndarray:
     return out
 
 
+def transpose_packed(words: np.ndarray, cols: int, ldw_t: int | None = None) -> np.ndarray:
+    """Packed words of the transposed sign matrix.
+
+    `words` holds a rows x cols sign matrix (see pack_signs); the result holds
+    its cols x rows transpose in the same format, row stride ldw_t words.
+    """
+    signs = unpack_words(words, cols)
+    return pack_signs(signs.T, ldw_t)
+
+
+def dx_factored(dy64: np.ndarray, f) -> np.ndarray:
+    """Input gradient of y = x dW^T for the output gradient dy [T, N]: dx [T, M].
+
+    dx = dy dW = sum_i gamma_i . B2^T (beta_i . (B1^T (alpha_i . dy))), the
+    backward pass of the sign-factor product that training through it needs
+    (LoRDBA page, section 2, Pipeline de Entrenamiento: the carriers and scales
+    are trained jointly, so the gradient flows back through both sign
+    matrices).  Term by term, in this order: scale dy by alpha_i, contract
+    with B1 over N, scale by beta_i, contract with B2 over R, scale by gamma_i.
+    """
+    alpha, beta, gamma = _scales(f)
+    dy = np.asarray(dy64, dtype=np.float64)
+    B1 = np.asarray(f.B1, dtype=np.float64)
+    B2 = np.asarray(f.B2, dtype=np.float64)
+    dx = np.zeros((dy.shape[0], B2.shape[1]), dtype=np.float64)
+    for i in range(alpha.shape[0]):
+        g = (dy * alpha[i][None, :]) @ B1      # B1^T (alpha_i . dy)   [T, R]
+        h = (g * beta[i][None, :]) @ B2        # B2^T (beta_i . g)     [T, M]
+        dx += h * gamma[i][None, :]
+    return dx
+
+
+def matmul_dx(dy_bits: np.ndarray, f):
+    """Reference for the backward call: (exact float64 dx, expected bf16 bits)."""
+    dx = dx_factored(bf16_bits_to_f64(dy_bits), f)
+    return dx, round_to_bf16_bits(dx)
+
+
 # --------------------------------------------------------------------------
 # what the library call must return
 # --------------------------------------------------------------------------

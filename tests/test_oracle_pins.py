@@ -277,3 +277,64 @@ def test_accumulate_mode_adds_before_single_rounding():
     branch, _ = O.matmul(xb, f)
     assert np.array_equal(y64, branch + O.bf16_bits_to_f64(y_in))
     assert np.array_equal(bits, O.round_to_bf16_bits(y64))
+
+
+# ---------------------------------------------------------- backward (dx)
+
+def test_transpose_packed_matches_transposed_signs_and_round_trips():
+    rng = np.random.default_rng(41)
+    for rows, cols, extra in [(1, 1, 0), (33, 70, 1), (64, 32, 0), (5, 200, 3)]:
+        s = np.where(rng.random((rows, cols)) < 0.5, 1, -1).astype(np.int8)
+        w = O.pack_signs(s)
+        wt = O.transpose_packed(w, cols, O.words_per_row(rows) + extra)
+        assert np.array_equal(O.unpack_words(wt, rows), s.T)
+        assert np.array_equal(O.transpose_packed(wt, rows, O.words_per_row(cols)), w)
+
+
+def test_transpose_packed_golden_word():
+    # a 32 x 32 block with only row 3 all +1: the transpose has bit 3 set in every word
+    s = -np.ones((32, 32), dtype=np.int8)
+    s[3, :] = 1
+    wt = O.transpose_packed(O.pack_signs(s), 32)
+    assert (wt[:, 0] == np.uint32(1 << 3)).all()
+
+
+@pytest.mark.parametrize("N,M,R,ell,seed", [(8, 8, 4, 1, 5), (40, 24, 9, 2, 6), (17, 33, 12, 3, 7)])
+def test_dx_equals_dy_times_dense_update(N, M, R, ell, seed):
+    f = G.make_factors(N, M, R, ell, seed)
+    dy = np.random.default_rng(seed).standard_normal((5, N))
+    np.testing.assert_allclose(O.dx_factored(dy, f), dy @ O.dense_delta_w(f), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("ell", [1, 2, 4])
+def test_adjoint_identity(ell):
+    # <x dW^T, dy> = <x, dy dW> for any x and dy: the backward product is the adjoint of the forward one
+    f = G.make_factors(30, 20, 7, ell, 60 + ell)
+    rng = np.random.default_rng(70 + ell)
+    x = rng.standard_normal((6, 20))
+    dy = rng.standard_normal((6, 30))
+    lhs = float((O.y_factored(x, f) * dy).sum())
+    rhs = float((x * O.dx_factored(dy, f)).sum())
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+
+
+def test_dx_is_the_forward_product_of_the_transposed_factors():
+    # the library computes dx with its forward kernels on (B2^T, B1^T, gamma, beta, alpha)
+    f = G.make_factors(24, 40, 10, 2, 80)
+    ft = Factors(np.ascontiguousarray(f.B2.T), np.ascontiguousarray(f.B1.T), f.gamma, f.beta, f.alpha)
+    dy = np.random.default_rng(81).standard_normal((3, 24))
+    np.testing.assert_allclose(O.y_factored(dy, ft), O.dx_factored(dy, f), rtol=1e-12, atol=1e-12)
+
+
+def test_dx_bruteforce_tiny():
+    f = G.make_factors(8, 8, 4, 2, 90)
+    dy = np.random.default_rng(91).standard_normal((2, 8))
+    alpha, beta, gamma = (O.fp16_to_f64(a) for a in (f.alpha, f.beta, f.gamma))
+    want = np.zeros((2, 8))
+    for t in range(2):
+        for m in range(8):
+            for i in range(2):
+                for r in range(4):
+                    for n in range(8):
+                        want[t, m] += gamma[i, m] * f.B2[r, m] * beta[i, r] * f.B1[n, r] * alpha[i, n] * dy[t, n]
+    np.testing.assert_allclose(O.dx_factored(dy, f), want, rtol=1e-12, atol=1e-12)
