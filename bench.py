@@ -226,6 +226,8 @@ def to_device_factors(dbf, f):
 
 
 def clone_factors(dbf, pf):
+    """A copy of a factor set in fresh device memory (a transposed set clones into the plain
+    descriptor of the same product)."""
     return dbf.PackedFactors(pf.B1w.clone(), pf.B2w.clone(), pf.alpha.clone(), pf.beta.clone(),
                              pf.gamma.clone(), pf.N, pf.M, pf.R)
 
@@ -244,7 +246,9 @@ def call_footprint(N, M, R, ell, T, ldw1, ldw2):
 class DecodeWorkload:
     """L independent dbf_matmul calls per step (streamed decode)."""
 
-    def __init__(self, dbf, key, proj, T, outlier_scale=0.0, max_calls=4096):
+    def __init__(self, dbf, key, proj, T, outlier_scale=0.0, max_calls=4096, transposed=False):
+        """transposed: time the backward product dx = dy dW (dy [T, N] -> dx [T, M]) through the
+        transposed factors instead of the forward one."""
         import torch
         self.dbf, self.key, self.T = dbf, key, T
         self.N, self.M, self.R, self.ell = proj.N, proj.M, proj.R, proj.ell
@@ -252,11 +256,15 @@ class DecodeWorkload:
         base = to_device_factors(dbf, f)
         fp = call_footprint(self.N, self.M, self.R, self.ell, T, base.B1w.shape[1], base.B2w.shape[1])
         self.L = int(min(max_calls, max(8, math.ceil(4 * L2_BYTES / fp))))
-        xb = G.make_x(T, proj.M, proj.seed, outlier_scale=outlier_scale)
+        if transposed:
+            base = dbf.TransposedFactors(base)
+            xb = G.make_x(T, proj.N, proj.seed + 7)
+        else:
+            xb = G.make_x(T, proj.M, proj.seed, outlier_scale=outlier_scale)
         x0 = bf16_dev(xb)
         self.factors = [base] + [clone_factors(dbf, base) for _ in range(self.L - 1)]
         self.x = [x0] + [x0.clone() for _ in range(self.L - 1)]
-        self.y = [torch.empty((T, proj.N), dtype=torch.bfloat16, device="cuda") for _ in range(self.L)]
+        self.y = [torch.empty((T, base.N), dtype=torch.bfloat16, device="cuda") for _ in range(self.L)]
         self.ws = dbf.new_workspace(dbf.workspace_bytes(base, T), "cuda")
         self.launches_per_call = dbf.launch_count(base, T)
         self.fp_call = fp
@@ -297,17 +305,22 @@ class DecodeWorkload:
 
 
 class PrefillWorkload:
-    """The DBF MLP layer: up- and down-projection calls per step."""
+    """The DBF MLP layer: up- and down-projection calls per step (or, transposed, their
+    backward products dx = dy dW)."""
 
-    def __init__(self, dbf, key, projs, T):
+    def __init__(self, dbf, key, projs, T, transposed=False):
         import torch
         self.dbf, self.key, self.T = dbf, key, T
         self.items = []
         for p in projs:
             f = G.make_factors(p.N, p.M, p.R, p.ell, p.seed, p.sign_mode, p.scale_mode)
             pf = to_device_factors(dbf, f)
-            x = bf16_dev(G.make_x(T, p.M, p.seed))
-            y = torch.empty((T, p.N), dtype=torch.bfloat16, device="cuda")
+            if transposed:
+                pf = dbf.TransposedFactors(pf)
+                x = bf16_dev(G.make_x(T, p.N, p.seed + 7))
+            else:
+                x = bf16_dev(G.make_x(T, p.M, p.seed))
+            y = torch.empty((T, pf.N), dtype=torch.bfloat16, device="cuda")
             ws = dbf.new_workspace(dbf.workspace_bytes(pf, T), "cuda")
             self.items.append((pf, x, y, ws, p))
             del f
@@ -567,6 +580,10 @@ def make_workload(dbf, key, max_calls=None):
     cap = {} if max_calls is None else {"max_calls": max_calls}
     name, _, tok = key.rpartition("_T")
     T = int(tok)
+    if name == "adapter4k_dx":
+        return DecodeWorkload(dbf, key, CFG.ADAPTER_4K.projections[0], T, transposed=True, **cap)
+    if name == "dbfmlp_dx":
+        return PrefillWorkload(dbf, key, CFG.DBF_MLP.projections, T, transposed=True)
     if name == "adapter4k":
         return DecodeWorkload(dbf, key, CFG.ADAPTER_4K.projections[0], T, **cap)
     if name == "dbf1p5":
@@ -587,10 +604,12 @@ WORKLOAD_TITLES = {
     "tiny": "tiny: N=M=256 R=32 ell=1, T={T} tokens",
     "multiadapter": "multiadapter: 64 adapters N=M=4096 R=32 ell=2, T={T} routed decode tokens",
     "dbfmlp": "dbfmlp: DBF MLP up 14336x4096 + down 4096x14336, R=5013 ell=2, T={T} prefill tokens",
+    "adapter4k_dx": "adapter4k_dx: backward dx = dy dW of the LoRDBA adapter branch N=M=4096 R=64 ell=1, T={T}",
+    "dbfmlp_dx": "dbfmlp_dx: backward dx = dy dW of the DBF MLP up + down projections, R=5013 ell=2, T={T}",
 }
 
 SECONDARY = ["adapter4k_T1", "adapter4k_T4", "dbf1p5_T1", "dbf1p5_T8", "tiny_T8", "multiadapter_T256",
-             "dbfmlp_T2048"]
+             "dbfmlp_T2048", "adapter4k_dx_T16", "dbfmlp_dx_T2048"]
 
 
 def main(argv=None):

@@ -286,6 +286,41 @@ int dbf_unpack(const uint32_t *words, int64_t rows, int64_t cols, int64_t ldw, i
     return e == cudaSuccess ? DBF_OK : cuda_fail(e, "dbf_unpack");
 }
 
+int dbf_transpose_packed(const uint32_t *words, int64_t rows, int64_t cols, int64_t ldw, uint32_t *words_t,
+                         int64_t ldw_t, void *stream) {
+    if (rows < 0 || cols < 0) return DBF_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return DBF_OK;
+    if (!words || !words_t) return DBF_ERR_INVALID_ARG;
+    if (ldw < ceil_div(cols, 32) || ldw_t < ceil_div(rows, 32)) return DBF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(words) & 3) != 0 || (reinterpret_cast<uintptr_t>(words_t) & 3) != 0)
+        return DBF_ERR_ALIGNMENT;
+    cudaError_t e = dbfk::launch_transpose(words, rows, cols, ldw, words_t, ldw_t, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "dbf_transpose_packed");
+}
+
+int dbf_factors_transposed(const dbf_factors *f, const uint32_t *B2T, int32_t ldw_b2t, const uint32_t *B1T,
+                           int32_t ldw_b1t, dbf_factors *out) {
+    const int rc = check_factors(f);
+    if (rc) return rc;
+    if (!out || !B2T || !B1T) return DBF_ERR_INVALID_ARG;
+    if (ldw_b2t < ceil_div(f->R, 32) || ldw_b1t < ceil_div(f->N, 32)) return DBF_ERR_INVALID_ARG;
+    if (!aligned16(B2T) || !aligned16(B1T)) return DBF_ERR_ALIGNMENT;
+    dbf_factors t = {};
+    t.N = f->M;
+    t.M = f->N;
+    t.R = f->R;
+    t.ell = f->ell;
+    t.B1 = B2T;
+    t.ldw1 = ldw_b2t;
+    t.B2 = B1T;
+    t.ldw2 = ldw_b1t;
+    t.alpha = f->gamma;
+    t.beta = f->beta;
+    t.gamma = f->alpha;
+    *out = t;
+    return DBF_OK;
+}
+
 size_t dbf_workspace_bytes_path(const dbf_factors *f, int64_t T, int path) {
     if (check_factors(f) != DBF_OK || T < 0) return 0;
     if (path < DBF_PATH_AUTO || path > DBF_PATH_PREFILL) return 0;

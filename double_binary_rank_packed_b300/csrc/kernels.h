@@ -149,6 +149,8 @@ cudaError_t launch_pack(const int8_t *signs, int64_t rows, int64_t cols, uint32_
                         cudaStream_t stream);
 cudaError_t launch_unpack(const uint32_t *words, int64_t rows, int64_t cols, int64_t ldw, int8_t *signs,
                           cudaStream_t stream);
+cudaError_t launch_transpose(const uint32_t *words, int64_t rows, int64_t cols, int64_t ldw, uint32_t *words_t,
+                             int64_t ldw_t, cudaStream_t stream);
 cudaError_t launch_selftest_wait(int *status, uint64_t limit_ns, cudaStream_t stream);
 
 // Text returned by dbf_last_cuda_error() on this thread.

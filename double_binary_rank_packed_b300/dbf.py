@@ -37,7 +37,7 @@ EXPORTED = (
     "dbf_decode_max_tokens", "dbf_matmul", "dbf_matmul_path", "dbf_hostio_workspace_bytes",
     "dbf_matmul_hostio", "dbf_segmented_workspace_bytes", "dbf_matmul_segmented",
     "dbf_check_status", "dbf_selftest_bounded_wait", "dbf_status_string", "dbf_last_cuda_error",
-    "dbf_launch_count", "dbf_segmented_launch_count",
+    "dbf_launch_count", "dbf_segmented_launch_count", "dbf_transpose_packed", "dbf_factors_transposed",
 )
 
 
@@ -86,6 +86,8 @@ def _load():
         "dbf_status_string": (ctypes.c_char_p, [ci]),
         "dbf_last_cuda_error": (ctypes.c_char_p, []),
         "dbf_launch_count": (ci, [fp, i64, ci]),
+        "dbf_transpose_packed": (ci, [vp, i64, i64, i64, vp, i64, vp]),
+        "dbf_factors_transposed": (ci, [fp, vp, i32, vp, i32, fp]),
         "dbf_segmented_launch_count": (ci, [i32, i32, i32, i32, i64, i32]),
     }
     for name, (res, args) in sig.items():
@@ -148,6 +150,17 @@ def unpack(words: torch.Tensor, cols: int, stream=None) -> torch.Tensor:
     return signs
 
 
+def transpose_packed(words: torch.Tensor, cols: int, ldw_t: int | None = None, stream=None) -> torch.Tensor:
+    """Packed transpose of a rows x cols packed sign matrix (dbf_transpose_packed)."""
+    rows, ldw = words.shape
+    if ldw_t is None:
+        ldw_t = words_per_row(rows)
+    out = torch.empty((cols, ldw_t), dtype=torch.int32, device=words.device)
+    _check(_lib.dbf_transpose_packed(_ptr(words), rows, cols, ldw, _ptr(out), ldw_t, _stream_handle(stream)),
+           "dbf_transpose_packed")
+    return out
+
+
 # ------------------------------------------------------------------ factors
 
 class PackedFactors:
@@ -180,6 +193,26 @@ class PackedFactors:
 
     def struct_bytes(self) -> bytes:
         return ctypes.string_at(ctypes.addressof(self._struct), ctypes.sizeof(DbfFactors))
+
+
+class TransposedFactors(PackedFactors):
+    """Factors of the backward product dx = dy dW (dbf_factors_transposed).
+
+    Holds the packed transposes of B1 and B2 (made once with
+    dbf_transpose_packed) and shares the scale tensors of `f`; use it with
+    matmul / matmul_path: matmul(TransposedFactors(f), dy) is dx.
+    """
+
+    def __init__(self, f: PackedFactors, stream=None):
+        self.source = f
+        self.B1w = transpose_packed(f.B2w, f.M, stream=stream)  # B2^T: [M][ceil(R/32)]
+        self.B2w = transpose_packed(f.B1w, f.R, stream=stream)  # B1^T: [R][ceil(N/32)]
+        self.alpha, self.beta, self.gamma = f.gamma, f.beta, f.alpha
+        self.N, self.M, self.R, self.ell = f.M, f.N, f.R, f.ell
+        self._struct = DbfFactors()
+        _check(_lib.dbf_factors_transposed(ctypes.byref(f.struct), _ptr(self.B1w), int(self.B1w.shape[1]),
+                                           _ptr(self.B2w), int(self.B2w.shape[1]), ctypes.byref(self._struct)),
+               "dbf_factors_transposed")
 
 
 def workspace_bytes(f: PackedFactors, T: int, path: int = PATH_AUTO) -> int:

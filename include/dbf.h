@@ -99,6 +99,36 @@ int dbf_pack(const int8_t *signs, int64_t rows, int64_t cols,
 int dbf_unpack(const uint32_t *words, int64_t rows, int64_t cols, int64_t ldw,
                int8_t *signs, void *stream);
 
+/*
+ * dbf_transpose_packed: packed sign matrix -> packed transpose.
+ *   words    device uint32 [rows][ldw], a rows x cols sign matrix in the
+ *            dbf_pack format (ldw >= ceil(cols/32))
+ *   words_t  device uint32 [cols][ldw_t], receives the cols x rows transpose
+ *            in the same format (ldw_t >= ceil(rows/32)); pad bits and pad
+ *            words are written as 0
+ * Both 4-byte aligned.  Setup operation for the backward product (the sign
+ * matrices transposed once per factor set).
+ */
+int dbf_transpose_packed(const uint32_t *words, int64_t rows, int64_t cols, int64_t ldw,
+                         uint32_t *words_t, int64_t ldw_t, void *stream);
+
+/*
+ * dbf_factors_transposed: descriptor of the backward (input-gradient) product
+ *     dx = dy dW = sum_i gamma_i . B2^T (beta_i . (B1^T (alpha_i . dy)))
+ * for dy [T][N] -> dx [T][M], the gradient that training through the
+ * sign-factor product needs (LoRDBA page, section 2, Pipeline de
+ * Entrenamiento: carriers and scales are trained jointly).  It has the form
+ * of the forward product with N' = M, M' = N, B1' = B2^T, B2' = B1^T,
+ * alpha' = gamma, beta' = beta, gamma' = alpha, so dbf_matmul (any path) with
+ * *out computes dx.  Host only: fills *out from f and the two transposes
+ * (from dbf_transpose_packed):
+ *   B2T  device uint32 [M][ldw_b2t], transpose of B2 (ldw_b2t >= ceil(R/32))
+ *   B1T  device uint32 [R][ldw_b1t], transpose of B1 (ldw_b1t >= ceil(N/32))
+ * 16-byte aligned.  The scale vectors are shared with f (no copy).
+ */
+int dbf_factors_transposed(const dbf_factors *f, const uint32_t *B2T, int32_t ldw_b2t,
+                           const uint32_t *B1T, int32_t ldw_b1t, dbf_factors *out);
+
 /* Device workspace (bytes) dbf_matmul needs for this shape and token count. */
 size_t dbf_workspace_bytes(const dbf_factors *f, int64_t T);
 
