@@ -122,6 +122,20 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// True in exactly one lane of a fully converged warp (elect.sync).  Single-
+// thread tcgen05/TMA issue goes through this inside a loop that the whole warp
+// runs: with the loop's waits and branches taken by one lane alone, the tensor
+// pipe was measured at about half its rate on 128 x 128 .. 256 tiles.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Arrive once on `bar` when all tcgen05.mma issued so far by this thread
 // have completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {

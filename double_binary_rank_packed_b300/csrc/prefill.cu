@@ -10,7 +10,9 @@
 // GEMM design (one CTA = 128 weight rows x BN activation rows, 192 threads):
 //   warp 0      TMA producer: 64-wide K slices of the activation tile
 //               (128-byte swizzle) into a 6-stage shared-memory ring
-//   warp 1      allocates tensor memory; one lane issues tcgen05.mma
+//   warp 1      allocates tensor memory and issues tcgen05.mma
+//   (both loops run on the whole converged warp, one elect.sync lane issuing:
+//   a loop run by one lane alone left the tensor pipe near half rate)
 //   warps 2..5  unpack: each thread owns one weight row (= one TMEM lane),
 //               reads two packed words per K step and writes 32 columns of
 //               +-1 fp16 pairs straight into tensor memory with tcgen05.st;
@@ -95,49 +97,55 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            pdl_wait();  // the activations are written by the previous kernel
-            int issued = 0;
-            for (int ks = 0; ks < nk; ++ks) {
-                const int s = ks % kStages;
-                const uint32_t n = ks / kStages;
-                if (!mbar_wait_bounded(&empty[s], (n & 1) ^ 1, abort_flag)) {
-                    *abort_flag = 1;
-                    record_status(a.status, DBF_ERR_TIMEOUT);
-                    break;
-                }
+        // the whole warp runs the loop; one elected lane issues each copy
+        pdl_wait();  // the activations are written by the previous kernel
+        int issued = 0;
+        for (int ks = 0; ks < nk; ++ks) {
+            const int s = ks % kStages;
+            const uint32_t n = ks / kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (n & 1) ^ 1, abort_flag))) {
+                *abort_flag = 1;
+                record_status(a.status, DBF_ERR_TIMEOUT);
+                break;
+            }
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&act_full[s], PfSmem<BN>::kTileBytes);
                 tma_load_2d(smem + s * PfSmem<BN>::kTileBytes, &act_map, &act_full[s], ks * kBK, col0);
-                ++issued;
             }
-            if (*abort_flag) {
-                // let every copy still in flight land before the block can exit
-                for (int ks = (issued > kStages ? issued - kStages : 0); ks < issued; ++ks)
-                    mbar_wait_bounded(&act_full[ks % kStages], (ks / kStages) & 1, nullptr);
-            }
+            __syncwarp();
+            ++issued;
+        }
+        if (*abort_flag && lane == 0) {
+            // let every copy still in flight land before the block can exit
+            for (int ks = (issued > kStages ? issued - kStages : 0); ks < issued; ++ks)
+                mbar_wait_bounded(&act_full[ks % kStages], (ks / kStages) & 1, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int issued = 0;
-            for (int ks = 0; ks < nk; ++ks) {
-                const int s = ks % kStages;
-                const uint32_t par = (ks / kStages) & 1;
-                if (!mbar_wait_bounded(&act_full[s], par, abort_flag) ||
-                    !mbar_wait_bounded(&a_full[s], par, abort_flag)) {
-                    *abort_flag = 1;
-                    record_status(a.status, DBF_ERR_TIMEOUT);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a_col = tmem + kAccCols + s * 32;
-                const uint32_t b_addr = smem_u32(smem + s * PfSmem<BN>::kTileBytes);
+        // the whole warp runs the loop; one elected lane issues the MMAs and
+        // the commits
+        for (int ks = 0; ks < nk; ++ks) {
+            const int s = ks % kStages;
+            const uint32_t par = (ks / kStages) & 1;
+            const bool ready =
+                mbar_wait_bounded(&act_full[s], par, abort_flag) && mbar_wait_bounded(&a_full[s], par, abort_flag);
+            if (!__all_sync(0xffffffffu, ready)) {
+                *abort_flag = 1;
+                record_status(a.status, DBF_ERR_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a_col = tmem + kAccCols + s * 32;
+            const uint32_t b_addr = smem_u32(smem + s * PfSmem<BN>::kTileBytes);
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)
                     tc_mma_ts(tmem, a_col + kk * 8, desc_sw128(b_addr + kk * 32), kIdesc, (ks | kk) != 0);
                 tc_commit(&empty[s]);
-                ++issued;
             }
+            __syncwarp();
+        }
+        if (elect_one()) {
             if (*abort_flag) {
                 tc_commit(drain);
                 mbar_wait_bounded(drain, 0, nullptr);
@@ -145,6 +153,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
                 tc_commit(acc_full);
             }
         }
+        __syncwarp();
     } else {
         // ------------------------------------------------ unpack, then epilogue
         const int q = warp & 3;                // TMEM lane quarter this warp may access
