@@ -240,6 +240,45 @@ def dx_factored(dy64: np.ndarray, f) -> np.ndarray:
     return dx
 
 
+def scale_grads_f64(x64: np.ndarray, dy64: np.ndarray, f):
+    """Gradients of L = sum_t <dy_t, y_t> with respect to the scale vectors.
+
+    Training through the product updates the scales together with the sign
+    carriers (LoRDBA page, section 2, Pipeline de Entrenamiento), so besides
+    dx it needs, for each envelope term i and the output gradient dy [T, N]:
+      dalpha_i[n] = sum_t dy_t[n] * (B1 (beta_i . B2 (gamma_i . x_t)))[n]
+      dbeta_i[r]  = sum_t (B1^T (alpha_i . dy_t))[r] * (B2 (gamma_i . x_t))[r]
+      dgamma_i[k] = sum_t x_t[k] * (B2^T (beta_i . B1^T (alpha_i . dy_t)))[k]
+    (y is linear in each of alpha_i, beta_i, gamma_i, so these are the
+    coefficients of that linear dependence).  The intermediates are formed
+    term by term in the order of the forward and backward products.
+    Returns (dalpha [ell, N], dbeta [ell, R], dgamma [ell, M]) in float64.
+    """
+    alpha, beta, gamma = _scales(f)
+    x = np.asarray(x64, dtype=np.float64)
+    dy = np.asarray(dy64, dtype=np.float64)
+    B1 = np.asarray(f.B1, dtype=np.float64)
+    B2 = np.asarray(f.B2, dtype=np.float64)
+    ell = alpha.shape[0]
+    dalpha = np.zeros((ell, B1.shape[0]))
+    dbeta = np.zeros((ell, B1.shape[1]))
+    dgamma = np.zeros((ell, B2.shape[1]))
+    for i in range(ell):
+        h = (x * gamma[i][None, :]) @ B2.T      # B2 (gamma_i . x_t)        [T, R]
+        u = (h * beta[i][None, :]) @ B1.T       # B1 (beta_i . h_t)         [T, N]
+        g = (dy * alpha[i][None, :]) @ B1       # B1^T (alpha_i . dy_t)     [T, R]
+        w = (g * beta[i][None, :]) @ B2         # B2^T (beta_i . g_t)       [T, M]
+        dalpha[i] = (dy * u).sum(axis=0)
+        dbeta[i] = (g * h).sum(axis=0)
+        dgamma[i] = (x * w).sum(axis=0)
+    return dalpha, dbeta, dgamma
+
+
+def scale_grads(x_bits: np.ndarray, dy_bits: np.ndarray, f):
+    """Reference for the backward call's scale gradients from bf16 x and dy."""
+    return scale_grads_f64(bf16_bits_to_f64(x_bits), bf16_bits_to_f64(dy_bits), f)
+
+
 def matmul_dx(dy_bits: np.ndarray, f):
     """Reference for the backward call: (exact float64 dx, expected bf16 bits)."""
     dx = dx_factored(bf16_bits_to_f64(dy_bits), f)

@@ -338,3 +338,98 @@ def test_dx_bruteforce_tiny():
                     for n in range(8):
                         want[t, m] += gamma[i, m] * f.B2[r, m] * beta[i, r] * f.B1[n, r] * alpha[i, n] * dy[t, n]
     np.testing.assert_allclose(O.dx_factored(dy, f), want, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------ scale gradients
+
+def _loss_dense(x, dy, f):
+    # L = sum_t <dy_t, y_t> through the dense route (dW built explicitly)
+    return float((O.y_dense(x, f) * dy).sum())
+
+
+def _with(f, **kw):
+    d = dict(B1=f.B1, B2=f.B2, alpha=f.alpha, beta=f.beta, gamma=f.gamma)
+    d.update(kw)
+    return Factors(d["B1"], d["B2"], d["alpha"], d["beta"], d["gamma"])
+
+
+@pytest.mark.parametrize("N,M,R,ell,seed", [(12, 9, 5, 1, 11), (30, 20, 7, 2, 12), (17, 33, 12, 3, 13)])
+def test_scale_grads_are_the_directional_derivatives(N, M, R, ell, seed):
+    # y is linear in each scale vector, so for a new fp16 vector s' the change of L is exactly
+    # <d, s' - s> (the difference of two fp16 numbers is exact in float64)
+    f = G.make_factors(N, M, R, ell, seed)
+    rng = np.random.default_rng(seed + 1)
+    x = rng.standard_normal((6, M))
+    dy = rng.standard_normal((6, N))
+    da, db, dg = O.scale_grads_f64(x, dy, f)
+    L0 = _loss_dense(x, dy, f)
+    for name, d in (("alpha", da), ("beta", db), ("gamma", dg)):
+        old = getattr(f, name)
+        new = (rng.standard_normal(old.shape) * 0.5).astype(np.float16)
+        L1 = _loss_dense(x, dy, _with(f, **{name: new}))
+        pred = float((d * (new.astype(np.float64) - old.astype(np.float64))).sum())
+        assert abs((L1 - L0) - pred) <= 1e-10 * max(1.0, abs(L0), abs(L1)), name
+
+
+@pytest.mark.parametrize("ell", [1, 2, 4])
+def test_scale_grads_euler_identity_per_term(ell):
+    # L is linear in alpha_i, in beta_i and in gamma_i, so <alpha_i, dalpha_i> = <beta_i, dbeta_i>
+    # = <gamma_i, dgamma_i> = the share of term i in L, computed here with term i alone
+    f = G.make_factors(26, 19, 8, ell, 40 + ell)
+    rng = np.random.default_rng(50 + ell)
+    x = rng.standard_normal((5, 19))
+    dy = rng.standard_normal((5, 26))
+    da, db, dg = O.scale_grads_f64(x, dy, f)
+    a, b, g = (O.fp16_to_f64(v) for v in (f.alpha, f.beta, f.gamma))
+    for i in range(ell):
+        fi = _with(f, alpha=f.alpha[i:i + 1], beta=f.beta[i:i + 1], gamma=f.gamma[i:i + 1])
+        Li = _loss_dense(x, dy, fi)
+        for v, d in ((a, da), (b, db), (g, dg)):
+            assert abs(float(v[i] @ d[i]) - Li) <= 1e-11 * max(1.0, abs(Li))
+
+
+def test_scale_grads_all_ones_signs_closed_form():
+    # B1 = B2 = all +1: B2 (gamma . x) has every entry s = gamma . x, B1^T (alpha . dy) every entry
+    # p = alpha . dy, so dalpha = sum_t dy_t * sum(beta) * s_t, dbeta = sum_t p_t s_t (same for
+    # every r) and dgamma = sum_t x_t * sum(beta) * p_t
+    N, M, R, ell = 9, 7, 5, 2
+    f = G.make_factors(N, M, R, ell, 31)
+    f = _with(f, B1=np.ones((N, R), dtype=np.int8), B2=np.ones((R, M), dtype=np.int8))
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((4, M))
+    dy = rng.standard_normal((4, N))
+    da, db, dg = O.scale_grads_f64(x, dy, f)
+    a, b, g = (O.fp16_to_f64(v) for v in (f.alpha, f.beta, f.gamma))
+    for i in range(ell):
+        s = x @ g[i]            # [T]
+        p = dy @ a[i]           # [T]
+        np.testing.assert_allclose(da[i], b[i].sum() * (dy * s[:, None]).sum(0), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(db[i], np.full(R, (p * s).sum()), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dg[i], b[i].sum() * (x * p[:, None]).sum(0), rtol=1e-12, atol=1e-12)
+
+
+def test_scale_grad_pins_catch_a_transposed_carrier(monkeypatch):
+    # plant a plausible mistake in the oracle (B2 used as if it were square-transposed: the
+    # dgamma path contracts with B2 reversed along r) and check that the derivative pin sees it
+    f = G.make_factors(10, 10, 10, 1, 21)
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((3, 10))
+    dy = rng.standard_normal((3, 10))
+    good = O.scale_grads_f64(x, dy, f)
+    bad_f = _with(f, B2=np.ascontiguousarray(f.B2[::-1]))
+    real = O.scale_grads_f64
+
+    def planted(x64, dy64, ff):
+        da, db, _ = real(x64, dy64, ff)
+        _, _, dg = real(x64, dy64, bad_f)
+        return da, db, dg
+
+    monkeypatch.setattr(O, "scale_grads_f64", planted)
+    da, db, dg = O.scale_grads_f64(x, dy, f)
+    L0 = _loss_dense(x, dy, f)
+    new = (rng.standard_normal(f.gamma.shape) * 0.5).astype(np.float16)
+    L1 = _loss_dense(x, dy, _with(f, gamma=new))
+    pred_bad = float((dg * (new.astype(np.float64) - f.gamma.astype(np.float64))).sum())
+    pred_good = float((good[2] * (new.astype(np.float64) - f.gamma.astype(np.float64))).sum())
+    assert abs((L1 - L0) - pred_good) <= 1e-10 * max(1.0, abs(L0))
+    assert abs((L1 - L0) - pred_bad) > 1e-6 * max(1.0, abs(L0))
