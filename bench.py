@@ -351,6 +351,58 @@ class PrefillWorkload:
         return self.L * self.T
 
 
+class BackwardWorkload:
+    """The backward pass of the DBF MLP layer: one dbf_backward call (dx and the scale gradients
+    dalpha, dbeta, dgamma) per projection per step."""
+
+    def __init__(self, dbf, key, projs, T):
+        import torch
+        self.dbf, self.key, self.T = dbf, key, T
+        self.items = []
+        for p in projs:
+            f = G.make_factors(p.N, p.M, p.R, p.ell, p.seed, p.sign_mode, p.scale_mode)
+            pf = to_device_factors(dbf, f)
+            ft = dbf.TransposedFactors(pf)
+            x = bf16_dev(G.make_x(T, p.M, p.seed))
+            dy = bf16_dev(G.make_x(T, p.N, p.seed + 7))
+            out = (torch.empty((T, p.M), dtype=torch.bfloat16, device="cuda"),
+                   torch.empty((p.ell, p.N), dtype=torch.float32, device="cuda"),
+                   torch.empty((p.ell, p.R), dtype=torch.float32, device="cuda"),
+                   torch.empty((p.ell, p.M), dtype=torch.float32, device="cuda"))
+            ws = dbf.new_workspace(dbf.backward_workspace_bytes(pf, T), "cuda")
+            self.items.append((pf, ft, x, dy, out, ws, p))
+            del f
+        self.L = len(self.items)
+        self.launches_per_call = 6  # two prologues and four GEMMs (dbf_backward)
+        # x, dy read; dx written; signs read in both orientations; scales read; gradients written
+        self.bytes_per_call = sum(2 * T * (p.M + p.N) + 2 * T * p.M + 2 * (p.R * (p.N + p.M)) // 8
+                                  + 2 * p.ell * (p.N + p.R + p.M) + 4 * p.ell * (p.N + p.R + p.M)
+                                  for *_, p in self.items) / self.L
+        # four GEMMs: the forward recomputed (x -> V -> dalpha) and the transposed product (dy -> V' -> dx)
+        self.flops_per_call = sum(2 * CFG.flops(p.N, p.M, p.R, p.ell, T) for *_, p in self.items) / self.L
+        self.bound = "tensor"
+        self.graph = None
+
+    def run_eager(self):
+        for pf, ft, x, dy, out, ws, _ in self.items:
+            self.dbf.backward(pf, ft, x, dy, workspace=ws, out=out)
+
+    capture = DecodeWorkload.capture
+    step = DecodeWorkload.step
+
+    def footprint_per_step(self):
+        return sum(2 * call_footprint(p.N, p.M, p.R, p.ell, self.T, pf.B1w.shape[1], pf.B2w.shape[1])
+                   for pf, _, _, _, _, _, p in self.items)
+
+    @property
+    def calls(self):
+        return self.L
+
+    @property
+    def tokens_per_step(self):
+        return self.L * self.T
+
+
 class SegmentedWorkload:
     """Routed multi-adapter batches: one dbf_matmul_segmented call per adapter pool, L pools per step."""
 
@@ -576,7 +628,8 @@ def workload_line(wl, ms_step, steps, peaks, extra=None):
 
 
 def make_workload(dbf, key, max_calls=None):
-    """Workload by key: adapter4k_T{1,4,16}, dbf1p5_T{1,8}, tiny_T{1,8}, multiadapter_T256, dbfmlp_T2048."""
+    """Workload by key: adapter4k_T{1,4,16}, dbf1p5_T{1,8}, tiny_T{1,8}, multiadapter_T256, dbfmlp_T2048,
+    adapter4k_dx_T16, dbfmlp_dx_T2048, dbfmlp_bwd_T2048."""
     cap = {} if max_calls is None else {"max_calls": max_calls}
     name, _, tok = key.rpartition("_T")
     T = int(tok)
@@ -584,6 +637,8 @@ def make_workload(dbf, key, max_calls=None):
         return DecodeWorkload(dbf, key, CFG.ADAPTER_4K.projections[0], T, transposed=True, **cap)
     if name == "dbfmlp_dx":
         return PrefillWorkload(dbf, key, CFG.DBF_MLP.projections, T, transposed=True)
+    if name == "dbfmlp_bwd":
+        return BackwardWorkload(dbf, key, CFG.DBF_MLP.projections, T)
     if name == "adapter4k":
         return DecodeWorkload(dbf, key, CFG.ADAPTER_4K.projections[0], T, **cap)
     if name == "dbf1p5":
@@ -606,10 +661,12 @@ WORKLOAD_TITLES = {
     "dbfmlp": "dbfmlp: DBF MLP up 14336x4096 + down 4096x14336, R=5013 ell=2, T={T} prefill tokens",
     "adapter4k_dx": "adapter4k_dx: backward dx = dy dW of the LoRDBA adapter branch N=M=4096 R=64 ell=1, T={T}",
     "dbfmlp_dx": "dbfmlp_dx: backward dx = dy dW of the DBF MLP up + down projections, R=5013 ell=2, T={T}",
+    "dbfmlp_bwd": "dbfmlp_bwd: backward pass (dx, dalpha, dbeta, dgamma) of the DBF MLP up + down projections, "
+                  "R=5013 ell=2, T={T}",
 }
 
 SECONDARY = ["adapter4k_T1", "adapter4k_T4", "dbf1p5_T1", "dbf1p5_T8", "tiny_T8", "multiadapter_T256",
-             "dbfmlp_T2048", "adapter4k_dx_T16", "dbfmlp_dx_T2048"]
+             "dbfmlp_T2048", "adapter4k_dx_T16", "dbfmlp_dx_T2048", "dbfmlp_bwd_T2048"]
 
 
 def main(argv=None):

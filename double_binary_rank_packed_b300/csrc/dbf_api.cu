@@ -240,6 +240,136 @@ int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
     return DBF_OK;
 }
 
+// workspace of the backward call: X' (max(M, N) columns), V (reused as V'), H
+size_t ws_backward(int64_t N, int64_t M, int64_t R, int64_t ell, int64_t T) {
+    const int64_t C = ell * T;
+    return align_up(size_t(C) * xs_ld(std::max(M, N)) * 2) + 2 * align_up(size_t(C) * v_ld(R) * 2);
+}
+
+// Backward of y = sum_i alpha_i . B1 (beta_i . B2 (gamma_i . x)) for the output
+// gradient dy, on the prefill GEMMs (six launches):
+//   prologue   X'  = fp16(gamma_i . x)
+//   gemm<1>    V   = fp16(beta_i . B2 X'),  H = fp16(B2 X')
+//   gemm<2>    dalpha_i[n] = sum_t dy[t][n] (B1 V)[t, i][n]          (no y)
+//   prologue   DY' = fp16(alpha_i . dy)
+//   gemm<1>    V'  = fp16(beta_i . B1^T DY'),  dbeta_i[r] = sum_t (B1^T DY')[t, i][r] H[t, i][r]
+//   gemm<2>    dx  = bf16(sum_i gamma_i . B2^T V'),  dgamma_i[k] = sum_t x[t][k] (B2^T V')[t, i][k]
+int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x, const uint16_t *dy, int64_t T,
+                 uint16_t *dx, float *dalpha, float *dbeta, float *dgamma, void *ws, cudaStream_t stream) {
+    using namespace dbfk;
+    const int ell = f->ell;
+    const int64_t C = ell * T;
+    if (ceil_div(C, prefill_bn(ell)) > 65535) return DBF_ERR_UNSUPPORTED;
+    const int N = f->N, M = f->M, R = f->R;
+    const int ldv = static_cast<int>(v_ld(R));
+    const int ldm = static_cast<int>(xs_ld(M)), ldn = static_cast<int>(xs_ld(N));
+    char *base = static_cast<char *>(ws);
+    __half *xs = reinterpret_cast<__half *>(base);
+    __half *V = reinterpret_cast<__half *>(base + align_up(size_t(C) * xs_ld(std::max(M, N)) * 2));
+    __half *H = reinterpret_cast<__half *>(reinterpret_cast<char *>(V) + align_up(size_t(C) * ldv * 2));
+    const int bn = prefill_bn(ell);
+    const auto *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
+    const auto *dyb = reinterpret_cast<const __nv_bfloat16 *>(dy);
+    const auto *alpha = reinterpret_cast<const __half *>(f->alpha);
+    const auto *beta = reinterpret_cast<const __half *>(f->beta);
+    const auto *gamma = reinterpret_cast<const __half *>(f->gamma);
+
+    cudaError_t e = cudaMemsetAsync(dalpha, 0, sizeof(float) * size_t(ell) * N, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, sizeof(float) * size_t(ell) * R, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dgamma, 0, sizeof(float) * size_t(ell) * M, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "backward: zero the scale gradients");
+
+    PfArgs a = {};
+    a.ell = ell;
+    a.C = static_cast<int>(C);
+    a.V = V;
+    a.ldv = ldv;
+    a.status = status_ptr();
+
+    // ---- forward recompute: X', V and H, then dalpha
+    // no programmatic overlap with the memsets above
+    e = launch_prefill_prologue(xb, static_cast<int>(T), M, M, gamma, ell, xs, ldm, stream, false);
+    if (e != cudaSuccess) return cuda_fail(e, "backward prologue x");
+    CUtensorMap map;
+    if (!encode_act_map(&map, xs, static_cast<int>(C), ldm, ldm, bn)) {
+        snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
+        return DBF_ERR_CUDA;
+    }
+    PfArgs s1 = a;
+    s1.bits = f->B2;
+    s1.ldw = f->ldw2;
+    s1.rows = R;
+    s1.rows_store = ldv;
+    s1.Kw = static_cast<int>(ceil_div(M, 32));
+    s1.nk = static_cast<int>(ceil_div(M, 64));
+    s1.beta = beta;
+    s1.h_out = H;
+    e = launch_prefill_gemm(1, map, s1, bn, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "backward gemm: x -> V, H");
+
+    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bn)) {
+        snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
+        return DBF_ERR_CUDA;
+    }
+    PfArgs s2 = a;
+    s2.bits = f->B1;
+    s2.ldw = f->ldw1;
+    s2.rows = N;
+    s2.rows_store = N;
+    s2.Kw = static_cast<int>(ceil_div(R, 32));
+    s2.nk = static_cast<int>(ceil_div(R, 64));
+    s2.alpha = alpha;
+    s2.ldy = N;
+    s2.skip_store = 1;
+    s2.red_src = dyb;
+    s2.ld_src = N;
+    s2.red = dalpha;
+    e = launch_prefill_gemm(2, map, s2, bn, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "backward gemm: dalpha");
+
+    // ---- through the transposed factors: V' and dbeta, then dx and dgamma
+    e = launch_prefill_prologue(dyb, static_cast<int>(T), N, N, alpha, ell, xs, ldn, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "backward prologue dy");
+    if (!encode_act_map(&map, xs, static_cast<int>(C), ldn, ldn, bn)) {
+        snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
+        return DBF_ERR_CUDA;
+    }
+    PfArgs t1 = a;
+    t1.bits = ft->B2;  // B1^T [R x N]
+    t1.ldw = ft->ldw2;
+    t1.rows = R;
+    t1.rows_store = ldv;
+    t1.Kw = static_cast<int>(ceil_div(N, 32));
+    t1.nk = static_cast<int>(ceil_div(N, 64));
+    t1.beta = beta;
+    t1.h_in = H;
+    t1.red = dbeta;
+    e = launch_prefill_gemm(1, map, t1, bn, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "backward gemm: dbeta");
+
+    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bn)) {
+        snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
+        return DBF_ERR_CUDA;
+    }
+    PfArgs t2 = a;
+    t2.bits = ft->B1;  // B2^T [M x R]
+    t2.ldw = ft->ldw1;
+    t2.rows = M;
+    t2.rows_store = M;
+    t2.Kw = static_cast<int>(ceil_div(R, 32));
+    t2.nk = static_cast<int>(ceil_div(R, 64));
+    t2.alpha = gamma;
+    t2.y = reinterpret_cast<__nv_bfloat16 *>(dx);
+    t2.ldy = M;
+    t2.skip_store = dx ? 0 : 1;
+    t2.red_src = xb;
+    t2.ld_src = M;
+    t2.red = dgamma;
+    e = launch_prefill_gemm(2, map, t2, bn, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "backward gemm: dx, dgamma");
+    return DBF_OK;
+}
+
 }  // namespace
 
 namespace dbfk {
@@ -354,6 +484,39 @@ int dbf_matmul_path(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t
 int dbf_matmul(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *workspace,
                size_t ws_bytes, void *stream) {
     return dbf_matmul_path(f, x, T, y, accumulate, workspace, ws_bytes, stream, DBF_PATH_AUTO);
+}
+
+size_t dbf_backward_workspace_bytes(const dbf_factors *f, int64_t T) {
+    if (check_factors(f) != DBF_OK || T < 0) return 0;
+    return ws_backward(f->N, f->M, f->R, f->ell, T);
+}
+
+int dbf_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x, const uint16_t *dy, int64_t T,
+                 uint16_t *dx, float *dalpha, float *dbeta, float *dgamma, void *workspace, size_t ws_bytes,
+                 void *stream) {
+    int rc = check_factors(f);
+    if (rc) return rc;
+    rc = check_factors(ft);
+    if (rc) return rc;
+    if (ft->N != f->M || ft->M != f->N || ft->R != f->R || ft->ell != f->ell) return DBF_ERR_INVALID_ARG;
+    if (T < 0 || !dalpha || !dbeta || !dgamma) return DBF_ERR_INVALID_ARG;
+    if (T > (int64_t(1) << 26)) return DBF_ERR_UNSUPPORTED;
+    if (T > 0 && (!x || !dy)) return DBF_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || (dy && !aligned16(dy)) || (dx && !aligned16(dx)) || !aligned16(dalpha) ||
+        !aligned16(dbeta) || !aligned16(dgamma))
+        return DBF_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(dalpha, 0, sizeof(float) * size_t(f->ell) * f->N, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, sizeof(float) * size_t(f->ell) * f->R, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dgamma, 0, sizeof(float) * size_t(f->ell) * f->M, s);
+        return e == cudaSuccess ? DBF_OK : cuda_fail(e, "backward: zero the scale gradients");
+    }
+    const size_t need = ws_backward(f->N, f->M, f->R, f->ell, T);
+    if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
+    if (!status_ptr()) return cuda_fail(cudaGetLastError(), "status word");
+    return run_backward(f, ft, x, dy, T, dx, dalpha, dbeta, dgamma, workspace, s);
 }
 
 size_t dbf_hostio_workspace_bytes(const dbf_factors *f, int64_t T) {

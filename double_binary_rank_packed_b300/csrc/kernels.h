@@ -134,6 +134,14 @@ struct PfArgs {
     int ldy;
     int accumulate;
     int *status;
+    // backward-pass options (all zero for the forward product).  acc(t, i)
+    // is the accumulator of activation row t*ell + i before the epilogue scale.
+    __half *h_out;                 // stage 1: also store fp16(acc) in V's layout
+    const __half *h_in;            // stage 1: red[i][row] += sum_t acc(t, i) * H[t*ell+i][row]
+    const __nv_bfloat16 *red_src;  // stage 2: red[i][row] += sum_t red_src[t][row] * acc(t, i)
+    int ld_src;
+    float *red;                    // [ell][rows] fp32, accumulated with atomics
+    int skip_store;                // stage 2: do not write y (reduction only)
 };
 
 cudaError_t launch_prefill_prologue(const __nv_bfloat16 *x, int T, int M, int ldx, const __half *gamma, int ell,

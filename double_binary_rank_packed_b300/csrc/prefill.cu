@@ -46,6 +46,56 @@ struct PfSmem {
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int q) { return static_cast<uint32_t>(32 * q) << 16; }
 
+// Copy the reduction operand of one tile into shared memory, row-major with
+// 128 halves per line (the tile's 128 weight rows): stage 1 the BN columns of
+// H (line c = activation row col0 + c, positions row0 .. row0+127 of V's
+// layout), stage 2 the BN/ELL tokens of red_src (line t = token col0/ELL + t,
+// rows row0 .. row0+127).  Entries outside the matrices are 0.  e = 0..127.
+template <int STAGE, int BN, int ELL>
+__device__ __forceinline__ void stage_reduction_tile(const PfArgs &a, unsigned char *smem, int row0, int col0, int e) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring was last used by TMA and MMA
+    uint4 *dst = reinterpret_cast<uint4 *>(smem);
+    // 16-byte cp.async copies, all in flight at once; a source size of 0 writes zeros
+    // the operand's base (16-byte aligned whenever copies are issued) stands in for empty sources
+    const void *base = (STAGE == 1) ? static_cast<const void *>(a.h_in) : static_cast<const void *>(a.red_src);
+    auto copy16 = [&](int v, const void *src, bool in) {
+        const void *p = in ? src : base;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst + v)), "l"(p),
+                     "r"(in ? 16 : 0)
+                     : "memory");
+    };
+    if constexpr (STAGE == 1) {
+        // lines = BN columns, 16 vectors of 8 halves each; ldv is a multiple of 64
+        for (int v = e; v < BN * 16; v += 128) {
+            const int c = v >> 4, q = v & 15;
+            const int col = col0 + c, p = row0 + 8 * q;
+            const bool in = col < a.C && p + 8 <= a.ldv;
+            copy16(v, a.h_in + (in ? static_cast<size_t>(col) * a.ldv + p : 0), in);
+        }
+    } else {
+        constexpr int NT = BN / ELL;
+        const int T = a.C / ELL, t0 = col0 / ELL;
+        const bool vec = (a.ld_src % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.red_src) & 15) == 0);
+        for (int v = e; v < NT * 16; v += 128) {
+            const int tl = v >> 4, q = v & 15;
+            const int t = t0 + tl, n = row0 + 8 * q;
+            const __nv_bfloat16 *src = a.red_src + static_cast<size_t>(t < T ? t : 0) * a.ld_src + n;
+            if (vec && (t >= T || n + 8 <= a.rows)) {
+                copy16(v, src, t < T);
+            } else {
+                // unaligned rows or the last partial vector of a row: element copies
+                uint16_t h[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    h[j] = (t < T && n + j < a.rows) ? reinterpret_cast<const uint16_t *>(src)[j] : uint16_t(0);
+                dst[v] = make_uint4(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16),
+                                    h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
+            }
+        }
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 template <int BN, int STAGE, int ELL>
 __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                                                                  const PfArgs a) {
@@ -206,6 +256,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
         // epilogue
         pdl_wait();  // outputs may still be read by the previous kernel
         const bool acc_ready = ok && __all_sync(0xffffffffu, mbar_wait_bounded(acc_full, 0, abort_flag));
+        // backward reductions: the tile of the second operand (H for stage 1, dy or x for stage 2)
+        // is staged in the ring, idle once the accumulator is complete, with one batch of
+        // coalesced loads instead of a dependent load per accumulator chunk
+        const __half *stile = reinterpret_cast<const __half *>(smem);
+        const bool staged = (STAGE == 1) ? (a.h_in != nullptr) : (a.red_src != nullptr);
+        if (staged) {
+            if (acc_ready) stage_reduction_tile<STAGE, BN, ELL>(a, smem, row0, col0, threadIdx.x - 64);
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+        }
         if (acc_ready) {
             tc_fence_after();
             if constexpr (STAGE == 1) {
@@ -216,6 +275,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
                     bsc[i] = row_ok ? __half2float(a.beta[static_cast<size_t>(i) * a.rows + row]) : 0.f;
                 const bool store_row = row < a.rows_store;  // whole 32-row groups agree
                 const int pos = (row & ~31) + 2 * (lane & 15);
+                const int own_pos = pos + (lane >> 4);      // where this lane's own row lands
+                float red_part[ELL];
+#pragma unroll
+                for (int i = 0; i < ELL; ++i) red_part[i] = 0.f;
                 constexpr int CW = 8 * ELL;  // columns per chunk (whole tokens)
                 for (int cb = 0; cb < BN; cb += CW) {
                     uint32_t raw[32];
@@ -244,7 +307,29 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
                         const __half2 h = (lane < 16) ? __floats2half2_rn(v0, recv) : __floats2half2_rn(recv, v1);
                         if (store_row && c < a.C)
                             *reinterpret_cast<__half2 *>(a.V + static_cast<size_t>(c) * a.ldv + pos) = h;
+                        if (a.h_out) {
+                            // the unscaled product, same layout
+                            const float u0 = __uint_as_float(raw[j]), u1 = __uint_as_float(raw[j + 1]);
+                            const float usend = (lane < 16) ? u1 : u0;
+                            const float urecv = __shfl_xor_sync(0xffffffffu, usend, 16);
+                            const __half2 hu =
+                                (lane < 16) ? __floats2half2_rn(u0, urecv) : __floats2half2_rn(urecv, u1);
+                            if (store_row && c < a.C)
+                                *reinterpret_cast<__half2 *>(a.h_out + static_cast<size_t>(c) * a.ldv + pos) = hu;
+                        }
                     }
+                    if (a.h_in && row_ok) {
+                        // dbeta: acc(t, i) * H[t*ell+i][row], summed over this tile's tokens
+                        // (columns past C were staged as 0)
+#pragma unroll
+                        for (int j = 0; j < CW; ++j)
+                            red_part[j % ELL] +=
+                                __uint_as_float(raw[j]) * __half2float(stile[(cb + j) * 128 + (own_pos - row0)]);
+                    }
+                }
+                if (a.red && row_ok) {
+#pragma unroll
+                    for (int i = 0; i < ELL; ++i) atomicAdd(a.red + static_cast<size_t>(i) * a.rows + row, red_part[i]);
                 }
             } else {
                 // y[t][row] = bf16(sum_i alpha_i[row] * acc[t*ELL+i] (+ y))
@@ -255,6 +340,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
                 const bool paired = (a.ldy % 2 == 0) && (a.rows_store % 2 == 0);
                 constexpr int CW = 8 * ELL;
                 const int T = a.C / ELL;
+                float red_part[ELL];
+#pragma unroll
+                for (int i = 0; i < ELL; ++i) red_part[i] = 0.f;
                 for (int cb = 0; cb < BN; cb += CW) {
                     uint32_t raw[32];
                     if constexpr (CW == 8) {
@@ -272,6 +360,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
                     }
                     tmem_ld_wait();
                     const int tb = (col0 + cb) / ELL;
+                    if (a.red_src && row_ok) {
+                        // dalpha / dgamma: red_src[t][row] * acc(t, i), summed over this tile's tokens
+                        // (tokens past T were staged as 0)
+                        const __nv_bfloat16 *st = reinterpret_cast<const __nv_bfloat16 *>(smem);
+#pragma unroll
+                        for (int tt = 0; tt < 8; ++tt) {
+                            const float src = __bfloat162float(st[(cb / ELL + tt) * 128 + (row - row0)]);
+#pragma unroll
+                            for (int i = 0; i < ELL; ++i) red_part[i] += src * __uint_as_float(raw[tt * ELL + i]);
+                        }
+                    }
+                    if (a.skip_store) continue;
                     float out[8];
 #pragma unroll
                     for (int tt = 0; tt < 8; ++tt) {
@@ -314,6 +414,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
                             }
                         }
                     }
+                }
+                if (a.red && row_ok) {
+#pragma unroll
+                    for (int i = 0; i < ELL; ++i) atomicAdd(a.red + static_cast<size_t>(i) * a.rows + row, red_part[i]);
                 }
             }
         } else {

@@ -38,6 +38,7 @@ EXPORTED = (
     "dbf_matmul_hostio", "dbf_segmented_workspace_bytes", "dbf_matmul_segmented",
     "dbf_check_status", "dbf_selftest_bounded_wait", "dbf_status_string", "dbf_last_cuda_error",
     "dbf_launch_count", "dbf_segmented_launch_count", "dbf_transpose_packed", "dbf_factors_transposed",
+    "dbf_backward", "dbf_backward_workspace_bytes",
 )
 
 
@@ -89,6 +90,8 @@ def _load():
         "dbf_transpose_packed": (ci, [vp, i64, i64, i64, vp, i64, vp]),
         "dbf_factors_transposed": (ci, [fp, vp, i32, vp, i32, fp]),
         "dbf_segmented_launch_count": (ci, [i32, i32, i32, i32, i64, i32]),
+        "dbf_backward": (ci, [fp, fp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]),
+        "dbf_backward_workspace_bytes": (sz, [fp, i64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -263,6 +266,51 @@ def matmul_path(f: PackedFactors, x: torch.Tensor, y: torch.Tensor | None = None
 def matmul(f: PackedFactors, x: torch.Tensor, y: torch.Tensor | None = None, accumulate: bool = False,
            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     return matmul_path(f, x, y, accumulate, workspace, PATH_AUTO, stream)
+
+
+def backward_workspace_bytes(f: PackedFactors, T: int) -> int:
+    return int(_lib.dbf_backward_workspace_bytes(ctypes.byref(f.struct), T))
+
+
+def backward(f: PackedFactors, ft: "TransposedFactors", x: torch.Tensor, dy: torch.Tensor, dx: bool = True,
+             workspace: torch.Tensor | None = None, stream=None, out=None):
+    """dx, dalpha, dbeta, dgamma of L = sum_t <dy_t, y_t> (dbf_backward).
+
+    x bf16 [T, M], dy bf16 [T, N]; returns (dx bf16 [T, M] or None, dalpha fp32 [ell, N],
+    dbeta fp32 [ell, R], dgamma fp32 [ell, M]).  `out` may hold those four tensors
+    (dx may be None) to write into instead of new ones.
+    """
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != f.M:
+        raise ValueError("x must be bf16 [T, M]")
+    if dy.dtype != torch.bfloat16 or dy.dim() != 2 or dy.shape != (x.shape[0], f.N):
+        raise ValueError("dy must be bf16 [T, N]")
+    x = x.contiguous()
+    dy = dy.contiguous()
+    T = x.shape[0]
+    ell = f.alpha.shape[0]
+    dev = x.device
+    if out is not None:
+        dxt, da, db, dg = out
+        shapes = ((ell, f.N), (ell, f.R), (ell, f.M))
+        if any(t.dtype != torch.float32 or tuple(t.shape) != sh or not t.is_contiguous()
+               for t, sh in zip((da, db, dg), shapes)):
+            raise ValueError("out: dalpha, dbeta, dgamma must be contiguous fp32 [ell, N], [ell, R], [ell, M]")
+        if dxt is not None and (dxt.dtype != torch.bfloat16 or tuple(dxt.shape) != (T, f.M)
+                                or not dxt.is_contiguous()):
+            raise ValueError("out: dx must be contiguous bf16 [T, M]")
+    else:
+        dxt = torch.empty((T, f.M), dtype=torch.bfloat16, device=dev) if dx else None
+        da = torch.empty((ell, f.N), dtype=torch.float32, device=dev)
+        db = torch.empty((ell, f.R), dtype=torch.float32, device=dev)
+        dg = torch.empty((ell, f.M), dtype=torch.float32, device=dev)
+    need = backward_workspace_bytes(f, T)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    rc = _lib.dbf_backward(ctypes.byref(f.struct), ctypes.byref(ft.struct), _ptr(x), _ptr(dy), T,
+                           _ptr(dxt) if dxt is not None else None, _ptr(da), _ptr(db), _ptr(dg),
+                           _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(rc, "dbf_backward")
+    return dxt, da, db, dg
 
 
 def hostio_workspace_bytes(f: PackedFactors, T: int) -> int:

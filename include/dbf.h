@@ -129,6 +129,40 @@ int dbf_transpose_packed(const uint32_t *words, int64_t rows, int64_t cols, int6
 int dbf_factors_transposed(const dbf_factors *f, const uint32_t *B2T, int32_t ldw_b2t,
                            const uint32_t *B1T, int32_t ldw_b1t, dbf_factors *out);
 
+/*
+ * dbf_backward: everything training needs from one backward pass through the
+ * product (LoRDBA page, section 2, Pipeline de Entrenamiento: the sign
+ * carriers and the scales are trained jointly), for the output gradient dy of
+ * L = sum_t <dy_t, y_t>:
+ *     dx[t]       = sum_i gamma_i . B2^T (beta_i . B1^T (alpha_i . dy_t))
+ *     dalpha_i[n] = sum_t dy_t[n] * (B1 (beta_i . B2 (gamma_i . x_t)))[n]
+ *     dbeta_i[r]  = sum_t (B1^T (alpha_i . dy_t))[r] * (B2 (gamma_i . x_t))[r]
+ *     dgamma_i[k] = sum_t x_t[k] * (B2^T (beta_i . B1^T (alpha_i . dy_t)))[k]
+ *   f, ft     host pointers: the factors and their transposed descriptor
+ *             (dbf_factors_transposed; only its sign matrices are read, the
+ *             scales come from f); shapes must match (ft->N == f->M, ...)
+ *   x         device bf16 [T][M], the forward input
+ *   dy        device bf16 [T][N]
+ *   dx        device bf16 [T][M], or NULL to skip writing dx
+ *   dalpha    device fp32 [ell][N], dbeta fp32 [ell][R], dgamma fp32 [ell][M]:
+ *             overwritten (zeroed first, then accumulated with atomics, so
+ *             the last bits vary from run to run)
+ *   workspace device, >= dbf_backward_workspace_bytes(f, T), 256-byte aligned
+ * Runs on the prefill (tensor-core) kernels for every T: the forward is
+ * recomputed (x -> V, H; then V -> dalpha without writing y), then the
+ * transposed product gives dbeta, dx and dgamma: six launches, 2x the FLOPs
+ * of one forward call.  Intermediates are fp16 as in the forward product.
+ * All device pointers 16-byte aligned.  Asynchronous on `stream`; errors as
+ * dbf_matmul.  The workspace must not be shared with concurrent calls.
+ */
+int dbf_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
+                 const uint16_t *dy, int64_t T, uint16_t *dx, float *dalpha,
+                 float *dbeta, float *dgamma, void *workspace, size_t ws_bytes,
+                 void *stream);
+
+/* Device workspace (bytes) dbf_backward needs for this shape and token count. */
+size_t dbf_backward_workspace_bytes(const dbf_factors *f, int64_t T);
+
 /* Device workspace (bytes) dbf_matmul needs for this shape and token count. */
 size_t dbf_workspace_bytes(const dbf_factors *f, int64_t T);
 

@@ -274,6 +274,34 @@ def scale_grads_f64(x64: np.ndarray, dy64: np.ndarray, f):
     return dalpha, dbeta, dgamma
 
 
+def scale_grads_sampled(x64: np.ndarray, dy64: np.ndarray, f, n_idx, r_idx, k_idx):
+    """scale_grads_f64 restricted to the listed output channels n, middle
+    channels r and input channels k (same definitions; only the columns of
+    the intermediates those entries need are formed, except g, which dgamma
+    needs whole).  Returns (dalpha [ell, len(n_idx)], dbeta [ell, len(r_idx)],
+    dgamma [ell, len(k_idx)]).
+    """
+    alpha, beta, gamma = _scales(f)
+    x = np.asarray(x64, dtype=np.float64)
+    dy = np.asarray(dy64, dtype=np.float64)
+    n_idx, r_idx, k_idx = (np.asarray(v) for v in (n_idx, r_idx, k_idx))
+    B1 = np.asarray(f.B1, dtype=np.float64)
+    B2 = np.asarray(f.B2, dtype=np.float64)
+    ell = alpha.shape[0]
+    da = np.zeros((ell, n_idx.size))
+    db = np.zeros((ell, r_idx.size))
+    dg = np.zeros((ell, k_idx.size))
+    for i in range(ell):
+        h = (x * gamma[i][None, :]) @ B2.T                       # [T, R]
+        u_n = (h * beta[i][None, :]) @ B1[n_idx].T               # [T, n']
+        g = (dy * alpha[i][None, :]) @ B1                        # [T, R]
+        w_k = (g * beta[i][None, :]) @ B2[:, k_idx]              # [T, k']
+        da[i] = (dy[:, n_idx] * u_n).sum(axis=0)
+        db[i] = (g[:, r_idx] * h[:, r_idx]).sum(axis=0)
+        dg[i] = (x[:, k_idx] * w_k).sum(axis=0)
+    return da, db, dg
+
+
 def scale_grads(x_bits: np.ndarray, dy_bits: np.ndarray, f):
     """Reference for the backward call's scale gradients from bf16 x and dy."""
     return scale_grads_f64(bf16_bits_to_f64(x_bits), bf16_bits_to_f64(dy_bits), f)

@@ -433,3 +433,15 @@ def test_scale_grad_pins_catch_a_transposed_carrier(monkeypatch):
     pred_good = float((good[2] * (new.astype(np.float64) - f.gamma.astype(np.float64))).sum())
     assert abs((L1 - L0) - pred_good) <= 1e-10 * max(1.0, abs(L0))
     assert abs((L1 - L0) - pred_bad) > 1e-6 * max(1.0, abs(L0))
+
+
+def test_scale_grads_sampled_equals_full():
+    f = G.make_factors(40, 28, 11, 2, 71)
+    rng = np.random.default_rng(72)
+    x = rng.standard_normal((7, 28))
+    dy = rng.standard_normal((7, 40))
+    full = O.scale_grads_f64(x, dy, f)
+    n, r, k = [0, 5, 39], [10, 3], [27, 0, 13, 14]
+    part = O.scale_grads_sampled(x, dy, f, n, r, k)
+    for want, got, idx in zip(full, part, (n, r, k)):
+        np.testing.assert_allclose(got, want[:, idx], rtol=1e-12, atol=1e-12)
