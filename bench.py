@@ -403,6 +403,66 @@ class BackwardWorkload:
         return self.L * self.T
 
 
+QKV_SHAPES = ((4096, 4096, 3072), (1024, 4096, 1536), (1024, 4096, 2048))
+
+
+class GroupedWorkload:
+    """q, k and v of a 4096-wide block with grouped-query heads, each at its own middle dimension
+    (non-uniform R), applied to the same tokens: one dbf_matmul_grouped call per group (or, with
+    separate=True, three dbf_matmul calls), L groups with distinct factors per step."""
+
+    def __init__(self, dbf, key, T, separate=False, max_calls=4096):
+        import torch
+        self.dbf, self.key, self.T, self.separate = dbf, key, T, separate
+        base = []
+        for k, (N, M, R) in enumerate(QKV_SHAPES):
+            f = G.make_factors(N, M, R, 1, 6000 + k)
+            base.append(to_device_factors(dbf, f))
+            del f
+        fp = sum(call_footprint(N, M, R, 1, T, pf.B1w.shape[1], pf.B2w.shape[1])
+                 for (N, M, R), pf in zip(QKV_SHAPES, base))
+        self.L = int(min(max_calls, max(8, math.ceil(4 * L2_BYTES / fp))))
+        self.fp_call = fp
+        x0 = bf16_dev(G.make_x(T, 4096, 6010))
+        self.groups = [base] + [[clone_factors(dbf, pf) for pf in base] for _ in range(self.L - 1)]
+        self.x = [x0] + [x0.clone() for _ in range(self.L - 1)]
+        self.y = [[torch.empty((T, N), dtype=torch.bfloat16, device="cuda") for (N, _, _) in QKV_SHAPES]
+                  for _ in range(self.L)]
+        if separate:
+            self.ws = dbf.new_workspace(max(dbf.workspace_bytes(pf, T) for pf in base), "cuda")
+            self.launches_per_call = sum(dbf.launch_count(pf, T) for pf in base)
+        else:
+            self.ws = dbf.new_workspace(dbf.grouped_workspace_bytes(base, T), "cuda")
+            self.launches_per_call = dbf.grouped_launch_count(base, T)
+        self.bytes_per_call = sum(CFG.algorithmic_bytes(N, M, R, 1, T) for (N, M, R) in QKV_SHAPES)
+        self.flops_per_call = sum(CFG.flops(N, M, R, 1, T) for (N, M, R) in QKV_SHAPES)
+        self.bound = "hbm"
+        self.graph = None
+
+    def run_eager(self):
+        for l in range(self.L):
+            x = self.x[l]
+            if self.separate:
+                for pf, y in zip(self.groups[l], self.y[l]):
+                    self.dbf.matmul(pf, x, y, workspace=self.ws)
+            else:
+                self.dbf.matmul_grouped(self.groups[l], [x, x, x], self.y[l], workspace=self.ws)
+
+    capture = DecodeWorkload.capture
+    step = DecodeWorkload.step
+
+    def footprint_per_step(self):
+        return self.L * self.fp_call
+
+    @property
+    def calls(self):
+        return self.L
+
+    @property
+    def tokens_per_step(self):
+        return self.L * self.T
+
+
 class SegmentedWorkload:
     """Routed multi-adapter batches: one dbf_matmul_segmented call per adapter pool, L pools per step."""
 
@@ -629,7 +689,7 @@ def workload_line(wl, ms_step, steps, peaks, extra=None):
 
 def make_workload(dbf, key, max_calls=None):
     """Workload by key: adapter4k_T{1,4,16}, dbf1p5_T{1,8}, tiny_T{1,8}, multiadapter_T256, dbfmlp_T2048,
-    adapter4k_dx_T16, dbfmlp_dx_T2048, dbfmlp_bwd_T2048."""
+    adapter4k_dx_T16, dbfmlp_dx_T2048, dbfmlp_bwd_T2048, dbfqkv_T8 (grouped), dbfqkv_sep_T8."""
     cap = {} if max_calls is None else {"max_calls": max_calls}
     name, _, tok = key.rpartition("_T")
     T = int(tok)
@@ -639,6 +699,10 @@ def make_workload(dbf, key, max_calls=None):
         return PrefillWorkload(dbf, key, CFG.DBF_MLP.projections, T, transposed=True)
     if name == "dbfmlp_bwd":
         return BackwardWorkload(dbf, key, CFG.DBF_MLP.projections, T)
+    if name == "dbfqkv":
+        return GroupedWorkload(dbf, key, T, **cap)
+    if name == "dbfqkv_sep":
+        return GroupedWorkload(dbf, key, T, separate=True, **cap)
     if name == "adapter4k":
         return DecodeWorkload(dbf, key, CFG.ADAPTER_4K.projections[0], T, **cap)
     if name == "dbf1p5":
@@ -663,10 +727,14 @@ WORKLOAD_TITLES = {
     "dbfmlp_dx": "dbfmlp_dx: backward dx = dy dW of the DBF MLP up + down projections, R=5013 ell=2, T={T}",
     "dbfmlp_bwd": "dbfmlp_bwd: backward pass (dx, dalpha, dbeta, dgamma) of the DBF MLP up + down projections, "
                   "R=5013 ell=2, T={T}",
+    "dbfqkv": "dbfqkv: q 4096x4096 R=3072, k and v 1024x4096 R=1536 / 2048 (non-uniform R), ell=1, one grouped "
+              "call per token batch, T={T} decode tokens",
+    "dbfqkv_sep": "dbfqkv_sep: the same q, k, v projections as three separate calls, T={T} decode tokens",
 }
 
 SECONDARY = ["adapter4k_T1", "adapter4k_T4", "dbf1p5_T1", "dbf1p5_T8", "tiny_T8", "multiadapter_T256",
-             "dbfmlp_T2048", "adapter4k_dx_T16", "dbfmlp_dx_T2048", "dbfmlp_bwd_T2048"]
+             "dbfmlp_T2048", "adapter4k_dx_T16", "dbfmlp_dx_T2048", "dbfmlp_bwd_T2048", "dbfqkv_T8",
+             "dbfqkv_sep_T8"]
 
 
 def main(argv=None):

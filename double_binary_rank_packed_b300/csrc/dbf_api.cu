@@ -486,6 +486,93 @@ int dbf_matmul(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, 
     return dbf_matmul_path(f, x, T, y, accumulate, workspace, ws_bytes, stream, DBF_PATH_AUTO);
 }
 
+}  // extern "C"
+
+namespace {
+
+// grouped call: validation shared by the workspace query and the call
+int check_group(const dbf_factors *fs, int32_t G) {
+    if (!fs || G < 1) return DBF_ERR_INVALID_ARG;
+    if (G > dbfk::kMaxGroup) return DBF_ERR_UNSUPPORTED;
+    for (int p = 0; p < G; ++p) {
+        const int rc = check_factors(&fs[p]);
+        if (rc) return rc;
+        if (fs[p].ell != fs[0].ell) return DBF_ERR_INVALID_ARG;
+    }
+    return DBF_OK;
+}
+
+size_t ws_grouped(const dbf_factors *fs, int G, int64_t T) {
+    size_t need = 0;
+    for (int p = 0; p < G; ++p) {
+        const dbf_factors &f = fs[p];
+        if (T <= kDecodeMaxTokens)
+            need += ws_decode(f.N, f.M, f.R, f.ell, T);  // each problem its own V
+        else
+            need = std::max(need, ws_prefill(f.N, f.M, f.R, f.ell, T));  // problems run one after another
+    }
+    return need;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dbf_grouped_workspace_bytes(const dbf_factors *fs, int32_t G, int64_t T) {
+    if (check_group(fs, G) != DBF_OK || T < 0) return 0;
+    return ws_grouped(fs, G, T);
+}
+
+int dbf_grouped_launch_count(const dbf_factors *fs, int32_t G, int64_t T) {
+    if (check_group(fs, G) != DBF_OK || T < 0) return -1;
+    if (T == 0) return 0;
+    return T <= kDecodeMaxTokens ? 2 : 3 * G;
+}
+
+int dbf_matmul_grouped(const dbf_factors *fs, int32_t G, const uint16_t *const *xs, uint16_t *const *ys, int64_t T,
+                       int accumulate, void *workspace, size_t ws_bytes, void *stream) {
+    int rc = check_group(fs, G);
+    if (rc) return rc;
+    if (T < 0 || (accumulate != 0 && accumulate != 1)) return DBF_ERR_INVALID_ARG;
+    if (T == 0) return DBF_OK;
+    if (T > (int64_t(1) << 26)) return DBF_ERR_UNSUPPORTED;
+    if (!xs || !ys) return DBF_ERR_INVALID_ARG;
+    for (int p = 0; p < G; ++p) {
+        if (!xs[p] || !ys[p]) return DBF_ERR_INVALID_ARG;
+        if (!aligned16(xs[p]) || !aligned16(ys[p])) return DBF_ERR_ALIGNMENT;
+    }
+    const size_t need = ws_grouped(fs, G, T);
+    if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
+    if (!status_ptr()) return cuda_fail(cudaGetLastError(), "status word");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > kDecodeMaxTokens) {
+        // large batches: each problem is a full set of GEMMs, launch cost is negligible
+        for (int p = 0; p < G; ++p) {
+            rc = run_prefill(&fs[p], xs[p], T, ys[p], accumulate, workspace, s);
+            if (rc) return rc;
+        }
+        return DBF_OK;
+    }
+    dbfk::DecodeGroupCall c = {};
+    c.G = G;
+    c.T = static_cast<int>(T);
+    c.ell = fs[0].ell;
+    c.accumulate = accumulate;
+    c.status = status_ptr();
+    char *base = static_cast<char *>(workspace);
+    for (int p = 0; p < G; ++p) {
+        c.f[p] = &fs[p];
+        c.x[p] = reinterpret_cast<const __nv_bfloat16 *>(xs[p]);
+        c.y[p] = reinterpret_cast<__nv_bfloat16 *>(ys[p]);
+        c.V[p] = reinterpret_cast<__half *>(base);
+        c.ldv[p] = static_cast<int>(v_ld(fs[p].R));
+        base += ws_decode(fs[p].N, fs[p].M, fs[p].R, fs[p].ell, T);
+    }
+    const cudaError_t e = dbfk::launch_decode_grouped(c, num_sms(), s);
+    return e == cudaSuccess ? DBF_OK : map_launch_error(e, "grouped decode");
+}
+
 size_t dbf_backward_workspace_bytes(const dbf_factors *f, int64_t T) {
     if (check_factors(f) != DBF_OK || T < 0) return 0;
     return ws_backward(f->N, f->M, f->R, f->ell, T);

@@ -646,8 +646,10 @@ __host__ __device__ inline StageSmem stage_smem(int CPAD, int RBW, int KS, int W
     return L;
 }
 
+// bx: this CTA's index along the rows of its problem (blockIdx.x, or the
+// offset inside its problem's range in a grouped launch)
 template <int CT, int RBW, int STAGE, bool SEG>
-__global__ void __launch_bounds__(kThreads, 2) dec_stage_kernel(const DecArgs a) {
+__device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
     constexpr int CPAD = 8 * CT;
     constexpr int C4 = CPAD / 4;
     constexpr int RWS = 16 * RBW;
@@ -657,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_stage_kernel(const DecArgs a)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, c = lane & 3;
     const int KS = a.KS, Wc = a.Wc;
     const int rank = (KS > 1) ? static_cast<int>(cluster_ctarank()) : 0;
-    const int row0 = (blockIdx.x / KS) * RWS;
+    const int row0 = (bx / KS) * RWS;
     const int ell = a.ell;
 
     const uint32_t *bits = a.bits;
@@ -670,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_stage_kernel(const DecArgs a)
         const int s = blockIdx.y;
         const int o0 = a.seg_off[s], o1 = a.seg_off[s + 1], ad = a.seg_ad[s];
         if (o0 < 0 || o1 < o0 || o1 > a.T || ad < 0 || ad >= a.n_adapters) {
-            if (tid == 0 && blockIdx.x == 0) record_status(a.status, DBF_ERR_DEVICE_ARG);
+            if (tid == 0 && bx == 0) record_status(a.status, DBF_ERR_DEVICE_ARG);
             return;  // uniform over the cluster: every CTA of it reads the same entry
         }
         t0 = o0;
@@ -912,6 +914,22 @@ __global__ void __launch_bounds__(kThreads, 2) dec_stage_kernel(const DecArgs a)
     if (KS > 1) cluster_wait_acquire();  // peers may read this CTA's partial until they arrive
 }
 
+template <int CT, int RBW, int STAGE, bool SEG>
+__global__ void __launch_bounds__(kThreads, 2) dec_stage_kernel(const DecArgs a) {
+    dec_stage_body<CT, RBW, STAGE, SEG>(a, static_cast<int>(blockIdx.x));
+}
+
+// Grouped launch: G independent problems of any shape (same ell and T) in one
+// launch.  Problem p owns CTAs [block0[p], block0[p+1]) along x, a multiple of
+// the cluster size, and runs exactly as its own launch would.
+template <int CT, int RBW, int STAGE>
+__global__ void __launch_bounds__(kThreads, 2) dec_stage_group_kernel(const __grid_constant__ DecGroupArgs g) {
+    const int b = static_cast<int>(blockIdx.x);
+    int p = 0;
+    while (p + 1 < g.G && b >= g.block0[p + 1]) ++p;
+    dec_stage_body<CT, RBW, STAGE, false>(g.p[p], b - g.block0[p]);
+}
+
 // ================================================================ launchers
 
 template <typename Kern, typename Args>
@@ -971,6 +989,26 @@ cudaError_t launch_stage_ct(const DecPlan &plan, const DecArgs &args, int grid_y
                                      : cudaErrorInvalidValue;
         case 8: return plan.RBW == 2 ? launch_stage_one<8, 2, STAGE, SEG>(plan, args, grid_y, stream, pdl)
                                      : cudaErrorInvalidValue;
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int CT, int RBW, int STAGE>
+cudaError_t launch_group_one(const DecPlan &plan, const DecGroupArgs &g, cudaStream_t stream, bool pdl) {
+    static int configured = 0;
+    return launch_ex(dec_stage_group_kernel<CT, RBW, STAGE>, configured, plan.grid_x, 1, plan.smem, plan.KS, g,
+                     stream, pdl);
+}
+
+template <int STAGE>
+cudaError_t launch_group_stage(const DecPlan &plan, const DecGroupArgs &g, cudaStream_t stream, bool pdl) {
+    switch (plan.CT) {
+        case 1: return plan.RBW == 2 ? launch_group_one<1, 2, STAGE>(plan, g, stream, pdl)
+                                     : launch_group_one<1, 4, STAGE>(plan, g, stream, pdl);
+        case 2: return plan.RBW == 2 ? launch_group_one<2, 2, STAGE>(plan, g, stream, pdl)
+                                     : launch_group_one<2, 4, STAGE>(plan, g, stream, pdl);
+        case 4: return plan.RBW == 2 ? launch_group_one<4, 2, STAGE>(plan, g, stream, pdl) : cudaErrorInvalidValue;
+        case 8: return plan.RBW == 2 ? launch_group_one<8, 2, STAGE>(plan, g, stream, pdl) : cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1192,6 +1230,128 @@ cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int
     cudaError_t e = launch_decode_stage(1, seg, p1, a1, problems, stream, true);
     if (e != cudaSuccess) return e;
     return launch_decode_stage(2, seg, p2, a2, problems, stream, true);
+}
+
+// Plan of a grouped stage: one CT, RBW and KS for every problem of the launch
+// (the cluster size is a launch property), each problem with its own K slice
+// width; the same latency model as a single problem, with the work of all
+// problems spread over the SMs and the slowest CTA as a floor.
+DecPlan plan_group_stage(const int *rows_cover, const int *Kw, int G, int columns, int max_ct, int num_sms, int ell,
+                         bool stage1, bool accumulate) {
+    DecPlan best = {};
+    const int ct = ct_for(columns, max_ct);
+    const int cpad = 8 * ct;
+    int min_kw = Kw[0];
+    for (int p = 1; p < G; ++p) min_kw = std::min(min_kw, Kw[p]);
+    double best_cost = 1e300;
+    for (int RBW = 2; RBW <= 4; RBW *= 2) {
+        if (ct >= 4 && RBW > 2) break;
+        for (int KS = 1; KS <= 8; KS *= 2) {
+            if (KS > 1 && (KS > min_kw || 16 * RBW / KS < 8)) break;
+            size_t smem = 0;
+            int64_t ctas = 0;
+            double work = 0.0, max_work = 0.0;
+            const int nwb = ct >= 4 ? 1 : (ct >= 2 ? 2 : 4);
+            const double epi = double(16 * RBW / KS) * cpad * 8.0 / kThreads * 20.0;
+            for (int p = 0; p < G; ++p) {
+                const int Wc = (Kw[p] + KS - 1) / KS;
+                smem = std::max(smem, stage_smem(cpad, RBW, KS, Wc, ell, stage1, accumulate).total);
+                const int groups = (rows_cover[p] + 16 * RBW - 1) / (16 * RBW);
+                const int Wp = (Wc + kWarps - 1) / kWarps;
+                const double w = Wp * (60.0 * ct + 30.0 * RBW + 12.0 * RBW * ct) +
+                                 (std::ceil(double(Wp) / nwb) - 1.0) * 700.0 + epi;
+                ctas += int64_t(groups) * KS;
+                work += double(groups) * KS * w;
+                max_work = std::max(max_work, w);
+            }
+            if (smem > kSmemCap || ctas > (int64_t(1) << 30)) continue;
+            const int occ = occupancy_for(smem);
+            const double waves = std::ceil(double(ctas) / (double(num_sms) * occ));
+            const double cost = waves * 1500.0 + std::max(work / num_sms, max_work) + (KS > 1 ? 900.0 : 0.0);
+            if (cost < best_cost) {
+                best_cost = cost;
+                best.CT = ct;
+                best.RBW = RBW;
+                best.KS = KS;
+                best.Wc = 0;  // per problem
+                best.grid_x = static_cast<int>(ctas);
+                best.smem = smem;
+            }
+        }
+    }
+    return best;
+}
+
+// Both decode stages of a group of independent problems, one launch per stage.
+cudaError_t launch_decode_grouped(const DecodeGroupCall &c, int num_sms, cudaStream_t stream) {
+    const int G = c.G, ell = c.ell;
+    if (G < 1 || G > kMaxGroup) return cudaErrorInvalidValue;
+    const int cols = static_cast<int>(std::min<int64_t>(int64_t(ell) * c.T, 64));
+    int rows1[kMaxGroup], kw1[kMaxGroup], rows2[kMaxGroup], kw2[kMaxGroup];
+    for (int p = 0; p < G; ++p) {
+        const dbf_factors *f = c.f[p];
+        rows1[p] = (f->R + 31) & ~31;
+        kw1[p] = (f->M + 31) / 32;
+        rows2[p] = f->N;
+        kw2[p] = (f->R + 31) / 32;
+    }
+    const DecPlan p1 = plan_group_stage(rows1, kw1, G, cols, 8, num_sms, ell, true, true);
+    if (p1.smem == 0) return cudaErrorNotSupported;
+    DecPlan p2 = plan_group_stage(rows2, kw2, G, cols, p1.CT, num_sms, ell, false, c.accumulate != 0);
+    if (p2.smem == 0 || p2.CT != p1.CT) return cudaErrorNotSupported;
+
+    DecGroupArgs g1 = {}, g2 = {};
+    g1.G = g2.G = G;
+    int b1 = 0, b2 = 0;
+    for (int p = 0; p < G; ++p) {
+        const dbf_factors *f = c.f[p];
+        DecArgs a = {};
+        a.ell = ell;
+        a.T = c.T;
+        a.x = c.x[p];
+        a.ldx = f->M;
+        a.V = c.V[p];
+        a.ldv = c.ldv[p];
+        a.y = c.y[p];
+        a.ldy = f->N;
+        a.accumulate = c.accumulate;
+        a.status = c.status;
+
+        DecArgs a1 = a;
+        a1.bits = f->B2;
+        a1.ldw = f->ldw2;
+        a1.gamma = reinterpret_cast<const __half *>(f->gamma);
+        a1.beta = reinterpret_cast<const __half *>(f->beta);
+        a1.rows = f->R;
+        a1.rows_out = rows1[p];
+        a1.K = f->M;
+        a1.Kw = kw1[p];
+        a1.KS = p1.KS;
+        a1.Wc = (kw1[p] + p1.KS - 1) / p1.KS;
+        g1.p[p] = a1;
+        g1.block0[p] = b1;
+        b1 += ((rows1[p] + 16 * p1.RBW - 1) / (16 * p1.RBW)) * p1.KS;
+
+        DecArgs a2 = a;
+        a2.bits = f->B1;
+        a2.ldw = f->ldw1;
+        a2.alpha = reinterpret_cast<const __half *>(f->alpha);
+        a2.rows = f->N;
+        a2.rows_out = f->N;
+        a2.K = f->R;
+        a2.Kw = kw2[p];
+        a2.KS = p2.KS;
+        a2.Wc = (kw2[p] + p2.KS - 1) / p2.KS;
+        g2.p[p] = a2;
+        g2.block0[p] = b2;
+        b2 += ((rows2[p] + 16 * p2.RBW - 1) / (16 * p2.RBW)) * p2.KS;
+    }
+    g1.block0[G] = b1;
+    g2.block0[G] = b2;
+    if (b1 != p1.grid_x || b2 != p2.grid_x) return cudaErrorInvalidValue;
+    cudaError_t e = launch_group_stage<1>(p1, g1, stream, true);
+    if (e != cudaSuccess) return e;
+    return launch_group_stage<2>(p2, g2, stream, true);
 }
 
 }  // namespace dbfk

@@ -49,6 +49,15 @@ struct DecArgs {
     int *status;
 };
 
+// Grouped decode launch (several problems of different shapes, one launch
+// per stage): the per-problem arguments travel as the kernel parameter.
+constexpr int kMaxGroup = 16;
+struct DecGroupArgs {
+    int G;
+    int block0[kMaxGroup + 1];  // first CTA of each problem along x; block0[G] = grid size
+    DecArgs p[kMaxGroup];
+};
+
 struct DecPlan {
     int CT;          // n8 column tiles (columns per chunk = 8*CT); 0 = no plan
     int RBW;         // 16-row blocks per CTA (2 or 4)
@@ -114,6 +123,20 @@ struct DecodeCall {
 // Both stages; V is device scratch of ell*T rows x ldv halves.  Returns
 // cudaErrorNotSupported when no tile plan fits the shape.
 cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int num_sms, cudaStream_t stream);
+
+// G independent problems (same ell and T, any N, M, R), both stages in one
+// launch each; V[p] is scratch of ell*T rows x ldv[p] halves.  Returns
+// cudaErrorNotSupported when no common tile plan fits.
+struct DecodeGroupCall {
+    int G, T, ell, accumulate;
+    const dbf_factors *f[kMaxGroup];
+    const __nv_bfloat16 *x[kMaxGroup];
+    __nv_bfloat16 *y[kMaxGroup];
+    __half *V[kMaxGroup];
+    int ldv[kMaxGroup];
+    int *status;
+};
+cudaError_t launch_decode_grouped(const DecodeGroupCall &c, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------- prefill path
 

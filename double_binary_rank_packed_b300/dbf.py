@@ -38,7 +38,8 @@ EXPORTED = (
     "dbf_matmul_hostio", "dbf_segmented_workspace_bytes", "dbf_matmul_segmented",
     "dbf_check_status", "dbf_selftest_bounded_wait", "dbf_status_string", "dbf_last_cuda_error",
     "dbf_launch_count", "dbf_segmented_launch_count", "dbf_transpose_packed", "dbf_factors_transposed",
-    "dbf_backward", "dbf_backward_workspace_bytes",
+    "dbf_backward", "dbf_backward_workspace_bytes", "dbf_matmul_grouped", "dbf_grouped_workspace_bytes",
+    "dbf_grouped_launch_count",
 )
 
 
@@ -92,6 +93,9 @@ def _load():
         "dbf_segmented_launch_count": (ci, [i32, i32, i32, i32, i64, i32]),
         "dbf_backward": (ci, [fp, fp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]),
         "dbf_backward_workspace_bytes": (sz, [fp, i64]),
+        "dbf_matmul_grouped": (ci, [fp, i32, vp, vp, i64, ci, vp, sz, vp]),
+        "dbf_grouped_workspace_bytes": (sz, [fp, i32, i64]),
+        "dbf_grouped_launch_count": (ci, [fp, i32, i64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -311,6 +315,50 @@ def backward(f: PackedFactors, ft: "TransposedFactors", x: torch.Tensor, dy: tor
                            _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(rc, "dbf_backward")
     return dxt, da, db, dg
+
+
+def _group_structs(fs):
+    arr = (DbfFactors * len(fs))()
+    for k, f in enumerate(fs):
+        arr[k] = f.struct
+    return arr
+
+
+def grouped_workspace_bytes(fs, T: int) -> int:
+    return int(_lib.dbf_grouped_workspace_bytes(_group_structs(fs), len(fs), T))
+
+
+def grouped_launch_count(fs, T: int) -> int:
+    return int(_lib.dbf_grouped_launch_count(_group_structs(fs), len(fs), T))
+
+
+def matmul_grouped(fs, xs, ys=None, accumulate: bool = False, workspace: torch.Tensor | None = None, stream=None):
+    """ys[p] = product of fs[p] applied to xs[p] for G independent projections (dbf_matmul_grouped).
+
+    fs: list of PackedFactors (one ell); xs: list of bf16 [T, M_p]; ys: list of bf16 [T, N_p] or None.
+    """
+    G = len(fs)
+    if G == 0 or len(xs) != G or (ys is not None and len(ys) != G):
+        raise ValueError("fs, xs (and ys) must have the same non-zero length")
+    xs = [x.contiguous() for x in xs]
+    T = xs[0].shape[0]
+    for f, x in zip(fs, xs):
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape != (T, f.M):
+            raise ValueError("every x must be bf16 [T, M_p] with one T")
+    if ys is None:
+        if accumulate:
+            raise ValueError("accumulate needs ys")
+        ys = [torch.empty((T, f.N), dtype=torch.bfloat16, device=xs[0].device) for f in fs]
+    structs = _group_structs(fs)
+    need = int(_lib.dbf_grouped_workspace_bytes(structs, G, T))
+    if workspace is None:
+        workspace = new_workspace(need, xs[0].device)
+    xp = (ctypes.c_void_p * G)(*[x.data_ptr() for x in xs])
+    yp = (ctypes.c_void_p * G)(*[y.data_ptr() for y in ys])
+    rc = _lib.dbf_matmul_grouped(structs, G, xp, yp, T, int(bool(accumulate)), _ptr(workspace),
+                                 workspace.numel(), _stream_handle(stream))
+    _check(rc, "dbf_matmul_grouped")
+    return ys
 
 
 def hostio_workspace_bytes(f: PackedFactors, T: int) -> int:

@@ -163,6 +163,35 @@ int dbf_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
 /* Device workspace (bytes) dbf_backward needs for this shape and token count. */
 size_t dbf_backward_workspace_bytes(const dbf_factors *f, int64_t T);
 
+/*
+ * dbf_matmul_grouped: G independent products in one call,
+ *     ys[p] = sum_i alpha_i . B1 (beta_i . (B2 (gamma_i . xs[p])))  with fs[p],
+ * for projections whose middle dimension R differs from one to the next (the
+ * DBF page, section 2 "Control Granular de Compresión" and section 3: the
+ * compression ratio is set per layer through the middle dimension, giving
+ * non-uniform bits per layer), or any N and M.
+ *   fs      host array of G descriptors (device pointers inside), one ell for all
+ *   G       1 .. 16
+ *   xs, ys  host arrays of G device pointers: bf16 [T][fs[p].M] and [T][fs[p].N],
+ *           16-byte aligned
+ *   T, accumulate, workspace, stream as dbf_matmul; workspace >=
+ *           dbf_grouped_workspace_bytes(fs, G, T)
+ * T <= dbf_decode_max_tokens(): two launches for the whole group (one per
+ * decode stage; every problem keeps its own shape), instead of one or two per
+ * problem.  Larger T: each problem runs the prefill kernels in turn.  Errors
+ * as dbf_matmul; DBF_ERR_UNSUPPORTED for G > 16 or when no common tile plan
+ * fits the group.
+ */
+int dbf_matmul_grouped(const dbf_factors *fs, int32_t G, const uint16_t *const *xs,
+                       uint16_t *const *ys, int64_t T, int accumulate, void *workspace,
+                       size_t ws_bytes, void *stream);
+
+/* Device workspace (bytes) dbf_matmul_grouped needs; 0 for invalid arguments. */
+size_t dbf_grouped_workspace_bytes(const dbf_factors *fs, int32_t G, int64_t T);
+
+/* Kernels one dbf_matmul_grouped call launches; -1 for invalid arguments. */
+int dbf_grouped_launch_count(const dbf_factors *fs, int32_t G, int64_t T);
+
 /* Device workspace (bytes) dbf_matmul needs for this shape and token count. */
 size_t dbf_workspace_bytes(const dbf_factors *f, int64_t T);
 

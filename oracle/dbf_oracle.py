@@ -329,6 +329,21 @@ def matmul(x_bits: np.ndarray, f, y_in_bits: np.ndarray | None = None):
     return y, round_to_bf16_bits(y)
 
 
+def matmul_grouped(x_bits_list, factor_list, y_in_bits_list=None):
+    """Reference for a grouped call: [(exact y, expected bf16 bits)] per problem.
+
+    Independent products with their own factors, e.g. layers whose middle
+    dimension differs (DBF page, section 2, Control Granular de Compresión:
+    the ratio is set per layer through k).  Each entry is `matmul` of its
+    own problem; nothing couples them.
+    """
+    out = []
+    for p, (xb, f) in enumerate(zip(x_bits_list, factor_list)):
+        y_in = None if y_in_bits_list is None else y_in_bits_list[p]
+        out.append(matmul(xb, f, y_in))
+    return out
+
+
 def matmul_segmented(x_bits: np.ndarray, adapters, seg_offsets, seg_adapter,
                      y_in_bits: np.ndarray | None = None):
     """Reference for a routed batch: tokens [off[s], off[s+1]) use adapter seg_adapter[s].

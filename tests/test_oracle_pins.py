@@ -445,3 +445,17 @@ def test_scale_grads_sampled_equals_full():
     part = O.scale_grads_sampled(x, dy, f, n, r, k)
     for want, got, idx in zip(full, part, (n, r, k)):
         np.testing.assert_allclose(got, want[:, idx], rtol=1e-12, atol=1e-12)
+
+
+def test_grouped_is_the_list_of_independent_products():
+    # a group couples nothing: each entry equals the plain call on its own problem, whatever the
+    # other problems are, and reordering the group reorders the results
+    shapes = [(12, 9, 5, 2), (20, 33, 17, 2), (7, 4, 30, 2)]
+    fs = [G.make_factors(N, M, R, ell, 90 + k) for k, (N, M, R, ell) in enumerate(shapes)]
+    xs = [G.make_x(3, f.M, 95 + k) for k, f in enumerate(fs)]
+    got = O.matmul_grouped(xs, fs)
+    rev = O.matmul_grouped(xs[::-1], fs[::-1])[::-1]
+    for (y, bits), (y2, bits2), xb, f in zip(got, rev, xs, fs):
+        yd = O.y_dense(O.bf16_bits_to_f64(xb), f)
+        np.testing.assert_allclose(y, yd, rtol=1e-12, atol=1e-12)
+        assert np.array_equal(bits, bits2)
