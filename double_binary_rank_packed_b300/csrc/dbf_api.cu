@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -53,6 +54,46 @@ int num_sms() {
         sms[dev] = v > 0 ? v : 148;
     }
     return sms[dev];
+}
+
+// Streams and events of the pipelined host-io call, created once per device.
+constexpr int kPipeSlots = 3;
+struct HostioPipe {
+    cudaStream_t in = nullptr, cmp = nullptr, out = nullptr;
+    cudaEvent_t fork = nullptr, join[3] = {nullptr, nullptr, nullptr};
+    cudaEvent_t h2d[kPipeSlots] = {}, done[kPipeSlots] = {}, d2h[kPipeSlots] = {};
+};
+std::mutex g_pipe_mu;
+
+HostioPipe *hostio_pipe(cudaError_t *err) {
+    static HostioPipe pipes[kMaxDevices];
+    static bool ready[kMaxDevices] = {false};
+    const int dev = current_device();
+    *err = cudaSuccess;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    HostioPipe &p = pipes[dev];
+    if (!ready[dev]) {
+        cudaError_t e = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.cmp, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking);
+        cudaEvent_t *all[] = {&p.fork, &p.join[0], &p.join[1], &p.join[2]};
+        for (cudaEvent_t *ev : all)
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        for (int k = 0; k < kPipeSlots && e == cudaSuccess; ++k) {
+            e = cudaEventCreateWithFlags(&p.h2d[k], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.done[k], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.d2h[k], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) {
+            *err = e;
+            return nullptr;
+        }
+        ready[dev] = true;
+    }
+    return &p;
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -638,6 +679,75 @@ int dbf_matmul_hostio(const dbf_factors *f, const uint16_t *x_host, int64_t T, u
     e = cudaMemcpyAsync(y_host, yd, size_t(T) * f->N * 2, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return cuda_fail(e, "hostio y readback");
     return DBF_OK;
+}
+
+size_t dbf_hostio_batch_workspace_bytes(const dbf_factors *fs, int32_t L, int64_t T) {
+    if (!fs || L < 1 || T < 0) return 0;
+    size_t slot = 0;
+    for (int l = 0; l < L; ++l) {
+        if (check_factors(&fs[l]) != DBF_OK) return 0;
+        slot = std::max(slot, align_up(dbf_hostio_workspace_bytes(&fs[l], T)));
+    }
+    return kPipeSlots * slot;
+}
+
+int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *const *x_host, uint16_t *const *y_host,
+                            int64_t T, int accumulate, void *workspace, size_t ws_bytes, void *stream) {
+    if (!fs || L < 0 || T < 0 || (accumulate != 0 && accumulate != 1)) return DBF_ERR_INVALID_ARG;
+    if (L == 0 || T == 0) return DBF_OK;
+    if (!x_host || !y_host) return DBF_ERR_INVALID_ARG;
+    size_t slot = 0;
+    for (int l = 0; l < L; ++l) {
+        const int rc = check_factors(&fs[l]);
+        if (rc) return rc;
+        if (!x_host[l] || !y_host[l]) return DBF_ERR_INVALID_ARG;
+        slot = std::max(slot, align_up(dbf_hostio_workspace_bytes(&fs[l], T)));
+    }
+    if (!workspace || ws_bytes < kPipeSlots * slot) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    cudaError_t e;
+    HostioPipe *p = hostio_pipe(&e);
+    if (!p) return cuda_fail(e, "hostio pipeline streams");
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    // fork: the three pipeline streams start after the work already on the caller's stream
+    e = cudaEventRecord(p->fork, user);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->in, p->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->cmp, p->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->out, p->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "hostio pipeline fork");
+    char *ws = static_cast<char *>(workspace);
+    for (int l = 0; l < L; ++l) {
+        const dbf_factors *f = &fs[l];
+        const int k = l % kPipeSlots;
+        char *base = ws + size_t(k) * slot;
+        uint16_t *xd = reinterpret_cast<uint16_t *>(base);
+        uint16_t *yd = reinterpret_cast<uint16_t *>(base + align_up(size_t(T) * f->M * 2));
+        char *inner = base + align_up(size_t(T) * f->M * 2) + align_up(size_t(T) * f->N * 2);
+        const size_t inner_bytes = slot - size_t(inner - base);
+        // copy-in: the slot is free once its previous read-back has finished
+        if (l >= kPipeSlots) e = cudaStreamWaitEvent(p->in, p->d2h[k], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(xd, x_host[l], size_t(T) * f->M * 2, cudaMemcpyHostToDevice, p->in);
+        if (e == cudaSuccess && accumulate)
+            e = cudaMemcpyAsync(yd, y_host[l], size_t(T) * f->N * 2, cudaMemcpyHostToDevice, p->in);
+        if (e == cudaSuccess) e = cudaEventRecord(p->h2d[k], p->in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(p->cmp, p->h2d[k], 0);
+        if (e != cudaSuccess) return cuda_fail(e, "hostio pipeline copy-in");
+        const int rc = dbf_matmul(f, xd, T, yd, accumulate, inner, inner_bytes, p->cmp);
+        if (rc) return rc;
+        e = cudaEventRecord(p->done[k], p->cmp);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(p->out, p->done[k], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(y_host[l], yd, size_t(T) * f->N * 2, cudaMemcpyDeviceToHost, p->out);
+        if (e == cudaSuccess) e = cudaEventRecord(p->d2h[k], p->out);
+        if (e != cudaSuccess) return cuda_fail(e, "hostio pipeline read-back");
+    }
+    // join: the caller's stream continues after all three pipeline streams
+    cudaStream_t ss[3] = {p->in, p->cmp, p->out};
+    for (int j = 0; j < 3 && e == cudaSuccess; ++j) {
+        e = cudaEventRecord(p->join[j], ss[j]);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(user, p->join[j], 0);
+    }
+    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "hostio pipeline join");
 }
 
 size_t dbf_segmented_workspace_bytes(int32_t N, int32_t M, int32_t R, int32_t ell, int64_t T, int32_t S) {

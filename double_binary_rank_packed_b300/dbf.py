@@ -39,7 +39,7 @@ EXPORTED = (
     "dbf_check_status", "dbf_selftest_bounded_wait", "dbf_status_string", "dbf_last_cuda_error",
     "dbf_launch_count", "dbf_segmented_launch_count", "dbf_transpose_packed", "dbf_factors_transposed",
     "dbf_backward", "dbf_backward_workspace_bytes", "dbf_matmul_grouped", "dbf_grouped_workspace_bytes",
-    "dbf_grouped_launch_count",
+    "dbf_grouped_launch_count", "dbf_matmul_hostio_batch", "dbf_hostio_batch_workspace_bytes",
 )
 
 
@@ -96,6 +96,8 @@ def _load():
         "dbf_matmul_grouped": (ci, [fp, i32, vp, vp, i64, ci, vp, sz, vp]),
         "dbf_grouped_workspace_bytes": (sz, [fp, i32, i64]),
         "dbf_grouped_launch_count": (ci, [fp, i32, i64]),
+        "dbf_matmul_hostio_batch": (ci, [fp, i32, vp, vp, i64, ci, vp, sz, vp]),
+        "dbf_hostio_batch_workspace_bytes": (sz, [fp, i32, i64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -375,6 +377,40 @@ def matmul_hostio(f: PackedFactors, x_host: torch.Tensor, y_host: torch.Tensor, 
                                 _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(rc, "dbf_matmul_hostio")
     return y_host
+
+
+def hostio_batch_workspace_bytes(fs, T: int) -> int:
+    return int(_lib.dbf_hostio_batch_workspace_bytes(_group_structs(fs), len(fs), T))
+
+
+def matmul_hostio_batch(fs, xs_host, ys_host, accumulate: bool = False, workspace: torch.Tensor | None = None,
+                        stream=None):
+    """L independent host-io calls, copies overlapped with the kernels (dbf_matmul_hostio_batch).
+
+    fs: list of PackedFactors; xs_host, ys_host: lists of CPU bf16 tensors [T, M_l] and [T, N_l]
+    (pinned for overlap).  Returns ys_host.
+    """
+    L = len(fs)
+    if L == 0:
+        return ys_host
+    if len(xs_host) != L or len(ys_host) != L:
+        raise ValueError("fs, xs_host and ys_host must have the same length")
+    T = xs_host[0].shape[0]
+    for f, x, y in zip(fs, xs_host, ys_host):
+        if x.device.type != "cpu" or y.device.type != "cpu" or not x.is_contiguous() or not y.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors")
+        if x.dtype != torch.bfloat16 or x.shape != (T, f.M) or y.dtype != torch.bfloat16 or y.shape != (T, f.N):
+            raise ValueError("x_host bf16 [T, M_l] and y_host bf16 [T, N_l] with one T")
+    structs = _group_structs(fs)
+    need = int(_lib.dbf_hostio_batch_workspace_bytes(structs, L, T))
+    if workspace is None:
+        workspace = new_workspace(need, "cuda")
+    xp = (ctypes.c_void_p * L)(*[x.data_ptr() for x in xs_host])
+    yp = (ctypes.c_void_p * L)(*[y.data_ptr() for y in ys_host])
+    rc = _lib.dbf_matmul_hostio_batch(structs, L, xp, yp, T, int(bool(accumulate)), _ptr(workspace),
+                                      workspace.numel(), _stream_handle(stream))
+    _check(rc, "dbf_matmul_hostio_batch")
+    return ys_host
 
 
 def adapter_table(adapters, device) -> torch.Tensor:

@@ -192,6 +192,29 @@ size_t dbf_grouped_workspace_bytes(const dbf_factors *fs, int32_t G, int64_t T);
 /* Kernels one dbf_matmul_grouped call launches; -1 for invalid arguments. */
 int dbf_grouped_launch_count(const dbf_factors *fs, int32_t G, int64_t T);
 
+/*
+ * dbf_matmul_hostio_batch: L independent dbf_matmul_hostio calls (host x in,
+ * host y out, each with its own factors fs[l]) pipelined over three slots of
+ * device buffers: the copy of x[l+1] to the device and of y[l-1] back to the
+ * host run while the kernels of call l run, on the library's own copy-in,
+ * compute and read-back streams, which start after the work already queued on
+ * `stream` and which `stream` waits for at the end (capturable in a CUDA graph
+ * that captures `stream`).
+ *   fs              host array of L descriptors
+ *   x_host, y_host  host arrays of L host pointers, bf16 [T][fs[l].M] and
+ *                   [T][fs[l].N]; page-locked memory for the copies to overlap
+ *   workspace       device, >= dbf_hostio_batch_workspace_bytes(fs, L, T)
+ * L = 0 or T = 0 is a no-op.  Host-thread safe (an internal lock); the
+ * pipeline streams are shared per device, so concurrent batches serialise.
+ * Errors as dbf_matmul.
+ */
+int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *const *x_host,
+                            uint16_t *const *y_host, int64_t T, int accumulate,
+                            void *workspace, size_t ws_bytes, void *stream);
+
+/* Device workspace (bytes) of dbf_matmul_hostio_batch; 0 for invalid arguments. */
+size_t dbf_hostio_batch_workspace_bytes(const dbf_factors *fs, int32_t L, int64_t T);
+
 /* Device workspace (bytes) dbf_matmul needs for this shape and token count. */
 size_t dbf_workspace_bytes(const dbf_factors *f, int64_t T);
 
