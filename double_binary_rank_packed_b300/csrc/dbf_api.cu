@@ -228,13 +228,13 @@ int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
     using namespace dbfk;
     const int ell = f->ell;
     const int64_t C = ell * T;
-    // activation tiles are the second grid dimension (at most 65535 of them)
-    if (ceil_div(C, prefill_bn(ell)) > 65535) return DBF_ERR_UNSUPPORTED;
     const int ldxs = static_cast<int>(xs_ld(f->M));
     const int ldv = static_cast<int>(v_ld(f->R));
     __half *xs = static_cast<__half *>(ws);
     __half *V = reinterpret_cast<__half *>(static_cast<char *>(ws) + align_up(size_t(C) * ldxs * 2));
-    const int bn = prefill_bn(ell);
+    // tile widths per GEMM; activation tiles are the second grid dimension (at most 65535 of them)
+    const int bn1 = prefill_pick_bn(ell, ldv, C, num_sms()), bn2 = prefill_pick_bn(ell, f->N, C, num_sms());
+    if (bn1 == 0 || bn2 == 0) return DBF_ERR_UNSUPPORTED;
 
     cudaError_t e = launch_prefill_prologue(reinterpret_cast<const __nv_bfloat16 *>(x), static_cast<int>(T), f->M,
                                             f->M, reinterpret_cast<const __half *>(f->gamma), ell, xs, ldxs, stream,
@@ -242,8 +242,8 @@ int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
     if (e != cudaSuccess) return cuda_fail(e, "prefill prologue");
 
     CUtensorMap map1, map2;
-    if (!encode_act_map(&map1, xs, static_cast<int>(C), ldxs, ldxs, bn) ||
-        !encode_act_map(&map2, V, static_cast<int>(C), ldv, ldv, bn)) {
+    if (!encode_act_map(&map1, xs, static_cast<int>(C), ldxs, ldxs, bn1) ||
+        !encode_act_map(&map2, V, static_cast<int>(C), ldv, ldv, bn2)) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
         return DBF_ERR_CUDA;
     }
@@ -266,7 +266,7 @@ int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
     a1.rows_store = ldv;
     a1.Kw = static_cast<int>(ceil_div(f->M, 32));
     a1.nk = static_cast<int>(ceil_div(f->M, 64));
-    e = launch_prefill_gemm(1, map1, a1, bn, stream, true);
+    e = launch_prefill_gemm(1, map1, a1, bn1, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "prefill gemm 1");
 
     PfArgs a2 = a;
@@ -276,7 +276,7 @@ int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
     a2.rows_store = f->N;
     a2.Kw = static_cast<int>(ceil_div(f->R, 32));
     a2.nk = static_cast<int>(ceil_div(f->R, 64));
-    e = launch_prefill_gemm(2, map2, a2, bn, stream, true);
+    e = launch_prefill_gemm(2, map2, a2, bn2, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "prefill gemm 2");
     return DBF_OK;
 }
@@ -300,7 +300,6 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     using namespace dbfk;
     const int ell = f->ell;
     const int64_t C = ell * T;
-    if (ceil_div(C, prefill_bn(ell)) > 65535) return DBF_ERR_UNSUPPORTED;
     const int N = f->N, M = f->M, R = f->R;
     const int ldv = static_cast<int>(v_ld(R));
     const int ldm = static_cast<int>(xs_ld(M)), ldn = static_cast<int>(xs_ld(N));
@@ -308,7 +307,10 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     __half *xs = reinterpret_cast<__half *>(base);
     __half *V = reinterpret_cast<__half *>(base + align_up(size_t(C) * xs_ld(std::max(M, N)) * 2));
     __half *H = reinterpret_cast<__half *>(reinterpret_cast<char *>(V) + align_up(size_t(C) * ldv * 2));
-    const int bn = prefill_bn(ell);
+    // tile widths of the four GEMMs: rows R, N, R and M
+    const int bnR = prefill_pick_bn(ell, ldv, C, num_sms()), bnN = prefill_pick_bn(ell, N, C, num_sms());
+    const int bnM = prefill_pick_bn(ell, M, C, num_sms());
+    if (bnR == 0 || bnN == 0 || bnM == 0) return DBF_ERR_UNSUPPORTED;
     const auto *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
     const auto *dyb = reinterpret_cast<const __nv_bfloat16 *>(dy);
     const auto *alpha = reinterpret_cast<const __half *>(f->alpha);
@@ -332,7 +334,7 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     e = launch_prefill_prologue(xb, static_cast<int>(T), M, M, gamma, ell, xs, ldm, stream, false);
     if (e != cudaSuccess) return cuda_fail(e, "backward prologue x");
     CUtensorMap map;
-    if (!encode_act_map(&map, xs, static_cast<int>(C), ldm, ldm, bn)) {
+    if (!encode_act_map(&map, xs, static_cast<int>(C), ldm, ldm, bnR)) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
         return DBF_ERR_CUDA;
     }
@@ -345,10 +347,10 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     s1.nk = static_cast<int>(ceil_div(M, 64));
     s1.beta = beta;
     s1.h_out = H;
-    e = launch_prefill_gemm(1, map, s1, bn, stream, true);
+    e = launch_prefill_gemm(1, map, s1, bnR, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward gemm: x -> V, H");
 
-    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bn)) {
+    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bnN)) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
         return DBF_ERR_CUDA;
     }
@@ -365,13 +367,13 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     s2.red_src = dyb;
     s2.ld_src = N;
     s2.red = dalpha;
-    e = launch_prefill_gemm(2, map, s2, bn, stream, true);
+    e = launch_prefill_gemm(2, map, s2, bnN, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward gemm: dalpha");
 
     // ---- through the transposed factors: V' and dbeta, then dx and dgamma
     e = launch_prefill_prologue(dyb, static_cast<int>(T), N, N, alpha, ell, xs, ldn, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward prologue dy");
-    if (!encode_act_map(&map, xs, static_cast<int>(C), ldn, ldn, bn)) {
+    if (!encode_act_map(&map, xs, static_cast<int>(C), ldn, ldn, bnR)) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
         return DBF_ERR_CUDA;
     }
@@ -385,10 +387,10 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     t1.beta = beta;
     t1.h_in = H;
     t1.red = dbeta;
-    e = launch_prefill_gemm(1, map, t1, bn, stream, true);
+    e = launch_prefill_gemm(1, map, t1, bnR, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward gemm: dbeta");
 
-    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bn)) {
+    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bnM)) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
         return DBF_ERR_CUDA;
     }
@@ -406,7 +408,7 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     t2.red_src = xb;
     t2.ld_src = M;
     t2.red = dgamma;
-    e = launch_prefill_gemm(2, map, t2, bn, stream, true);
+    e = launch_prefill_gemm(2, map, t2, bnM, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward gemm: dx, dgamma");
     return DBF_OK;
 }

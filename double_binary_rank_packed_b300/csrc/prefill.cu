@@ -534,19 +534,51 @@ cudaError_t launch_gemm_t(const CUtensorMap &map, const PfArgs &a, cudaStream_t 
 }
 
 template <int STAGE>
-cudaError_t launch_gemm_stage(const CUtensorMap &map, const PfArgs &a, cudaStream_t stream, bool pdl) {
-    switch (a.ell) {
-        case 1: return launch_gemm_t<256, STAGE, 1>(map, a, stream, pdl);
-        case 2: return launch_gemm_t<256, STAGE, 2>(map, a, stream, pdl);
-        case 3: return launch_gemm_t<240, STAGE, 3>(map, a, stream, pdl);
-        case 4: return launch_gemm_t<256, STAGE, 4>(map, a, stream, pdl);
+cudaError_t launch_gemm_stage(const CUtensorMap &map, const PfArgs &a, int bn, cudaStream_t stream, bool pdl) {
+    switch (a.ell * 1000 + bn) {
+        case 1256: return launch_gemm_t<256, STAGE, 1>(map, a, stream, pdl);
+        case 1240: return launch_gemm_t<240, STAGE, 1>(map, a, stream, pdl);
+        case 1192: return launch_gemm_t<192, STAGE, 1>(map, a, stream, pdl);
+        case 2256: return launch_gemm_t<256, STAGE, 2>(map, a, stream, pdl);
+        case 2240: return launch_gemm_t<240, STAGE, 2>(map, a, stream, pdl);
+        case 2192: return launch_gemm_t<192, STAGE, 2>(map, a, stream, pdl);
+        case 3240: return launch_gemm_t<240, STAGE, 3>(map, a, stream, pdl);
+        case 3192: return launch_gemm_t<192, STAGE, 3>(map, a, stream, pdl);
+        case 4256: return launch_gemm_t<256, STAGE, 4>(map, a, stream, pdl);
+        case 4224: return launch_gemm_t<224, STAGE, 4>(map, a, stream, pdl);
+        case 4192: return launch_gemm_t<192, STAGE, 4>(map, a, stream, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-int prefill_bn(int ell) { return ell == 3 ? 240 : 256; }
+// Activation rows per tile of one GEMM launch.  The candidates are multiples
+// of 16 (MMA N) and of 8*ell (whole tokens per epilogue chunk); the model is
+// the slowest SM: whole waves of tiles (one CTA per SM) times the time of a
+// K step, measured at max(2*BN, ~400) cycles for a 128-row tile with its A
+// operand in tensor memory.  Equal costs keep the wider tile (fewer tile
+// prologues and epilogues).  0 when no candidate keeps the grid's second
+// dimension within 65535.
+int prefill_pick_bn(int ell, int rows_cover, int64_t C, int num_sms) {
+    static const int w12[] = {256, 240, 192}, w3[] = {240, 192}, w4[] = {256, 224, 192};
+    const int *w = (ell == 3) ? w3 : (ell == 4 ? w4 : w12);
+    const int nw = (ell == 3) ? 2 : 3;
+    const int64_t rb = (rows_cover + 127) / 128;
+    int best = 0;
+    double best_cost = 1e300;
+    for (int k = 0; k < nw; ++k) {
+        const int64_t cb = (C + w[k] - 1) / w[k];
+        if (cb > 65535) continue;
+        const double waves = std::ceil(double(rb * cb) / std::max(num_sms, 1));
+        const double cost = waves * std::max(2.0 * w[k], 400.0);
+        if (cost < best_cost * (1.0 - 1e-9)) {
+            best_cost = cost;
+            best = w[k];
+        }
+    }
+    return best;
+}
 
 cudaError_t launch_prefill_prologue(const __nv_bfloat16 *x, int T, int M, int ldx, const __half *gamma, int ell,
                                     __half *xs, int ldxs, cudaStream_t stream, bool pdl) {
@@ -567,9 +599,8 @@ cudaError_t launch_prefill_prologue(const __nv_bfloat16 *x, int T, int M, int ld
 
 cudaError_t launch_prefill_gemm(int stage, const CUtensorMap &act_map, const PfArgs &args, int bn,
                                 cudaStream_t stream, bool pdl) {
-    (void)bn;
-    return stage == 1 ? launch_gemm_stage<1>(act_map, args, stream, pdl)
-                      : launch_gemm_stage<2>(act_map, args, stream, pdl);
+    return stage == 1 ? launch_gemm_stage<1>(act_map, args, bn, stream, pdl)
+                      : launch_gemm_stage<2>(act_map, args, bn, stream, pdl);
 }
 
 // Tensor map over an fp16 activation matrix [rows][ld] (logical K extent
