@@ -233,7 +233,8 @@ int run_prefill(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
     __half *xs = static_cast<__half *>(ws);
     __half *V = reinterpret_cast<__half *>(static_cast<char *>(ws) + align_up(size_t(C) * ldxs * 2));
     // tile widths per GEMM; activation tiles are the second grid dimension (at most 65535 of them)
-    const int bn1 = prefill_pick_bn(ell, ldv, C, num_sms()), bn2 = prefill_pick_bn(ell, f->N, C, num_sms());
+    const int bn1 = prefill_pick_bn(ell, ldv, C, static_cast<int>(ceil_div(f->M, 64)), num_sms());
+    const int bn2 = prefill_pick_bn(ell, f->N, C, static_cast<int>(ceil_div(f->R, 64)), num_sms());
     if (bn1 == 0 || bn2 == 0) return DBF_ERR_UNSUPPORTED;
 
     cudaError_t e = launch_prefill_prologue(reinterpret_cast<const __nv_bfloat16 *>(x), static_cast<int>(T), f->M,
@@ -308,9 +309,11 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     __half *V = reinterpret_cast<__half *>(base + align_up(size_t(C) * xs_ld(std::max(M, N)) * 2));
     __half *H = reinterpret_cast<__half *>(reinterpret_cast<char *>(V) + align_up(size_t(C) * ldv * 2));
     // tile widths of the four GEMMs: rows R, N, R and M
-    const int bnR = prefill_pick_bn(ell, ldv, C, num_sms()), bnN = prefill_pick_bn(ell, N, C, num_sms());
-    const int bnM = prefill_pick_bn(ell, M, C, num_sms());
-    if (bnR == 0 || bnN == 0 || bnM == 0) return DBF_ERR_UNSUPPORTED;
+    const int nkM = static_cast<int>(ceil_div(M, 64)), nkN = static_cast<int>(ceil_div(N, 64));
+    const int nkR = static_cast<int>(ceil_div(R, 64));
+    const int bn1 = prefill_pick_bn(ell, ldv, C, nkM, num_sms()), bn2 = prefill_pick_bn(ell, N, C, nkR, num_sms());
+    const int bn3 = prefill_pick_bn(ell, ldv, C, nkN, num_sms()), bn4 = prefill_pick_bn(ell, M, C, nkR, num_sms());
+    if (bn1 == 0 || bn2 == 0 || bn3 == 0 || bn4 == 0) return DBF_ERR_UNSUPPORTED;
     const auto *xb = reinterpret_cast<const __nv_bfloat16 *>(x);
     const auto *dyb = reinterpret_cast<const __nv_bfloat16 *>(dy);
     const auto *alpha = reinterpret_cast<const __half *>(f->alpha);
@@ -334,7 +337,7 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     e = launch_prefill_prologue(xb, static_cast<int>(T), M, M, gamma, ell, xs, ldm, stream, false);
     if (e != cudaSuccess) return cuda_fail(e, "backward prologue x");
     CUtensorMap map;
-    if (!encode_act_map(&map, xs, static_cast<int>(C), ldm, ldm, bnR)) {
+    if (!encode_act_map(&map, xs, static_cast<int>(C), ldm, ldm, bn1)) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
         return DBF_ERR_CUDA;
     }
@@ -347,10 +350,10 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     s1.nk = static_cast<int>(ceil_div(M, 64));
     s1.beta = beta;
     s1.h_out = H;
-    e = launch_prefill_gemm(1, map, s1, bnR, stream, true);
+    e = launch_prefill_gemm(1, map, s1, bn1, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward gemm: x -> V, H");
 
-    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bnN)) {
+    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bn2)) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
         return DBF_ERR_CUDA;
     }
@@ -367,13 +370,13 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     s2.red_src = dyb;
     s2.ld_src = N;
     s2.red = dalpha;
-    e = launch_prefill_gemm(2, map, s2, bnN, stream, true);
+    e = launch_prefill_gemm(2, map, s2, bn2, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward gemm: dalpha");
 
     // ---- through the transposed factors: V' and dbeta, then dx and dgamma
     e = launch_prefill_prologue(dyb, static_cast<int>(T), N, N, alpha, ell, xs, ldn, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward prologue dy");
-    if (!encode_act_map(&map, xs, static_cast<int>(C), ldn, ldn, bnR)) {
+    if (!encode_act_map(&map, xs, static_cast<int>(C), ldn, ldn, bn3)) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
         return DBF_ERR_CUDA;
     }
@@ -387,10 +390,10 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     t1.beta = beta;
     t1.h_in = H;
     t1.red = dbeta;
-    e = launch_prefill_gemm(1, map, t1, bnR, stream, true);
+    e = launch_prefill_gemm(1, map, t1, bn3, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward gemm: dbeta");
 
-    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bnM)) {
+    if (!encode_act_map(&map, V, static_cast<int>(C), ldv, ldv, bn4)) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed");
         return DBF_ERR_CUDA;
     }
@@ -408,7 +411,7 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
     t2.red_src = xb;
     t2.ld_src = M;
     t2.red = dgamma;
-    e = launch_prefill_gemm(2, map, t2, bnM, stream, true);
+    e = launch_prefill_gemm(2, map, t2, bn4, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "backward gemm: dx, dgamma");
     return DBF_OK;
 }

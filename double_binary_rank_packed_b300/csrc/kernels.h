@@ -171,7 +171,7 @@ cudaError_t launch_prefill_prologue(const __nv_bfloat16 *x, int T, int M, int ld
                                     __half *xs, int ldxs, cudaStream_t stream, bool pdl);
 cudaError_t launch_prefill_gemm(int stage, const CUtensorMap &act_map, const PfArgs &args, int bn,
                                 cudaStream_t stream, bool pdl);
-int prefill_pick_bn(int ell, int rows_cover, int64_t C, int num_sms);
+int prefill_pick_bn(int ell, int rows_cover, int64_t C, int nk, int num_sms);
 bool encode_act_map(CUtensorMap *map, const __half *base, int rows, int cols_pad, int ld, int box_rows);
 
 // --------------------------------------------------------------- misc

@@ -34,14 +34,27 @@ namespace dbfk {
 namespace {
 
 constexpr int kPfThreads = 192;
-constexpr int kStages = 6;
 constexpr int kBK = 64;  // K elements per stage (128 bytes of fp16)
 
+// Tile layouts.  BN = 192: two CTAs per SM, each with 256 tensor-memory
+// columns (accumulator [0, 192), a 2-stage ring of A slices after it) and a
+// 4-stage shared-memory ring; the two CTAs interleave their MMA streams and
+// hide each other's tile prologue and epilogue.  Wider tiles: one CTA per SM,
+// 6-stage rings, all 512 columns.  The A ring (signs in tensor memory) and
+// the activation ring (shared memory) have their own barriers.
 template <int BN>
 struct PfSmem {
+    static constexpr bool kPair = BN <= 192;
+    static constexpr int kStages = kPair ? 4 : 6;    // shared-memory ring
+    static constexpr int kAStages = kPair ? 2 : 6;   // tensor-memory ring
+    static constexpr uint32_t kTmemCols = kPair ? 256 : 512;
+    static constexpr uint32_t kAOff = kPair ? 192 : 256;  // first A-ring column
     static constexpr int kTileBytes = BN * 128;
     static constexpr int kBarOffset = kStages * kTileBytes;
     static constexpr int kBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+    static_assert(kAOff >= BN && kAOff + 32 * kAStages <= kTmemCols, "tensor memory layout");
+    static_assert(!kPair || 3 * (kBytes + 1024) > 228 * 1024, "a third CTA must not fit next to two");
+    static_assert(2 * kStages + 2 * kAStages + 2 <= 30, "barrier area");
 };
 
 __device__ __forceinline__ uint32_t tmem_lane_base(int q) { return static_cast<uint32_t>(32 * q) << 16; }
@@ -102,17 +115,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int kStages = PfSmem<BN>::kStages, kAStages = PfSmem<BN>::kAStages;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PfSmem<BN>::kBarOffset);
-    uint64_t *act_full = bars;                 // [kStages]
-    uint64_t *a_full = bars + kStages;         // [kStages]
-    uint64_t *empty = bars + 2 * kStages;      // [kStages]
-    uint64_t *acc_full = bars + 3 * kStages;   // [1]
+    uint64_t *act_full = bars;                 // [kStages] activation slice landed
+    uint64_t *empty = bars + kStages;          // [kStages] MMAs that read the slice are done
+    uint64_t *a_full = bars + 2 * kStages;     // [kAStages] 128 unpack threads wrote the A slice
+    uint64_t *a_empty = a_full + kAStages;     // [kAStages] MMAs that read the A slice are done
+    uint64_t *acc_full = a_empty + kAStages;   // [1]
     uint64_t *drain = acc_full + 1;            // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    constexpr uint32_t kTmemCols = 512;
-    constexpr uint32_t kAccCols = 256;           // accumulator columns [0, BN)
+    constexpr uint32_t kTmemCols = PfSmem<BN>::kTmemCols;
+    constexpr uint32_t kAccCols = PfSmem<BN>::kAOff;  // accumulator columns [0, BN), the A ring after
     constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -126,8 +141,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&act_full[s], 1);
-            mbar_init(&a_full[s], 128);
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(&a_full[s], 128);
+            mbar_init(&a_empty[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(drain, 1);
@@ -175,23 +193,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
         // the whole warp runs the loop; one elected lane issues the MMAs and
         // the commits
         for (int ks = 0; ks < nk; ++ks) {
-            const int s = ks % kStages;
-            const uint32_t par = (ks / kStages) & 1;
-            const bool ready =
-                mbar_wait_bounded(&act_full[s], par, abort_flag) && mbar_wait_bounded(&a_full[s], par, abort_flag);
+            const int s = ks % kStages, sa = ks % kAStages;
+            const bool ready = mbar_wait_bounded(&act_full[s], (ks / kStages) & 1, abort_flag) &&
+                               mbar_wait_bounded(&a_full[sa], (ks / kAStages) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, ready)) {
                 *abort_flag = 1;
                 record_status(a.status, DBF_ERR_TIMEOUT);
                 break;
             }
             tc_fence_after();
-            const uint32_t a_col = tmem + kAccCols + s * 32;
+            const uint32_t a_col = tmem + kAccCols + sa * 32;
             const uint32_t b_addr = smem_u32(smem + s * PfSmem<BN>::kTileBytes);
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)
                     tc_mma_ts(tmem, a_col + kk * 8, desc_sw128(b_addr + kk * 32), kIdesc, (ks | kk) != 0);
                 tc_commit(&empty[s]);
+                tc_commit(&a_empty[sa]);
             }
             __syncwarp();
         }
@@ -228,10 +246,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
             for (int u = 0; u < 4; ++u) {
                 const int ks = kb * 4 + u;
                 if (ks >= nk || !ok) break;
-                const int s = ks % kStages;
-                const uint32_t n = ks / kStages;
+                const int s = ks % kAStages;
+                const uint32_t n = ks / kAStages;
                 // warp-uniform decision: tcgen05.st below is a warp-collective instruction
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (n & 1) ^ 1, abort_flag))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&a_empty[s], (n & 1) ^ 1, abort_flag))) {
                     *abort_flag = 1;
                     record_status(a.status, DBF_ERR_TIMEOUT);
                     ok = false;
@@ -555,23 +573,32 @@ cudaError_t launch_gemm_stage(const CUtensorMap &map, const PfArgs &a, int bn, c
 
 // Activation rows per tile of one GEMM launch.  The candidates are multiples
 // of 16 (MMA N) and of 8*ell (whole tokens per epilogue chunk); the model is
-// the slowest SM: whole waves of tiles (one CTA per SM) times the time of a
-// K step, measured at max(2*BN, ~400) cycles for a 128-row tile with its A
-// operand in tensor memory.  Equal costs keep the wider tile (fewer tile
-// prologues and epilogues).  0 when no candidate keeps the grid's second
-// dimension within 65535.
-int prefill_pick_bn(int ell, int rows_cover, int64_t C, int num_sms) {
+// the slowest SM: whole waves of tiles times the time of a wave.  One CTA per
+// SM: a K step measured max(2*BN, ~400) cycles for a 128-row tile with its A
+// operand in tensor memory, plus a tile's prologue, pipeline fill and
+// epilogue (~8 us, from the gap between that rate and the measured GEMMs).
+// Two CTAs per SM (BN = 192): their MMA streams keep the pipe busy at 2*BN
+// cycles a step each, and the per-tile costs overlap the other CTA's MMAs.
+// Equal costs keep the first candidate.  0 when no candidate keeps the grid's
+// second dimension within 65535.
+int prefill_pick_bn(int ell, int rows_cover, int64_t C, int nk, int num_sms) {
     static const int w12[] = {256, 240, 192}, w3[] = {240, 192}, w4[] = {256, 224, 192};
     const int *w = (ell == 3) ? w3 : (ell == 4 ? w4 : w12);
     const int nw = (ell == 3) ? 2 : 3;
     const int64_t rb = (rows_cover + 127) / 128;
+    const double tile_cost = 15000.0;  // cycles
     int best = 0;
     double best_cost = 1e300;
     for (int k = 0; k < nw; ++k) {
         const int64_t cb = (C + w[k] - 1) / w[k];
         if (cb > 65535) continue;
-        const double waves = std::ceil(double(rb * cb) / std::max(num_sms, 1));
-        const double cost = waves * std::max(2.0 * w[k], 400.0);
+        const double tiles = double(rb * cb);
+        const int sms = std::max(num_sms, 1);
+        double cost;
+        if (w[k] <= 192)
+            cost = std::ceil(tiles / (2.0 * sms)) * (2.0 * nk * 2.0 * w[k] + 0.5 * tile_cost);
+        else
+            cost = std::ceil(tiles / sms) * (nk * std::max(2.0 * w[k], 400.0) + tile_cost);
         if (cost < best_cost * (1.0 - 1e-9)) {
             best_cost = cost;
             best = w[k];
