@@ -4,6 +4,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -23,6 +25,7 @@ thread_local char g_last_error[256] = "";
 
 int cuda_fail(cudaError_t e, const char *where) {
     snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+    cudaGetLastError();  // a failed call leaves no error behind for the next launch check to pick up
     return DBF_ERR_CUDA;
 }
 
@@ -686,14 +689,71 @@ int dbf_matmul_hostio(const dbf_factors *f, const uint16_t *x_host, int64_t T, u
     return DBF_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+constexpr int kPipeChunk = 16;  // calls whose host buffers are contiguous share one copy each way
+
+// [start, end) of the allocation that holds host pointer p, as the driver
+// knows it (page-locked memory under unified addressing); false for memory
+// the driver does not know (pageable), whose calls are then copied one by one.
+bool host_allocation(const void *p, uintptr_t *start, uintptr_t *end) {
+    static PFN_cuPointerGetAttribute_v4000 get = nullptr;
+    static bool looked = false;
+    if (!looked) {
+        looked = true;
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &fn, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get = reinterpret_cast<PFN_cuPointerGetAttribute_v4000>(fn);
+    }
+    if (!get) return false;
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    const CUdeviceptr dp = static_cast<CUdeviceptr>(reinterpret_cast<uintptr_t>(p));
+    if (get(&base, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, dp) != CUDA_SUCCESS ||
+        get(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, dp) != CUDA_SUCCESS || size == 0) {
+        cudaGetLastError();
+        return false;
+    }
+    *start = static_cast<uintptr_t>(base);
+    *end = static_cast<uintptr_t>(base) + size;
+    return *start <= reinterpret_cast<uintptr_t>(p) && reinterpret_cast<uintptr_t>(p) < *end;
+}
+
+struct BatchSizes {
+    size_t x, y, inner, slot;  // per call maxima (aligned) and one slot
+};
+
+// Slot layout: x of up to kPipeChunk calls back to back, then their y, then
+// one inner workspace (the calls of a chunk run one after another on one
+// stream, so they share it, as consecutive dbf_matmul calls do).
+int batch_sizes(const dbf_factors *fs, int32_t L, int64_t T, BatchSizes *b) {
+    *b = {};
+    for (int l = 0; l < L; ++l) {
+        const int rc = check_factors(&fs[l]);
+        if (rc) return rc;
+        b->x = std::max(b->x, size_t(T) * fs[l].M * 2);
+        b->y = std::max(b->y, size_t(T) * fs[l].N * 2);
+        b->inner = std::max(b->inner, align_up(ws_for(&fs[l], T, DBF_PATH_AUTO)));
+    }
+    const size_t chunk = size_t(std::min(L, kPipeChunk));
+    b->slot = align_up(chunk * b->x) + align_up(chunk * b->y) + b->inner;
+    return DBF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t dbf_hostio_batch_workspace_bytes(const dbf_factors *fs, int32_t L, int64_t T) {
     if (!fs || L < 1 || T < 0) return 0;
-    size_t slot = 0;
-    for (int l = 0; l < L; ++l) {
-        if (check_factors(&fs[l]) != DBF_OK) return 0;
-        slot = std::max(slot, align_up(dbf_hostio_workspace_bytes(&fs[l], T)));
-    }
-    return kPipeSlots * slot;
+    BatchSizes b;
+    if (batch_sizes(fs, L, T, &b) != DBF_OK) return 0;
+    return kPipeSlots * b.slot;
 }
 
 int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *const *x_host, uint16_t *const *y_host,
@@ -701,14 +761,12 @@ int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *co
     if (!fs || L < 0 || T < 0 || (accumulate != 0 && accumulate != 1)) return DBF_ERR_INVALID_ARG;
     if (L == 0 || T == 0) return DBF_OK;
     if (!x_host || !y_host) return DBF_ERR_INVALID_ARG;
-    size_t slot = 0;
-    for (int l = 0; l < L; ++l) {
-        const int rc = check_factors(&fs[l]);
-        if (rc) return rc;
+    BatchSizes b;
+    int rc = batch_sizes(fs, L, T, &b);
+    if (rc) return rc;
+    for (int l = 0; l < L; ++l)
         if (!x_host[l] || !y_host[l]) return DBF_ERR_INVALID_ARG;
-        slot = std::max(slot, align_up(dbf_hostio_workspace_bytes(&fs[l], T)));
-    }
-    if (!workspace || ws_bytes < kPipeSlots * slot) return DBF_ERR_WORKSPACE;
+    if (!workspace || ws_bytes < kPipeSlots * b.slot) return DBF_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
     std::lock_guard<std::mutex> lock(g_pipe_mu);
     cudaError_t e;
@@ -722,29 +780,61 @@ int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *co
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p->out, p->fork, 0);
     if (e != cudaSuccess) return cuda_fail(e, "hostio pipeline fork");
     char *ws = static_cast<char *>(workspace);
-    for (int l = 0; l < L; ++l) {
-        const dbf_factors *f = &fs[l];
-        const int k = l % kPipeSlots;
-        char *base = ws + size_t(k) * slot;
-        uint16_t *xd = reinterpret_cast<uint16_t *>(base);
-        uint16_t *yd = reinterpret_cast<uint16_t *>(base + align_up(size_t(T) * f->M * 2));
-        char *inner = base + align_up(size_t(T) * f->M * 2) + align_up(size_t(T) * f->N * 2);
-        const size_t inner_bytes = slot - size_t(inner - base);
+    const size_t chunk_cap = size_t(std::min(L, kPipeChunk));
+    int l0 = 0;
+    for (int c = 0; l0 < L; ++c) {
+        // the chunk: calls l0 .. l1-1 whose host x (and y) follow one another in memory, with
+        // byte sizes that keep every device copy 16-byte aligned
+        auto xbytes = [&](int l) { return size_t(T) * fs[l].M * 2; };
+        auto ybytes = [&](int l) { return size_t(T) * fs[l].N * 2; };
+        // (both ends of a merged copy inside one allocation)
+        int l1 = l0 + 1;
+        uintptr_t xa = 0, xe = 0, ya = 0, ye = 0;
+        if (chunk_cap > 1 && host_allocation(x_host[l0], &xa, &xe) && host_allocation(y_host[l0], &ya, &ye)) {
+            while (l1 < L && size_t(l1 - l0) < chunk_cap && xbytes(l1 - 1) % 16 == 0 && ybytes(l1 - 1) % 16 == 0) {
+                const uintptr_t xp = reinterpret_cast<uintptr_t>(x_host[l1]);
+                const uintptr_t yp = reinterpret_cast<uintptr_t>(y_host[l1]);
+                if (xp != reinterpret_cast<uintptr_t>(x_host[l1 - 1]) + xbytes(l1 - 1) ||
+                    yp != reinterpret_cast<uintptr_t>(y_host[l1 - 1]) + ybytes(l1 - 1) || xp + xbytes(l1) > xe ||
+                    yp + ybytes(l1) > ye)
+                    break;
+                ++l1;
+            }
+        }
+        size_t xs = 0, ys = 0;
+        for (int l = l0; l < l1; ++l) {
+            xs += xbytes(l);
+            ys += ybytes(l);
+        }
+        const int k = c % kPipeSlots;
+        char *base = ws + size_t(k) * b.slot;
+        char *xd = base;
+        char *yd = base + align_up(chunk_cap * b.x);
+        char *inner = yd + align_up(chunk_cap * b.y);
         // copy-in: the slot is free once its previous read-back has finished
-        if (l >= kPipeSlots) e = cudaStreamWaitEvent(p->in, p->d2h[k], 0);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(xd, x_host[l], size_t(T) * f->M * 2, cudaMemcpyHostToDevice, p->in);
-        if (e == cudaSuccess && accumulate)
-            e = cudaMemcpyAsync(yd, y_host[l], size_t(T) * f->N * 2, cudaMemcpyHostToDevice, p->in);
-        if (e == cudaSuccess) e = cudaEventRecord(p->h2d[k], p->in);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(p->cmp, p->h2d[k], 0);
-        if (e != cudaSuccess) return cuda_fail(e, "hostio pipeline copy-in");
-        const int rc = dbf_matmul(f, xd, T, yd, accumulate, inner, inner_bytes, p->cmp);
-        if (rc) return rc;
+        if (c >= kPipeSlots && (e = cudaStreamWaitEvent(p->in, p->d2h[k], 0)) != cudaSuccess)
+            return cuda_fail(e, "hostio pipeline: wait for a free slot");
+        if ((e = cudaMemcpyAsync(xd, x_host[l0], xs, cudaMemcpyHostToDevice, p->in)) != cudaSuccess)
+            return cuda_fail(e, "hostio pipeline: copy x in");
+        if (accumulate && (e = cudaMemcpyAsync(yd, y_host[l0], ys, cudaMemcpyHostToDevice, p->in)) != cudaSuccess)
+            return cuda_fail(e, "hostio pipeline: copy y in");
+        if ((e = cudaEventRecord(p->h2d[k], p->in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(p->cmp, p->h2d[k], 0)) != cudaSuccess)
+            return cuda_fail(e, "hostio pipeline: hand the slot to the compute stream");
+        size_t xo = 0, yo = 0;
+        for (int l = l0; l < l1; ++l) {
+            rc = dbf_matmul(&fs[l], reinterpret_cast<const uint16_t *>(xd + xo), T,
+                            reinterpret_cast<uint16_t *>(yd + yo), accumulate, inner, b.inner, p->cmp);
+            if (rc) return rc;
+            xo += xbytes(l);
+            yo += ybytes(l);
+        }
         e = cudaEventRecord(p->done[k], p->cmp);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(p->out, p->done[k], 0);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(y_host[l], yd, size_t(T) * f->N * 2, cudaMemcpyDeviceToHost, p->out);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(y_host[l0], yd, ys, cudaMemcpyDeviceToHost, p->out);
         if (e == cudaSuccess) e = cudaEventRecord(p->d2h[k], p->out);
         if (e != cudaSuccess) return cuda_fail(e, "hostio pipeline read-back");
+        l0 = l1;
     }
     // join: the caller's stream continues after all three pipeline streams
     cudaStream_t ss[3] = {p->in, p->cmp, p->out};

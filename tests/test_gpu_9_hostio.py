@@ -88,3 +88,29 @@ def test_hostio_batch_empty_and_errors(cuda_lib):
     structs = (cuda_lib.DbfFactors * 1)(f.struct)
     assert cuda_lib._lib.dbf_matmul_hostio_batch(structs, 1, None, None, 4, 0, None, 0, None) == -1
     assert cuda_lib._lib.dbf_hostio_batch_workspace_bytes(structs, 0, 4) == 0
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_hostio_batch_contiguous_buffers_share_copies(cuda_lib, accumulate):
+    # calls whose host buffers follow one another are moved in chunks of up to 16 with one copy each
+    # way; 37 calls give chunks of 16, 16 and 5, and the shapes differ from call to call
+    T = 8
+    shapes = [(256, 512, 32), (512, 256, 48), (384, 384, 40)]
+    fs = [G.make_factors(*shapes[k % 3], 1, 4700 + k) for k in range(37)]
+    dfs = [U.device_factors(f) for f in fs]
+    xbs = [G.make_x(T, f.M, 4800 + k) for k, f in enumerate(fs)]
+    ybs = [G.make_x(T, f.N, 4900 + k) for k, f in enumerate(fs)]
+    xall = torch.from_numpy(np.concatenate([b.ravel() for b in xbs]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    yall = torch.from_numpy(np.concatenate([b.ravel() for b in ybs]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    xs, ys, ox, oy = [], [], 0, 0
+    for f in fs:
+        xs.append(xall[ox:ox + T * f.M].view(T, f.M))
+        ys.append(yall[oy:oy + T * f.N].view(T, f.N))
+        ox += T * f.M
+        oy += T * f.N
+    cuda_lib.matmul_hostio_batch(dfs, xs, ys, accumulate=accumulate)
+    torch.cuda.synchronize()
+    assert cuda_lib.check_status() == 0
+    for k, (xb, yb, f, y) in enumerate(zip(xbs, ybs, fs, ys)):
+        yref, _ = O.matmul(xb, f, yb if accumulate else None)
+        U.assert_close(_host_bits(y), yref, f"contiguous batch call {k}")
