@@ -60,6 +60,25 @@ def test_prefill_odd_shapes(cuda_lib, N, M, R, ell, T, pad):
     U.assert_close(got, y, f"prefill {N}x{M} R={R} ell={ell} T={T}")
 
 
+# Shapes that select each tile layout of the GEMMs (the launch picks 256, 240, 224 or 192 activation
+# rows per tile, one or two CTAs per SM, from the shape), as (stage-1 width, stage-2 width).
+@pytest.mark.parametrize("N,M,R,ell,T", [
+    (96, 2050, 2050, 1, 2048),   # 256, 240
+    (96, 2050, 33, 1, 17),       # 240, 192
+    (96, 2050, 1030, 2, 2048),   # 256, 192
+    (96, 2050, 33, 2, 17),       # 240, 192
+    (96, 2050, 33, 3, 17),       # 240, 192
+    (257, 64, 2050, 4, 3000),    # 192, 256
+    (96, 2050, 33, 4, 17),       # 224, 192
+])
+def test_prefill_each_tile_layout(cuda_lib, N, M, R, ell, T):
+    f = G.make_factors(N, M, R, ell, 1600 + N + T)
+    xb = G.make_x(T, M, 1600 + M + T)
+    got = run(cuda_lib, f, xb, path=2, guard=2)
+    y, _ = O.matmul(xb, f)
+    U.assert_close(got, y, f"prefill layout {N}x{M} R={R} ell={ell} T={T}")
+
+
 def test_prefill_accumulate(cuda_lib):
     f = G.make_factors(256, 320, 96, 2, 1400)
     xb = G.make_x(64, 320, 1400)

@@ -57,7 +57,8 @@ def test_backward_integer_mode_bit_exact(cuda_lib):
 
 @pytest.mark.parametrize("N,M,R,ell,T", [
     (300, 200, 77, 2, 300), (512, 384, 256, 1, 513), (96, 160, 40, 4, 70), (257, 130, 33, 3, 7),
-    (160, 96, 40, 2, 1), (4096, 4096, 64, 1, 16), (1024, 2048, 768, 2, 40)])
+    (160, 96, 40, 2, 1), (4096, 4096, 64, 1, 16), (1024, 2048, 768, 2, 40), (96, 2050, 1030, 2, 2048),
+    (257, 64, 2050, 4, 3000)])
 def test_backward_matches_oracle(cuda_lib, N, M, R, ell, T):
     f = G.make_factors(N, M, R, ell, 2400 + N + T)
     xb = G.make_x(T, M, 2410 + T)
