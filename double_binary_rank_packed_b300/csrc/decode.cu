@@ -548,23 +548,17 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
             __syncthreads();
         }
 
-        // ---- 6. stage 2 per (row block, column tile); y straight from the fragment
-        for (int it = warp; it < RB2 * CT; it += kWarps) {
-            const int rb2 = it % RB2, ct = it / RB2;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- 6. stage 2 per (row block, column tile); y straight from the fragment.
+        //         Routed batches give a warp many items (a CTA covers up to 1024
+        //         rows); there a warp runs kIB of them side by side: their MMA chains are
+        //         independent, so the MMA latency is paid once per batch, not per item.
+        constexpr int kIB = 4;
+        auto epilogue_item = [&](const float (&d)[4], int rb2, int ct) {
             const int n0 = 16 * rb2 + g;
-            for (int w = 0; w < Kw2; ++w) {
-                const uint4 bv = *reinterpret_cast<const uint4 *>(vs + (8 * ct + g) * ldv + 32 * w + 8 * c);
-                const uint32_t b[4] = {bv.x, bv.y, bv.z, bv.w};
-                uint32_t pa[4], pv[4];
-                sign_pairs8(b1_s[n0 * ldb1 + w], c, pa);
-                sign_pairs8(b1_s[(n0 + 8) * ldb1 + w], c, pv);
-                mma_word8(d, pa, pv, b);
-            }
             if (ell == 3) {
                 float dd[1][4] = {{d[0], d[1], d[2], d[3]}};
                 put_frag<1>(tile_addr + 4u * static_cast<uint32_t>(16 * rb2 * ldt + 8 * ct), ldt, dd, lane, false, 0);
-                continue;
+                return;
             }
             // rows n0 (d[0], d[1]) and n0 + 8 (d[2], d[3]); columns 8ct + 2c, 8ct + 2c + 1
 #pragma unroll
@@ -603,6 +597,57 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
                     }
                 }
             }
+        };
+        // few items per warp (the single-adapter shapes): one at a time, as a batch
+        // only adds work there
+        const bool batched = SEG && RB2 * CT >= 8 * kWarps;
+        if (!batched) {
+            for (int it = warp; it < RB2 * CT; it += kWarps) {
+                const int rb2 = it % RB2, ct = it / RB2;
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                const int n0 = 16 * rb2 + g;
+                for (int w = 0; w < Kw2; ++w) {
+                    const uint4 bv = *reinterpret_cast<const uint4 *>(vs + (8 * ct + g) * ldv + 32 * w + 8 * c);
+                    const uint32_t bb[4] = {bv.x, bv.y, bv.z, bv.w};
+                    uint32_t pa[4], pv[4];
+                    sign_pairs8(b1_s[n0 * ldb1 + w], c, pa);
+                    sign_pairs8(b1_s[(n0 + 8) * ldb1 + w], c, pv);
+                    mma_word8(d, pa, pv, bb);
+                }
+                epilogue_item(d, rb2, ct);
+            }
+        }
+        if constexpr (SEG) {
+        for (int it0 = warp; batched && it0 < RB2 * CT; it0 += kWarps * kIB) {
+            float d[kIB][4];
+            int rbv[kIB], ctv[kIB];
+#pragma unroll
+            for (int b = 0; b < kIB; ++b) {
+                const int it = it0 + b * kWarps;  // warp-uniform
+                rbv[b] = it % RB2;
+                ctv[b] = it / RB2;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) d[b][j] = 0.f;
+            }
+            for (int w = 0; w < Kw2; ++w) {
+#pragma unroll
+                for (int b = 0; b < kIB; ++b) {
+                    if (it0 + b * kWarps >= RB2 * CT) break;
+                    const int n0 = 16 * rbv[b] + g;
+                    const uint4 bv = *reinterpret_cast<const uint4 *>(vs + (8 * ctv[b] + g) * ldv + 32 * w + 8 * c);
+                    const uint32_t bb[4] = {bv.x, bv.y, bv.z, bv.w};
+                    uint32_t pa[4], pv[4];
+                    sign_pairs8(b1_s[n0 * ldb1 + w], c, pa);
+                    sign_pairs8(b1_s[(n0 + 8) * ldb1 + w], c, pv);
+                    mma_word8(d[b], pa, pv, bb);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kIB; ++b) {
+                if (it0 + b * kWarps >= RB2 * CT) break;
+                epilogue_item(d[b], rbv[b], ctv[b]);
+            }
+        }
         }
         if (ell == 3) {
             __syncthreads();
