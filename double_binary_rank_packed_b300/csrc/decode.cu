@@ -550,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
 
         // ---- 6. stage 2 per (row block, column tile); y straight from the fragment.
         //         Routed batches give a warp many items (a CTA covers up to 1024
-        //         rows); there a warp runs kIB of them side by side: their MMA chains are
-        //         independent, so the MMA latency is paid once per batch, not per item.
+        //         rows); there a warp runs kIB of them side by side, so their
+        //         independent chains of loads, MMAs and epilogue overlap.
         constexpr int kIB = 4;
         auto epilogue_item = [&](const float (&d)[4], int rb2, int ct) {
             const int n0 = 16 * rb2 + g;
