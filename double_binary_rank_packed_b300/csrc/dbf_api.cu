@@ -778,11 +778,11 @@ int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *co
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p->in, p->fork, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p->cmp, p->fork, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p->out, p->fork, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "hostio pipeline fork");
+    if (e != cudaSuccess) rc = cuda_fail(e, "hostio pipeline fork");  // still joined below
     char *ws = static_cast<char *>(workspace);
     const size_t chunk_cap = size_t(std::min(L, kPipeChunk));
     int l0 = 0;
-    for (int c = 0; l0 < L; ++c) {
+    for (int c = 0; l0 < L && rc == DBF_OK; ++c) {
         // the chunk: calls l0 .. l1-1 whose host x (and y) follow one another in memory, with
         // byte sizes that keep every device copy 16-byte aligned
         auto xbytes = [&](int l) { return size_t(T) * fs[l].M * 2; };
@@ -812,37 +812,52 @@ int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *co
         char *yd = base + align_up(chunk_cap * b.x);
         char *inner = yd + align_up(chunk_cap * b.y);
         // copy-in: the slot is free once its previous read-back has finished
-        if (c >= kPipeSlots && (e = cudaStreamWaitEvent(p->in, p->d2h[k], 0)) != cudaSuccess)
-            return cuda_fail(e, "hostio pipeline: wait for a free slot");
-        if ((e = cudaMemcpyAsync(xd, x_host[l0], xs, cudaMemcpyHostToDevice, p->in)) != cudaSuccess)
-            return cuda_fail(e, "hostio pipeline: copy x in");
-        if (accumulate && (e = cudaMemcpyAsync(yd, y_host[l0], ys, cudaMemcpyHostToDevice, p->in)) != cudaSuccess)
-            return cuda_fail(e, "hostio pipeline: copy y in");
+        if (c >= kPipeSlots && (e = cudaStreamWaitEvent(p->in, p->d2h[k], 0)) != cudaSuccess) {
+            rc = cuda_fail(e, "hostio pipeline: wait for a free slot");
+            break;
+        }
+        if ((e = cudaMemcpyAsync(xd, x_host[l0], xs, cudaMemcpyHostToDevice, p->in)) != cudaSuccess) {
+            rc = cuda_fail(e, "hostio pipeline: copy x in");
+            break;
+        }
+        if (accumulate && (e = cudaMemcpyAsync(yd, y_host[l0], ys, cudaMemcpyHostToDevice, p->in)) != cudaSuccess) {
+            rc = cuda_fail(e, "hostio pipeline: copy y in");
+            break;
+        }
         if ((e = cudaEventRecord(p->h2d[k], p->in)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(p->cmp, p->h2d[k], 0)) != cudaSuccess)
-            return cuda_fail(e, "hostio pipeline: hand the slot to the compute stream");
+            (e = cudaStreamWaitEvent(p->cmp, p->h2d[k], 0)) != cudaSuccess) {
+            rc = cuda_fail(e, "hostio pipeline: hand the slot to the compute stream");
+            break;
+        }
         size_t xo = 0, yo = 0;
-        for (int l = l0; l < l1; ++l) {
+        for (int l = l0; l < l1 && rc == DBF_OK; ++l) {
             rc = dbf_matmul(&fs[l], reinterpret_cast<const uint16_t *>(xd + xo), T,
                             reinterpret_cast<uint16_t *>(yd + yo), accumulate, inner, b.inner, p->cmp);
-            if (rc) return rc;
             xo += xbytes(l);
             yo += ybytes(l);
         }
+        if (rc) break;
         e = cudaEventRecord(p->done[k], p->cmp);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(p->out, p->done[k], 0);
         if (e == cudaSuccess) e = cudaMemcpyAsync(y_host[l0], yd, ys, cudaMemcpyDeviceToHost, p->out);
         if (e == cudaSuccess) e = cudaEventRecord(p->d2h[k], p->out);
-        if (e != cudaSuccess) return cuda_fail(e, "hostio pipeline read-back");
+        if (e != cudaSuccess) {
+            rc = cuda_fail(e, "hostio pipeline read-back");
+            break;
+        }
         l0 = l1;
     }
-    // join: the caller's stream continues after all three pipeline streams
+    // join, also after an error: the caller's stream continues after all three pipeline streams
+    // (work already queued there stays ordered before the caller's next work, and a CUDA graph
+    // capture never sees a fork without its join)
     cudaStream_t ss[3] = {p->in, p->cmp, p->out};
-    for (int j = 0; j < 3 && e == cudaSuccess; ++j) {
-        e = cudaEventRecord(p->join[j], ss[j]);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(user, p->join[j], 0);
+    cudaError_t ej = cudaSuccess;
+    for (int j = 0; j < 3 && ej == cudaSuccess; ++j) {
+        ej = cudaEventRecord(p->join[j], ss[j]);
+        if (ej == cudaSuccess) ej = cudaStreamWaitEvent(user, p->join[j], 0);
     }
-    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "hostio pipeline join");
+    if (rc) return rc;
+    return ej == cudaSuccess ? DBF_OK : cuda_fail(ej, "hostio pipeline join");
 }
 
 size_t dbf_segmented_workspace_bytes(int32_t N, int32_t M, int32_t R, int32_t ell, int64_t T, int32_t S) {
