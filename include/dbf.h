@@ -204,9 +204,13 @@ int dbf_grouped_launch_count(const dbf_factors *fs, int32_t G, int64_t T);
  *   x_host, y_host  host arrays of L host pointers, bf16 [T][fs[l].M] and
  *                   [T][fs[l].N]; page-locked memory for the copies to overlap
  *   workspace       device, >= dbf_hostio_batch_workspace_bytes(fs, L, T)
- * L = 0 or T = 0 is a no-op.  Host-thread safe (an internal lock); the
+ * Consecutive calls whose host buffers follow one another inside one
+ * page-locked allocation (e.g. one [L][T][M] buffer sliced per call) share
+ * one copy each way, up to 16 calls per copy; other calls are copied one by
+ * one.  L = 0 or T = 0 is a no-op.  Host-thread safe (an internal lock); the
  * pipeline streams are shared per device, so concurrent batches serialise.
- * Errors as dbf_matmul.
+ * Errors as dbf_matmul; after an error the pipeline is still joined back
+ * into `stream`, and calls of the batch may or may not have run.
  */
 int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *const *x_host,
                             uint16_t *const *y_host, int64_t T, int accumulate,
