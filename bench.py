@@ -403,6 +403,62 @@ class BackwardWorkload:
         return self.L * self.T
 
 
+# The 1.5 bits/weight layer of the DBF page (k(N+M)/(NM) = 1.5 at N = M = 4096).
+FACT_SHAPE = (4096, 4096, 3072)
+FACT_SCHED = {"inner": 10, "power_iters": 8, "rho_rel": 1.0}
+FP32_LANES_PER_SM = 128
+MAX_SM_MHZ = 2032
+
+
+def factorize_step_flops(n, p, k, inner):
+    """Algorithmic FLOPs of one ADMM step fitting an [n x k] factor to T [n x p]: F F^T, T F^T,
+    the inverse of F F^T + rho I (k^3: Cholesky, triangular inverse, product), and per
+    iteration the P-update (RHS times the inverse)."""
+    return 2 * k * k * p + 2 * n * k * p + k ** 3 + inner * 2 * n * k * k
+
+
+class FactorizeWorkload:
+    """One alternating round (A-step, then B-step) of the double binary factorization of a dense
+    4096 x 4096 weight at k = 3072: 10 ADMM iterations per step, 8 power iterations per SVID.
+    Run eagerly (about 1100 launches per round, each longer than its launch)."""
+
+    def __init__(self, dbf, key):
+        import numpy as np
+        import torch
+        N, M, k = FACT_SHAPE
+        self.dbf, self.key, self.N, self.M, self.k = dbf, key, N, M, k
+        self.W = torch.from_numpy(G.make_dense_weight(N, M, 4096)).cuda()
+        self.f = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in G.make_factorize_start(N, M, k, 4096)]
+        self.ws = dbf.new_workspace(dbf.factorize_workspace_bytes(N, M, k), "cuda")
+        self.calls = 1
+        self.T = 0
+        self.tokens_per_step = 0
+        self.launches_per_call = dbf.factorize_launch_count(N, M, k, 1, **FACT_SCHED)
+        inner = FACT_SCHED["inner"]
+        self.flops_per_call = factorize_step_flops(N, M, k, inner) + factorize_step_flops(M, N, k, inner)
+        self.bytes_per_call = 0
+        self.bound = "alu"
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        self.alu_peak_tflops = sms * FP32_LANES_PER_SM * 2 * MAX_SM_MHZ * 1e6 / 1e12
+        self.alu_peak_source = f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x {MAX_SM_MHZ} MHz"
+
+    def capture(self):
+        self.dbf.factorize(self.W, *self.f, outer=1, workspace=self.ws, **FACT_SCHED)
+
+    def step(self):
+        self.dbf.factorize(self.W, *self.f, outer=1, workspace=self.ws, **FACT_SCHED)
+
+    def footprint_per_step(self):
+        return self.ws.numel() + 4 * self.N * self.M
+
+    def line(self, ms_step, steps):
+        r = roofline_obj(self, ms_step, None, measured_traffic(self.key))
+        r["peak_source"] = self.alu_peak_source
+        return {"workload": self.key, "value": round(1e3 / ms_step, 3), "unit": "rounds/s",
+                "ms_per_step": round(ms_step, 3), "us_per_call": round(ms_step * 1e3, 1), "calls_per_step": 1,
+                "tflop_per_round": round(self.flops_per_call / 1e12, 4), "roofline": r}
+
+
 QKV_SHAPES = ((4096, 4096, 3072), (1024, 4096, 1536), (1024, 4096, 2048))
 
 
@@ -558,6 +614,10 @@ def roofline_obj(wl, ms_per_call, peaks, traffic):
         achieved = wl.bytes_per_call / (ms_per_call * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
+    elif wl.bound == "alu":
+        achieved = wl.flops_per_call / (ms_per_call * 1e-3) / 1e12
+        peak = round(wl.alu_peak_tflops, 2)
+        unit = "TFLOP/s"
     else:
         achieved = wl.flops_per_call / (ms_per_call * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
@@ -692,6 +752,8 @@ def workload_line(wl, ms_step, steps, peaks, extra=None):
 def make_workload(dbf, key, max_calls=None):
     """Workload by key: adapter4k_T{1,4,16}, dbf1p5_T{1,8}, tiny_T{1,8}, multiadapter_T256, dbfmlp_T2048,
     adapter4k_dx_T16, dbfmlp_dx_T2048, dbfmlp_bwd_T2048, dbfqkv_T8 (grouped), dbfqkv_sep_T8."""
+    if key == "dbffact1p5":
+        return FactorizeWorkload(dbf, key)
     cap = {} if max_calls is None else {"max_calls": max_calls}
     name, _, tok = key.rpartition("_T")
     T = int(tok)
@@ -732,11 +794,14 @@ WORKLOAD_TITLES = {
     "dbfqkv": "dbfqkv: q 4096x4096 R=3072, k and v 1024x4096 R=1536 / 2048 (non-uniform R), ell=1, one grouped "
               "call per token batch, T={T} decode tokens",
     "dbfqkv_sep": "dbfqkv_sep: the same q, k, v projections as three separate calls, T={T} decode tokens",
+    "dbffact1p5": "dbffact1p5: double binary factorization of a dense 4096x4096 fp32 weight at k=3072 "
+                  "(1.5 bits/weight), one alternating round (A-step + B-step, 10 ADMM iterations each, "
+                  "8 power iterations per SVID)",
 }
 
 SECONDARY = ["adapter4k_T1", "adapter4k_T4", "dbf1p5_T1", "dbf1p5_T8", "tiny_T8", "multiadapter_T256",
              "dbfmlp_T2048", "adapter4k_dx_T16", "dbfmlp_dx_T2048", "dbfmlp_bwd_T2048", "dbfqkv_T8",
-             "dbfqkv_sep_T8"]
+             "dbfqkv_sep_T8", "dbffact1p5"]
 
 
 def main(argv=None):
@@ -811,6 +876,16 @@ def main(argv=None):
             wl = make_workload(dbf, key)
             wl.capture()
             s2 = ClockSampler(local)
+            if isinstance(wl, FactorizeWorkload):
+                fsteps = max(3, min(args.steps, 5))
+                ms_w = time_steps(wl, fsteps, 3, None, s2)
+                d = wl.line(ms_w / fsteps, fsteps)
+                d["gpu_launches"] = fsteps * wl.launches_per_call
+                d["clocks"] = s2.summary()
+                also.append(d)
+                del wl
+                torch.cuda.empty_cache()
+                continue
             ms_w = time_steps(wl, args.steps, args.warmup, None, s2)
             d = workload_line(wl, ms_w / args.steps, args.steps, peaks)
             d["clocks"] = s2.summary()

@@ -437,6 +437,7 @@ const char *dbf_status_string(int code) {
         case DBF_ERR_CUDA: return "CUDA error";
         case DBF_ERR_TIMEOUT: return "device wait timed out";
         case DBF_ERR_DEVICE_ARG: return "device-side argument out of range";
+        case DBF_ERR_NUMERIC: return "non-positive pivot in the factorization's Cholesky step";
         default: return "unknown status";
     }
 }
@@ -932,6 +933,46 @@ int dbf_launch_count(const dbf_factors *f, int64_t T, int path) {
 int dbf_segmented_launch_count(int32_t N, int32_t M, int32_t R, int32_t ell, int64_t T, int32_t S) {
     if (check_dims(N, M, R, ell) != DBF_OK || T <= 0 || S <= 0) return 0;
     return fused_plan_for(N, M, R, ell, segment_tokens(T, S), S, false).CT != 0 ? 1 : 2;
+}
+
+static int check_factorize_args(int64_t N, int64_t M, int64_t k, const dbf_factorize_params *p) {
+    if (!p || N < 1 || M < 1 || k < 1) return DBF_ERR_INVALID_ARG;
+    if (p->outer < 0 || p->inner < 0 || p->power_iters < 0 || !(p->rho_rel > 0.f)) return DBF_ERR_INVALID_ARG;
+    if (N > 65535 || M > 65535 || k > 16384) return DBF_ERR_UNSUPPORTED;
+    return DBF_OK;
+}
+
+size_t dbf_factorize_workspace_bytes(int64_t N, int64_t M, int64_t k) {
+    if (N < 1 || M < 1 || k < 1 || N > 65535 || M > 65535 || k > 16384) return 0;
+    return dbfk::factorize_workspace_bytes(N, M, k);
+}
+
+int dbf_factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_params *p) {
+    if (check_factorize_args(N, M, k, p) != DBF_OK) return -1;
+    return dbfk::factorize_launch_count(N, M, k, *p);
+}
+
+int dbf_factorize(const float *W, int64_t N, int64_t M, int64_t k, const dbf_factorize_params *p, float *a,
+                  int8_t *A, float *m_left, float *m_right, int8_t *B, float *b, void *workspace, size_t ws_bytes,
+                  void *stream) {
+    int rc = check_factorize_args(N, M, k, p);
+    if (rc) return rc;
+    if (!W || !a || !A || !m_left || !m_right || !B || !b) return DBF_ERR_INVALID_ARG;
+    const size_t need = dbfk::factorize_workspace_bytes(N, M, k);
+    if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
+    const uintptr_t f4 = reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(a) |
+                         reinterpret_cast<uintptr_t>(m_left) | reinterpret_cast<uintptr_t>(m_right) |
+                         reinterpret_cast<uintptr_t>(b);
+    if (f4 & 3) return DBF_ERR_ALIGNMENT;
+    int *st = status_ptr();
+    if (!st) return cuda_fail(cudaGetLastError(), "status word");
+    cudaError_t e = dbfk::prepare_factorize(k);
+    if (e != cudaSuccess) return cuda_fail(e, "factorize: shared memory attribute");
+    if (p->outer == 0 || p->inner == 0) return DBF_OK;
+    e = dbfk::launch_factorize(W, int(N), int(M), int(k), *p, a, A, m_left, m_right, B, b, workspace, st,
+                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "factorize");
 }
 
 int dbf_check_status(void *stream) {

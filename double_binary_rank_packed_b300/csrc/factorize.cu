@@ -1,0 +1,475 @@
+// Double binary factorization of a dense matrix on the GPU.
+//
+// "Addition is almost all you need: Compressing large language models with
+// double binary factorization", section 2: W [N x M] ~ (a . A . m^T)(B . b^T)
+// with sign matrices A [N x k], B [k x M].  The factors are found by
+// alternating minimisation (Algoritmo de Optimización): with one factor
+// fixed, the other solves min 1/2 ||T - P F||^2 over P of the form
+// diag(r) S diag(c) by ADMM whose projection is SVID (the sign of the matrix
+// times a rank-1 approximation of its magnitude).  Written out:
+//
+//   P-update  P = (T F^T + rho (Z - U)) (F F^T + rho I)^-1
+//   Z-update  Z = SVID(P + U)       (power iteration from the all-ones direction)
+//   U-update  U = U + P - Z
+//
+// starting from Z = the factor being replaced and U = 0; rho is rho_rel times
+// the mean diagonal of F F^T (rho_rel when F is zero).  The A-step has T = W
+// and F = Q = diag(mR) B diag(b); the B-step is the same step on W^T with
+// F = P^T, whose result is Q^T = diag(b) B^T diag(mR).
+//
+// Everything is fp32.  The contractions (F F^T, T F^T, the inverse, the
+// P-update) run on a shared-memory-tiled SIMT GEMM: this is an optimiser
+// step that needs fp32 products, not a reduced-precision tensor-core one.
+// (F F^T + rho I)^-1 is formed once per step (blocked Cholesky, triangular
+// inverse, then L^-T L^-1 as an NT product, which makes it exactly
+// symmetric), so each ADMM iteration is one GEMM plus memory-bound passes.
+// All reductions have a fixed order: results do not vary between runs.
+#include <float.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dbfk {
+
+namespace {
+
+constexpr int kGemmBM = 128, kGemmBN = 128, kGemmBK = 8;
+constexpr int kCholNB = 32;
+constexpr int kColsThreads = 256;
+constexpr int kMaxColChunks = 128;
+
+// C = alpha * A B^T + beta * C; A [m x kk] (lda), B [n x kk] (ldb), C [m x n]
+// (ldc), all row-major fp32.  C is not read when beta == 0.  A 128 x 128 tile
+// per CTA, 8 x 8 outputs per thread, k-steps of 8 staged transposed in shared
+// memory; out-of-range rows and k are zero-filled.
+__global__ void __launch_bounds__(256) fz_gemm_nt_kernel(int m, int n, int kk, float alpha,
+                                                         const float *__restrict__ A, int64_t lda,
+                                                         const float *__restrict__ B, int64_t ldb, float beta,
+                                                         float *C, int64_t ldc) {
+    __shared__ __align__(16) float As[kGemmBK][kGemmBM];
+    __shared__ __align__(16) float Bs[kGemmBK][kGemmBN];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int row0 = blockIdx.y * kGemmBM, col0 = blockIdx.x * kGemmBN;
+    const int lr = tid >> 1, lt = (tid & 1) * 4;  // loader: row lr, k offsets lt..lt+3
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    const int ga = row0 + lr, gb = col0 + lr;
+    for (int t0 = 0; t0 < kk; t0 += kGemmBK) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int gt = t0 + lt + q;
+            As[lt + q][lr] = (ga < m && gt < kk) ? A[int64_t(ga) * lda + gt] : 0.f;
+            Bs[lt + q][lr] = (gb < n && gt < kk) ? B[int64_t(gb) * ldb + gt] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < kGemmBK; ++t) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[t][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[t][64 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[t][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[t][64 + tx * 4]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int gr = row0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
+        if (gr >= m) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int gc = col0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
+            if (gc >= n) continue;
+            float *c = C + int64_t(gr) * ldc + gc;
+            const float v = alpha * acc[i][j];
+            *c = (beta != 0.f) ? fmaf(beta, *c, v) : v;
+        }
+    }
+}
+
+// out[c][r] = in[r][c] through a 32 x 32 shared tile (block 32 x 8).
+template <typename Tv>
+__global__ void fz_transpose_kernel(const Tv *__restrict__ in, int rows, int cols, Tv *__restrict__ out) {
+    __shared__ Tv tile[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int dy = threadIdx.y; dy < 32; dy += 8) {
+        const int r = r0 + dy, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[dy][threadIdx.x] = in[int64_t(r) * cols + c];
+    }
+    __syncthreads();
+    for (int dy = threadIdx.y; dy < 32; dy += 8) {
+        const int c = c0 + dy, r = r0 + threadIdx.x;
+        if (c < cols && r < rows) out[int64_t(c) * rows + r] = tile[threadIdx.x][dy];
+    }
+}
+
+// F[j][i] = c[j] * S[i][j] * r[i] for j < k, i < p: the fixed factor in the
+// orientation the GEMMs read (S is [p x k] int8).  32 x 32 tiles.
+__global__ void fz_build_f_kernel(const float *__restrict__ r, const int8_t *__restrict__ S,
+                                  const float *__restrict__ c, int p, int k, float *__restrict__ F) {
+    __shared__ float tile[32][33];
+    const int j0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
+    for (int di = threadIdx.y; di < 32; di += 8) {
+        const int i = i0 + di, j = j0 + threadIdx.x;
+        if (i < p && j < k) tile[di][threadIdx.x] = float(S[int64_t(i) * k + j]) * r[i];
+    }
+    __syncthreads();
+    for (int dj = threadIdx.y; dj < 32; dj += 8) {
+        const int j = j0 + dj, i = i0 + threadIdx.x;
+        if (j < k && i < p) F[int64_t(j) * p + i] = c[j] * tile[threadIdx.x][dj];
+    }
+}
+
+// Fixed-order sum over a 1024-thread block (tree in shared memory).
+__device__ float block_sum_1024(float v, float *red) {
+    const int tid = threadIdx.x;
+    red[tid] = v;
+    __syncthreads();
+    for (int s = 512; s > 0; s >>= 1) {
+        if (tid < s) red[tid] += red[tid + s];
+        __syncthreads();
+    }
+    const float total = red[0];
+    __syncthreads();
+    return total;
+}
+
+// rho = rho_rel * mean(diag G) (rho_rel when that is 0), then G += rho I;
+// rho is left in *rho_out for the later passes.  One 1024-thread block.
+__global__ void __launch_bounds__(1024) fz_ridge_kernel(float *G, int k, float rho_rel, float *rho_out) {
+    __shared__ float red[1024];
+    float s = 0.f;
+    for (int j = threadIdx.x; j < k; j += 1024) s += G[int64_t(j) * k + j];
+    const float mean = block_sum_1024(s, red) / float(k);
+    const float rho = mean > 0.f ? rho_rel * mean : rho_rel;
+    for (int j = threadIdx.x; j < k; j += 1024) G[int64_t(j) * k + j] += rho;
+    if (threadIdx.x == 0) *rho_out = rho;
+}
+
+// Cholesky of the nb x nb diagonal block at (j0, j0) in place (one warp, lane
+// = row); the strict upper triangle of the block is zeroed.  A pivot that is
+// not positive records DBF_ERR_NUMERIC and continues with FLT_MIN.
+__global__ void fz_chol_diag_kernel(float *G, int k, int j0, int nb, int *status) {
+    __shared__ float L[kCholNB][kCholNB + 1];
+    const int lane = threadIdx.x;
+    if (lane < nb)
+        for (int c = 0; c < nb; ++c) L[lane][c] = G[int64_t(j0 + lane) * k + j0 + c];
+    __syncwarp();
+    for (int c = 0; c < nb; ++c) {
+        if (lane == c) {
+            float d = L[c][c];
+            if (!(d > 0.f)) {
+                record_status(status, DBF_ERR_NUMERIC);
+                d = FLT_MIN;
+            }
+            L[c][c] = sqrtf(d);
+        }
+        __syncwarp();
+        if (lane > c && lane < nb) L[lane][c] = L[lane][c] / L[c][c];
+        __syncwarp();
+        if (lane > c && lane < nb)
+            for (int cc = c + 1; cc <= lane; ++cc) L[lane][cc] -= L[lane][c] * L[cc][c];
+        __syncwarp();
+    }
+    if (lane < nb)
+        for (int c = 0; c < nb; ++c) G[int64_t(j0 + lane) * k + j0 + c] = (c <= lane) ? L[lane][c] : 0.f;
+}
+
+// Panel below the diagonal block: row r >= j0 + nb solves x L_jj^T = G[r, j0:j0+nb]
+// by forward substitution (one thread per row).
+__global__ void __launch_bounds__(128) fz_chol_panel_kernel(float *G, int k, int j0, int nb) {
+    __shared__ float L[kCholNB][kCholNB + 1];
+    for (int e = threadIdx.x; e < nb * nb; e += blockDim.x) {
+        const int a = e / nb, b = e - a * nb;
+        L[a][b] = G[int64_t(j0 + a) * k + j0 + b];
+    }
+    __syncthreads();
+    const int r = j0 + nb + blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= k) return;
+    float *row = G + int64_t(r) * k + j0;
+    float x[kCholNB];
+#pragma unroll
+    for (int c = 0; c < kCholNB; ++c) {
+        if (c < nb) {
+            float s = row[c];
+#pragma unroll
+            for (int t = 0; t < c; ++t) s -= x[t] * L[c][t];
+            x[c] = s / L[c][c];
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < kCholNB; ++c)
+        if (c < nb) row[c] = x[c];
+}
+
+// Row r of L^-T (= column r of L^-1): solve L x = e_r by forward substitution,
+// one warp per row, x staged in dynamic shared memory (k floats).
+__global__ void fz_tri_inv_rows_kernel(const float *__restrict__ L, int k, float *__restrict__ LinvT) {
+    extern __shared__ float xs[];
+    const int r = blockIdx.x, lane = threadIdx.x;
+    float *out = LinvT + int64_t(r) * k;
+    for (int c = lane; c < r; c += 32) out[c] = 0.f;
+    if (lane == 0) xs[r] = 1.f / L[int64_t(r) * k + r];
+    __syncwarp();
+    for (int c = r + 1; c < k; ++c) {
+        const float *lc = L + int64_t(c) * k;
+        float s = 0.f;
+        for (int t = r + lane; t < c; t += 32) s += lc[t] * xs[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) xs[c] = -s / lc[c];
+        __syncwarp();
+    }
+    for (int c = r + lane; c < k; c += 32) out[c] = xs[c];
+}
+
+// out[i] = sum_j |Y[i][j]| * v[j] (v == null: the constant vconst), one warp
+// per row; with S_out set, also S_out[i][j] = sign(Y[i][j]) (sign(0) = +1).
+__global__ void __launch_bounds__(256) fz_rows_absdot_kernel(const float *__restrict__ Y, int n, int k,
+                                                             const float *__restrict__ v, float vconst,
+                                                             float *__restrict__ out, int8_t *__restrict__ S_out) {
+    const int warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (warp >= n) return;
+    const float *y = Y + int64_t(warp) * k;
+    float s = 0.f;
+    for (int j = lane; j < k; j += 32) {
+        const float yv = y[j];
+        s += fabsf(yv) * (v ? v[j] : vconst);
+        if (S_out) S_out[int64_t(warp) * k + j] = yv >= 0.f ? int8_t(1) : int8_t(-1);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) out[warp] = s;
+}
+
+// part[ch][j] = sum over rows i of chunk ch of |Y[i][j]| * u[i]; one thread per column.
+__global__ void __launch_bounds__(kColsThreads) fz_cols_partial_kernel(const float *__restrict__ Y, int n, int k,
+                                                                       const float *__restrict__ u, int rows_per_chunk,
+                                                                       float *__restrict__ part) {
+    const int j = blockIdx.x * kColsThreads + threadIdx.x;
+    if (j >= k) return;
+    const int i0 = blockIdx.y * rows_per_chunk, i1 = min(n, i0 + rows_per_chunk);
+    float s = 0.f;
+    for (int i = i0; i < i1; ++i) s += fabsf(Y[int64_t(i) * k + j]) * u[i];
+    part[int64_t(blockIdx.y) * k + j] = s;
+}
+
+// v[j] = sum_ch part[ch][j], then v /= ||v|| when ||v|| > 0.  One block.
+__global__ void __launch_bounds__(1024) fz_cols_final_kernel(const float *__restrict__ part, int chunks, int k,
+                                                             float *__restrict__ v) {
+    __shared__ float red[1024];
+    float ss = 0.f;
+    for (int j = threadIdx.x; j < k; j += 1024) {
+        float s = 0.f;
+        for (int ch = 0; ch < chunks; ++ch) s += part[int64_t(ch) * k + j];
+        v[j] = s;
+        ss += s * s;
+    }
+    const float nrm = sqrtf(block_sum_1024(ss, red));
+    if (nrm > 0.f)
+        for (int j = threadIdx.x; j < k; j += 1024) v[j] = v[j] / nrm;
+}
+
+__global__ void fz_fill_kernel(float *v, int k, float value) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j < k) v[j] = value;
+}
+
+// The dual and right-hand-side pass.  z = s * r[i] * c[j] with s the sign of
+// the warm-start factor (init) or of Y = P + U held in UY (otherwise).
+//   init:  UY = 0,        RHS = Cw + rho z
+//   else:  UY = Y - z,    RHS = Cw + rho (z - UY)
+// Grid: x over column blocks of 256, y over rows.
+__global__ void __launch_bounds__(256) fz_dual_rhs_kernel(const float *__restrict__ Cw, float *UY,
+                                                          float *__restrict__ RHS, const int8_t *__restrict__ S0,
+                                                          const float *__restrict__ r, const float *__restrict__ c,
+                                                          const float *__restrict__ rho_p, int k, int init) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= k) return;
+    const int i = blockIdx.y;
+    const int64_t e = int64_t(i) * k + j;
+    const float rho = *rho_p;
+    const float rc = r[i] * c[j];
+    if (init) {
+        const float z = float(S0[e]) * rc;
+        UY[e] = 0.f;
+        RHS[e] = fmaf(rho, z, Cw[e]);
+    } else {
+        const float y = UY[e];
+        const float z = y >= 0.f ? rc : -rc;
+        const float un = y - z;
+        UY[e] = un;
+        RHS[e] = fmaf(rho, z - un, Cw[e]);
+    }
+}
+
+inline unsigned cdiv(int64_t a, int64_t b) { return unsigned((a + b - 1) / b); }
+inline size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
+
+cudaError_t gemm_nt(int m, int n, int kk, float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                    float beta, float *C, int64_t ldc, cudaStream_t s) {
+    if (m <= 0 || n <= 0) return cudaSuccess;
+    fz_gemm_nt_kernel<<<dim3(cdiv(n, kGemmBN), cdiv(m, kGemmBM)), 256, 0, s>>>(m, n, kk, alpha, A, lda, B, ldb, beta,
+                                                                               C, ldc);
+    return cudaGetLastError();
+}
+
+// Scratch of one factorization, carved from the caller's workspace.
+struct FzScratch {
+    float *Wt, *F, *G, *LinvT, *Ginv, *Cw, *UY, *RHS, *u, *part, *rho;
+    int8_t *Bt;
+};
+
+size_t carve(void *base, int64_t N, int64_t M, int64_t k, FzScratch *s) {
+    const int64_t nmax = std::max(N, M);
+    size_t off = 0;
+    char *b = static_cast<char *>(base);
+    auto take = [&](size_t bytes) {
+        char *p = b ? b + off : nullptr;
+        off += align_up(bytes);
+        return p;
+    };
+    FzScratch t;
+    t.Wt = reinterpret_cast<float *>(take(sizeof(float) * size_t(M) * N));
+    t.F = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * nmax));
+    t.G = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * k));
+    t.LinvT = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * k));
+    t.Ginv = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * k));
+    t.Cw = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * k));
+    t.UY = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * k));
+    t.RHS = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * k));
+    t.u = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax)));
+    t.part = reinterpret_cast<float *>(take(sizeof(float) * size_t(kMaxColChunks) * k));
+    t.rho = reinterpret_cast<float *>(take(sizeof(float) * 4));
+    t.Bt = reinterpret_cast<int8_t *>(take(size_t(M) * k));
+    if (s) *s = t;
+    return off;
+}
+
+int chol_steps(int k) { return (k + kCholNB - 1) / kCholNB; }
+
+// Launches of one ADMM step (a half of an alternating round).
+int step_launches(int k, int inner, int power_iters) {
+    if (inner <= 0) return 0;
+    const int chol = 3 * chol_steps(k) - 2;  // the last block has no panel and no trailing update
+    const int svid = (power_iters > 0 ? 3 * power_iters : 1) + 1;
+    // F, F F^T, ridge; Cholesky; L^-T rows, inverse, T F^T, first dual pass;
+    // per iteration the P-update GEMM, the SVID passes and (but the last) a dual pass
+    return 3 + chol + 4 + inner * (1 + svid) + (inner - 1);
+}
+
+// SVID of Y [n x k]: c (= v) by power iteration, then r = |Y| c; S_out optional.
+cudaError_t svid(const float *Y, int n, int k, int power_iters, const FzScratch &w, float *r, float *c,
+                 int8_t *S_out, cudaStream_t s) {
+    const float v0 = float(1.0 / sqrt(double(k)));
+    const int rows_per_chunk = std::max<int>(32, int((int64_t(n) + kMaxColChunks - 1) / kMaxColChunks));
+    const int chunks = int((int64_t(n) + rows_per_chunk - 1) / rows_per_chunk);
+    const unsigned row_blocks = cdiv(n, 8);
+    if (power_iters <= 0) {
+        fz_fill_kernel<<<cdiv(k, 256), 256, 0, s>>>(c, k, v0);
+    }
+    for (int q = 0; q < power_iters; ++q) {
+        fz_rows_absdot_kernel<<<row_blocks, 256, 0, s>>>(Y, n, k, q == 0 ? nullptr : c, v0, w.u, nullptr);
+        fz_cols_partial_kernel<<<dim3(cdiv(k, kColsThreads), chunks), kColsThreads, 0, s>>>(Y, n, k, w.u,
+                                                                                           rows_per_chunk, w.part);
+        fz_cols_final_kernel<<<1, 1024, 0, s>>>(w.part, chunks, k, c);
+    }
+    fz_rows_absdot_kernel<<<row_blocks, 256, 0, s>>>(Y, n, k, c, v0, r, S_out);
+    return cudaGetLastError();
+}
+
+// One alternating step: the left factor (r, S [n x k], c) of T [n x p] ~ P F
+// with F built from the other side's factor (r2 [p], S2 [p x k], c2 [k]).
+cudaError_t admm_step(const float *T, int n, int p, int k, const float *r2, const int8_t *S2, const float *c2,
+                      float *r, int8_t *S, float *c, const dbf_factorize_params &prm, const FzScratch &w,
+                      int *status, cudaStream_t s) {
+    if (prm.inner <= 0) return cudaSuccess;
+    cudaError_t e;
+    fz_build_f_kernel<<<dim3(cdiv(k, 32), cdiv(p, 32)), dim3(32, 8), 0, s>>>(r2, S2, c2, p, k, w.F);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = gemm_nt(k, k, p, 1.f, w.F, p, w.F, p, 0.f, w.G, k, s)) != cudaSuccess) return e;
+    fz_ridge_kernel<<<1, 1024, 0, s>>>(w.G, k, prm.rho_rel, w.rho);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    for (int j0 = 0; j0 < k; j0 += kCholNB) {
+        const int nb = std::min(kCholNB, k - j0);
+        fz_chol_diag_kernel<<<1, 32, 0, s>>>(w.G, k, j0, nb, status);
+        const int j1 = j0 + nb;
+        if (j1 < k) {
+            fz_chol_panel_kernel<<<cdiv(k - j1, 128), 128, 0, s>>>(w.G, k, j0, nb);
+            if ((e = gemm_nt(k - j1, k - j1, nb, -1.f, w.G + int64_t(j1) * k + j0, k, w.G + int64_t(j1) * k + j0, k,
+                             1.f, w.G + int64_t(j1) * k + j1, k, s)) != cudaSuccess)
+                return e;
+        }
+    }
+    const size_t tri_smem = sizeof(float) * size_t(k);
+    fz_tri_inv_rows_kernel<<<k, 32, tri_smem, s>>>(w.G, k, w.LinvT);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = gemm_nt(k, k, k, 1.f, w.LinvT, k, w.LinvT, k, 0.f, w.Ginv, k, s)) != cudaSuccess) return e;
+    if ((e = gemm_nt(n, k, p, 1.f, T, p, w.F, p, 0.f, w.Cw, k, s)) != cudaSuccess) return e;
+    const dim3 ew(cdiv(k, 256), n);
+    fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS, S, r, c, w.rho, k, 1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    for (int it = 0; it < prm.inner; ++it) {
+        const bool last = it == prm.inner - 1;
+        if ((e = gemm_nt(n, k, k, 1.f, w.RHS, k, w.Ginv, k, 1.f, w.UY, k, s)) != cudaSuccess) return e;
+        if ((e = svid(w.UY, n, k, prm.power_iters, w, r, c, last ? S : nullptr, s)) != cudaSuccess) return e;
+        if (!last) {
+            fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS, nullptr, r, c, w.rho, k, 0);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t factorize_workspace_bytes(int64_t N, int64_t M, int64_t k) { return carve(nullptr, N, M, k, nullptr); }
+
+int factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_params &p) {
+    (void)N;
+    (void)M;
+    if (p.outer <= 0 || p.inner <= 0) return 0;
+    // transposes of W and B in, the rounds, the transpose of B out
+    return 2 + p.outer * 2 * step_launches(int(k), p.inner, p.power_iters) + 1;
+}
+
+size_t factorize_tri_smem(int64_t k) { return sizeof(float) * size_t(k); }
+
+cudaError_t prepare_factorize(int64_t k) {
+    const size_t smem = factorize_tri_smem(k);
+    if (smem <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(fz_tri_inv_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+}
+
+cudaError_t launch_factorize(const float *W, int N, int M, int k, const dbf_factorize_params &p, float *a,
+                             int8_t *A, float *m_left, float *m_right, int8_t *B, float *b, void *workspace,
+                             int *status, cudaStream_t s) {
+    FzScratch w;
+    carve(workspace, N, M, k, &w);
+    cudaError_t e;
+    fz_transpose_kernel<float><<<dim3(cdiv(M, 32), cdiv(N, 32)), dim3(32, 8), 0, s>>>(W, N, M, w.Wt);
+    fz_transpose_kernel<int8_t><<<dim3(cdiv(M, 32), cdiv(k, 32)), dim3(32, 8), 0, s>>>(B, k, M, w.Bt);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    for (int o = 0; o < p.outer; ++o) {
+        // A-step: W ~ P Q with Q^T = diag(b) B^T diag(mR) fixed.
+        if ((e = admm_step(W, N, M, k, b, w.Bt, m_right, a, A, m_left, p, w, status, s)) != cudaSuccess) return e;
+        // B-step: W^T ~ Q^T P^T with P = diag(a) A diag(mL) fixed.
+        if ((e = admm_step(w.Wt, M, N, k, a, A, m_left, b, w.Bt, m_right, p, w, status, s)) != cudaSuccess)
+            return e;
+    }
+    fz_transpose_kernel<int8_t><<<dim3(cdiv(k, 32), cdiv(M, 32)), dim3(32, 8), 0, s>>>(w.Bt, M, k, B);
+    return cudaGetLastError();
+}
+
+}  // namespace dbfk

@@ -27,6 +27,7 @@ DBF_ERR_WORKSPACE = -4
 DBF_ERR_CUDA = -5
 DBF_ERR_TIMEOUT = -6
 DBF_ERR_DEVICE_ARG = -7
+DBF_ERR_NUMERIC = -8
 
 PATH_AUTO = 0
 PATH_DECODE = 1
@@ -40,6 +41,7 @@ EXPORTED = (
     "dbf_launch_count", "dbf_segmented_launch_count", "dbf_transpose_packed", "dbf_factors_transposed",
     "dbf_backward", "dbf_backward_workspace_bytes", "dbf_matmul_grouped", "dbf_grouped_workspace_bytes",
     "dbf_grouped_launch_count", "dbf_matmul_hostio_batch", "dbf_hostio_batch_workspace_bytes",
+    "dbf_factorize", "dbf_factorize_workspace_bytes", "dbf_factorize_launch_count",
 )
 
 
@@ -52,6 +54,13 @@ class DbfFactors(ctypes.Structure):
         ("B1", ctypes.c_void_p), ("B2", ctypes.c_void_p),
         ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
     ]
+
+
+class DbfFactorizeParams(ctypes.Structure):
+    """Mirror of struct dbf_factorize_params (include/dbf.h)."""
+
+    _fields_ = [("outer", ctypes.c_int32), ("inner", ctypes.c_int32), ("power_iters", ctypes.c_int32),
+                ("rho_rel", ctypes.c_float)]
 
 
 class DbfError(RuntimeError):
@@ -98,6 +107,10 @@ def _load():
         "dbf_grouped_launch_count": (ci, [fp, i32, i64]),
         "dbf_matmul_hostio_batch": (ci, [fp, i32, vp, vp, i64, ci, vp, sz, vp]),
         "dbf_hostio_batch_workspace_bytes": (sz, [fp, i32, i64]),
+        "dbf_factorize": (ci, [vp, i64, i64, i64, ctypes.POINTER(DbfFactorizeParams),
+                               vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "dbf_factorize_workspace_bytes": (sz, [i64, i64, i64]),
+        "dbf_factorize_launch_count": (ci, [i64, i64, i64, ctypes.POINTER(DbfFactorizeParams)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -439,6 +452,47 @@ def matmul_segmented(table: torch.Tensor, n_adapters: int, N: int, M: int, R: in
                                    _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(rc, "dbf_matmul_segmented")
     return y
+
+
+def factorize_workspace_bytes(N: int, M: int, k: int) -> int:
+    return int(_lib.dbf_factorize_workspace_bytes(N, M, k))
+
+
+def factorize_launch_count(N: int, M: int, k: int, outer: int, inner: int, power_iters: int,
+                           rho_rel: float) -> int:
+    prm = DbfFactorizeParams(outer, inner, power_iters, rho_rel)
+    return int(_lib.dbf_factorize_launch_count(N, M, k, ctypes.byref(prm)))
+
+
+def factorize(W: torch.Tensor, a: torch.Tensor, A: torch.Tensor, m_left: torch.Tensor, m_right: torch.Tensor,
+              B: torch.Tensor, b: torch.Tensor, outer: int = 6, inner: int = 10, power_iters: int = 8,
+              rho_rel: float = 1.0, workspace: torch.Tensor | None = None, stream=None):
+    """Double binary factorization W ~ (a . A . m^T)(B . b^T), m = m_left . m_right (dbf_factorize).
+
+    W fp32 [N, M]; the left factor a fp32 [N], A int8 [N, k], m_left fp32 [k] and the
+    right factor m_right fp32 [k], B int8 [k, M], b fp32 [M] are device tensors updated
+    in place (the left factor is the start of the first step; the right one is fixed
+    in it).  Returns (a, A, m_left, m_right, B, b).
+    """
+    if W.dtype != torch.float32 or W.dim() != 2:
+        raise ValueError("W must be fp32 [N, M]")
+    N, M = W.shape
+    k = A.shape[1] if A.dim() == 2 else -1
+    want = ((a, torch.float32, (N,)), (A, torch.int8, (N, k)), (m_left, torch.float32, (k,)),
+            (m_right, torch.float32, (k,)), (B, torch.int8, (k, M)), (b, torch.float32, (M,)))
+    for t, dt, sh in want:
+        if t.dtype != dt or tuple(t.shape) != sh or not t.is_contiguous() or t.device != W.device:
+            raise ValueError("factors: a fp32 [N], A int8 [N, k], m_left fp32 [k], m_right fp32 [k], "
+                             "B int8 [k, M], b fp32 [M], contiguous, on W's device")
+    W = W.contiguous()
+    prm = DbfFactorizeParams(outer, inner, power_iters, rho_rel)
+    need = factorize_workspace_bytes(N, M, k)
+    if workspace is None:
+        workspace = new_workspace(max(need, 256), W.device)
+    rc = _lib.dbf_factorize(_ptr(W), N, M, k, ctypes.byref(prm), _ptr(a), _ptr(A), _ptr(m_left), _ptr(m_right),
+                            _ptr(B), _ptr(b), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(rc, "dbf_factorize")
+    return a, A, m_left, m_right, B, b
 
 
 def check_status(stream=None) -> int:

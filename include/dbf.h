@@ -51,7 +51,8 @@ enum {
     DBF_ERR_WORKSPACE = -4,    /* workspace null or smaller than required     */
     DBF_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed        */
     DBF_ERR_TIMEOUT = -6,      /* device: a bounded wait ran out              */
-    DBF_ERR_DEVICE_ARG = -7    /* device: segment table out of range          */
+    DBF_ERR_DEVICE_ARG = -7,   /* device: segment table out of range          */
+    DBF_ERR_NUMERIC = -8       /* device: a Cholesky pivot was not positive   */
 };
 
 /* Kernel path selection for dbf_matmul_path (dbf_matmul uses DBF_PATH_AUTO). */
@@ -334,6 +335,64 @@ int dbf_selftest_bounded_wait(int64_t limit_us, void *stream);
  */
 int dbf_matmul_decode_noalloc(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
                               int accumulate, void *stream);
+
+/* ------------------------------------------------ dense factorization */
+/*
+ * Parameters of dbf_factorize.  The pages give the steps of the optimiser,
+ * not its schedule; these are the counts and the penalty it runs with.
+ */
+typedef struct dbf_factorize_params {
+    int32_t outer;        /* alternating rounds (A-step, then B-step), >= 0 */
+    int32_t inner;        /* ADMM iterations in each step, >= 0              */
+    int32_t power_iters;  /* power iterations of each SVID rank-1 step, >= 0 */
+    float rho_rel;        /* ADMM penalty as a multiple of mean(diag(F F^T)), > 0 */
+} dbf_factorize_params;
+
+/*
+ * dbf_factorize: double binary factorization of a dense matrix,
+ *     W ~ (a . A . m^T)(B . b^T),  m = m_left . m_right,
+ * ("Addition is almost all you need: Compressing large language models
+ * with double binary factorization", section 2, Formulación Matemática and
+ * Algoritmo de Optimización).  Each round fixes one factor and fits the
+ * other by ADMM with the SVID projection:
+ *     A-step  min 1/2 ||W - P Q||^2,  P = diag(a) A diag(m_left),
+ *             Q = diag(m_right) B diag(b) fixed;
+ *     B-step  the same on W^T for Q^T = diag(b) B^T diag(m_right), P fixed;
+ *     ADMM    P = (T F^T + rho (Z - U)) (F F^T + rho I)^-1,
+ *             Z = SVID(P + U), U = U + P - Z,
+ *             rho = rho_rel * mean(diag(F F^T)) (rho_rel if F is zero),
+ *             started from Z = the factor being replaced, U = 0;
+ *     SVID(Y) = sign(Y) (sign(0) = +1) times r c^T, c from power_iters
+ *             power iterations on |Y| from the all-ones direction
+ *             (v = |Y|^T |Y| v, normalised), r = |Y| c.
+ * The result of each step is the last Z.  With m = m_left . m_right the
+ * factors are those of dbf_factors with ell = 1: alpha = a, B1 = A,
+ * beta = m, B2 = B, gamma = b (pack A and B with dbf_pack, scales to fp16).
+ *   W        device fp32 [N][M] row-major (read only)
+ *   a, A, m_left    device fp32 [N], int8 [N][k] (+1/-1), fp32 [k]: the
+ *                   left factor; read as the start of the first A-step (a
+ *                   zero a starts it at Z = 0), overwritten with the result
+ *   m_right, B, b   device fp32 [k], int8 [k][M] (+1/-1), fp32 [M]: the
+ *                   right factor, fixed in the first A-step, overwritten
+ *   workspace  device, >= dbf_factorize_workspace_bytes(N, M, k), 256-byte
+ *              aligned, not shared with concurrent calls
+ * Computes in fp32 (SIMT GEMMs, blocked Cholesky); the reductions have a
+ * fixed order, so a rerun gives the same bits.  Limits: 1 <= N, M <= 65535,
+ * 1 <= k <= 16384, else DBF_ERR_UNSUPPORTED; null pointers or params out of
+ * range give DBF_ERR_INVALID_ARG.  Asynchronous on `stream`; a pivot that
+ * is not positive (possible only for a tiny rho_rel) is recorded as
+ * DBF_ERR_NUMERIC for dbf_check_status and the step continues.
+ * outer = 0 or inner = 0 leaves the factors as given.
+ */
+int dbf_factorize(const float *W, int64_t N, int64_t M, int64_t k, const dbf_factorize_params *params,
+                  float *a, int8_t *A, float *m_left, float *m_right, int8_t *B, float *b,
+                  void *workspace, size_t ws_bytes, void *stream);
+
+/* Device workspace (bytes) dbf_factorize needs; 0 for sizes out of range. */
+size_t dbf_factorize_workspace_bytes(int64_t N, int64_t M, int64_t k);
+
+/* Kernels one dbf_factorize call launches; -1 for arguments out of range. */
+int dbf_factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_params *params);
 
 /* Human-readable text for a DBF_* code (static string). */
 const char *dbf_status_string(int code);

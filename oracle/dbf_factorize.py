@@ -51,7 +51,7 @@ Readings where the pages are silent (each stated once here):
   * the importance weighting by activation norms and output gradients
     (same section) needs calibration data and is not part of this oracle.
 
-Pins (tests/test_oracle_pins.py): SVID is exact and idempotent on its set;
+Pins (tests/test_oracle_factorize_pins.py): SVID is exact and idempotent on its set;
 its rank-1 part converges to the leading singular pair of |Y| (library SVD);
 the P-update equals the ridge least-squares solution of a stacked system
 (library least squares); the exact factors of an exactly representable W
@@ -112,11 +112,14 @@ def p_update(t: np.ndarray, f: np.ndarray, z: np.ndarray, u: np.ndarray, rho: fl
     return np.linalg.solve(g, rhs.T).T
 
 
-def admm_left(t, f, r0, s0, c0, inner: int, power_iters: int, rho_rel: float, _dual_sign: float = 1.0):
+def admm_left(t, f, r0, s0, c0, inner: int, power_iters: int, rho_rel: float, _dual_sign: float = 1.0,
+              return_y: bool = False):
     """One alternating step: ADMM for min_P 1/2||T - P F||^2, P in the SVID set.
 
     t [n x p] target, f [k x p] fixed factor, (r0, s0, c0) the current left
-    factor (warm start).  Returns the new left factor (r, S, c).
+    factor (warm start).  Returns the new left factor (r, S, c), and with
+    return_y also the matrix P + U that the last SVID projected (None when
+    inner = 0): its entries near zero are where a sign is decided by rounding.
     `_dual_sign` exists only so that a test can plant a wrong dual update.
     """
     t = np.asarray(t, np.float64)
@@ -125,12 +128,14 @@ def admm_left(t, f, r0, s0, c0, inner: int, power_iters: int, rho_rel: float, _d
     r, s, c = np.asarray(r0, np.float64), np.asarray(s0, np.int8), np.asarray(c0, np.float64)
     z = svid_dense(r, s, c)
     u = np.zeros_like(z)
+    y = None
     for _ in range(inner):
         p = p_update(t, f, z, u, rho)
-        r, s, c = svid(p + u, power_iters)
+        y = p + u
+        r, s, c = svid(y, power_iters)
         z = svid_dense(r, s, c)
         u = u + _dual_sign * (p - z)
-    return r, s, c
+    return (r, s, c, y) if return_y else (r, s, c)
 
 
 def factorize(w, left, right, outer: int, inner: int, power_iters: int, rho_rel: float):

@@ -45,7 +45,7 @@ def test_struct_layout_matches_header(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         assert lib.status_string(code) != "unknown status"
     assert lib.status_string(5) == "unknown status"
 
@@ -108,3 +108,45 @@ def test_pack_and_segmented_host_checks(lib):
     assert L.dbf_matmul_segmented(None, 1, 64, 64, 32, 1, ctypes.c_void_p(FAKE), 8, ctypes.c_void_p(FAKE), None,
                                   None, 1, 0, None, 0, None) == lib.DBF_ERR_INVALID_ARG
     assert L.dbf_selftest_bounded_wait(0, None) == lib.DBF_ERR_INVALID_ARG
+
+
+def _fz_call(lib, N=64, M=48, k=16, prm=(2, 3, 4, 1.0), W=FAKE, ws=FAKE + 0x8000, ws_bytes=1 << 30, scale=FAKE):
+    p = lib.DbfFactorizeParams(*prm) if prm is not None else None
+    vp = ctypes.c_void_p
+    return lib._lib.dbf_factorize(vp(W), N, M, k, ctypes.byref(p) if p is not None else None,
+                                  vp(scale), vp(FAKE + 0x1000), vp(FAKE + 0x2000), vp(FAKE + 0x3000),
+                                  vp(FAKE + 0x4000), vp(FAKE + 0x5000), vp(ws), ws_bytes, None)
+
+
+def test_factorize_host_checks(lib):
+    assert _fz_call(lib, prm=None) == lib.DBF_ERR_INVALID_ARG
+    assert _fz_call(lib, N=0) == lib.DBF_ERR_INVALID_ARG
+    assert _fz_call(lib, k=0) == lib.DBF_ERR_INVALID_ARG
+    assert _fz_call(lib, prm=(-1, 3, 4, 1.0)) == lib.DBF_ERR_INVALID_ARG
+    assert _fz_call(lib, prm=(1, 3, 4, 0.0)) == lib.DBF_ERR_INVALID_ARG
+    assert _fz_call(lib, prm=(1, 3, 4, float("nan"))) == lib.DBF_ERR_INVALID_ARG
+    assert _fz_call(lib, N=65536) == lib.DBF_ERR_UNSUPPORTED
+    assert _fz_call(lib, k=16385) == lib.DBF_ERR_UNSUPPORTED
+    assert _fz_call(lib, W=0) == lib.DBF_ERR_INVALID_ARG
+    assert _fz_call(lib, ws_bytes=16) == lib.DBF_ERR_WORKSPACE
+    assert _fz_call(lib, ws=FAKE + 0x8010) == lib.DBF_ERR_ALIGNMENT
+    assert _fz_call(lib, scale=FAKE + 2) == lib.DBF_ERR_ALIGNMENT
+
+
+def test_factorize_sizes_and_launch_counts(lib):
+    ws = lib.factorize_workspace_bytes(4096, 4096, 1024)
+    # W^T, F, three k x k, three n x k, the sign transpose, small vectors
+    assert ws >= 4 * (4096 * 4096 + 1024 * 4096 + 3 * 1024 * 1024 + 3 * 4096 * 1024) + 4096 * 1024
+    assert ws % 256 == 0
+    assert lib.factorize_workspace_bytes(0, 4, 4) == 0
+    assert lib.factorize_workspace_bytes(4, 4, 16385) == 0
+    # per step: F, F F^T, ridge; 3 per 32-column Cholesky block less 2; L^-T, inverse,
+    # T F^T, first dual; per iteration 1 GEMM + 3q + 1 SVID passes, dual between iterations
+    k, inner, q = 70, 4, 5
+    step = 3 + (3 * 3 - 2) + 4 + inner * (1 + 3 * q + 1) + (inner - 1)
+    assert lib.factorize_launch_count(100, 80, k, 3, inner, q, 1.0) == 2 + 3 * 2 * step + 1
+    step0 = 3 + (3 * 3 - 2) + 4 + inner * (1 + 1 + 1) + (inner - 1)   # power_iters = 0: fill + rows
+    assert lib.factorize_launch_count(100, 80, k, 1, inner, 0, 1.0) == 2 + 2 * step0 + 1
+    assert lib.factorize_launch_count(100, 80, k, 0, inner, q, 1.0) == 0
+    assert lib.factorize_launch_count(100, 80, k, 1, 0, q, 1.0) == 0
+    assert lib.factorize_launch_count(100, 80, 0, 1, 1, q, 1.0) == -1

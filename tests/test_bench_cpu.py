@@ -63,5 +63,23 @@ def test_traffic_table_entries_name_existing_sources_and_go_stale_when_they_chan
 
 @pytest.mark.parametrize("key", bench.SECONDARY)
 def test_every_secondary_workload_has_a_title(key):
+    if "_T" not in key:   # not a token workload (the factorization round)
+        assert key in bench.WORKLOAD_TITLES
+        return
     name, _, tok = key.rpartition("_T")
     assert name in bench.WORKLOAD_TITLES and int(tok) > 0
+
+
+def test_factorize_flop_count():
+    # one step at N = M = 4096, k = 3072, 10 iterations: F F^T 77.3 G, T F^T 103.1 G,
+    # inverse 29.0 G, ten P-updates 773.1 G
+    f = bench.factorize_step_flops(4096, 4096, 3072, 10)
+    assert abs(f - (2 * 3072 ** 2 * 4096 + 2 * 4096 * 3072 * 4096 + 3072 ** 3 + 10 * 2 * 4096 * 3072 ** 2)) == 0
+    assert 0.98e12 < f < 0.99e12
+
+
+def test_alu_roofline():
+    class W:
+        bound, flops_per_call, alu_peak_tflops = "alu", 2e12, 77.0
+    r = bench.roofline_obj(W(), 50.0, None, None)     # 2 TFLOP in 50 ms = 40 TF/s
+    assert r["unit"] == "TFLOP/s" and abs(r["achieved"] - 40.0) < 1e-9 and abs(r["frac"] - 40 / 77) < 1e-4

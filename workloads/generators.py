@@ -17,6 +17,11 @@ Draw recipe (fixed so that every run and every machine sees the same data):
             rows of a T-row draw equal a T'-row draw
   integer x: rng = default_rng(seed + 501), uniform integers in [-4, 4]
   outlier columns: rng = default_rng(seed + 502), chosen without replacement
+  dense W:  rng = default_rng(seed + 600); W [N,M] = N(0,1) * 0.02 times a
+            per-row factor exp(N(0, 0.25)) (rows of unequal norm), float32
+  factorization start: rng = default_rng(seed + 601); B [k,M] signs; the
+            other parts are constants (a = 0, A = +1, m_left = 0,
+            m_right = 1, b = 1)
 """
 
 from __future__ import annotations
@@ -182,3 +187,22 @@ def make_routing(T: int, n_adapters: int, seed: int):
     offsets.append(T)
     return (np.asarray(offsets, dtype=np.int32),
             np.asarray(adapters, dtype=np.int32), a)
+
+
+def make_dense_weight(N: int, M: int, seed: int) -> np.ndarray:
+    """A dense float32 weight W [N, M] to factorize: N(0, 0.02^2) entries with
+    log-normal row norms (sigma 0.25), drawn from default_rng(seed + 600)."""
+    rng = np.random.default_rng(seed + 600)
+    w = rng.standard_normal((N, M)) * 0.02
+    w *= np.exp(0.25 * rng.standard_normal((N, 1)))
+    return w.astype(np.float32)
+
+
+def make_factorize_start(N: int, M: int, k: int, seed: int):
+    """Starting factors of a factorization: a zero left factor (a = 0, A = +1,
+    m_left = 0) and a right factor of random signs with unit scales.
+    Returns (a, A, m_left, m_right, B, b) as float32 / int8 numpy arrays."""
+    rng = np.random.default_rng(seed + 601)
+    B = draw_signs(rng, (k, M), "bernoulli")
+    return (np.zeros(N, np.float32), np.ones((N, k), np.int8), np.zeros(k, np.float32),
+            np.ones(k, np.float32), B, np.ones(M, np.float32))
