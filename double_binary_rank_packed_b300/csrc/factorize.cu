@@ -21,8 +21,9 @@
 // P-update) run on a shared-memory-tiled SIMT GEMM: this is an optimiser
 // step that needs fp32 products, not a reduced-precision tensor-core one.
 // (F F^T + rho I)^-1 is formed once per step (blocked Cholesky, triangular
-// inverse, then L^-T L^-1 as an NT product, which makes it exactly
-// symmetric), so each ADMM iteration is one GEMM plus memory-bound passes.
+// inverse, then the lower triangle of L^-T L^-1 as an NT product, mirrored,
+// so it is exactly symmetric and the P-update can read it in the NT layout),
+// so each ADMM iteration is one GEMM plus memory-bound passes.
 // All reductions have a fixed order: results do not vary between runs.
 #include <float.h>
 
@@ -38,42 +39,74 @@ namespace {
 constexpr int kGemmBM = 128, kGemmBN = 128, kGemmBK = 8;
 constexpr int kCholNB = 32;
 constexpr int kColsThreads = 256;
-constexpr int kMaxColChunks = 128;
+constexpr int kMaxColChunks = 32;
 
 // C = alpha * A B^T + beta * C; A [m x kk] (lda), B [n x kk] (ldb), C [m x n]
 // (ldc), all row-major fp32.  C is not read when beta == 0.  A 128 x 128 tile
-// per CTA, 8 x 8 outputs per thread, k-steps of 8 staged transposed in shared
-// memory; out-of-range rows and k are zero-filled.
-__global__ void __launch_bounds__(256) fz_gemm_nt_kernel(int m, int n, int kk, float alpha,
-                                                         const float *__restrict__ A, int64_t lda,
-                                                         const float *__restrict__ B, int64_t ldb, float beta,
-                                                         float *C, int64_t ldc) {
-    __shared__ __align__(16) float As[kGemmBK][kGemmBM];
-    __shared__ __align__(16) float Bs[kGemmBK][kGemmBN];
+// per CTA, 8 x 8 outputs per thread, k-steps of 8 staged transposed in two
+// shared-memory buffers: the next step's global loads are in flight while the
+// current one is multiplied.  Out-of-range rows and k are zero-filled.  VEC:
+// lda, ldb and kk are multiples of 4 and A, B 16-byte aligned, so each
+// thread's four k values are one float4 load.  lower: only the tiles that
+// touch the lower triangle (col <= row) are computed; the others are left as
+// they are (for products whose upper triangle nothing reads).
+template <bool VEC>
+__global__ void __launch_bounds__(256, 2) fz_gemm_nt_kernel(int m, int n, int kk, float alpha,
+                                                            const float *__restrict__ A, int64_t lda,
+                                                            const float *__restrict__ B, int64_t ldb, float beta,
+                                                            float *C, int64_t ldc, int lower) {
+    __shared__ __align__(16) float As[2][kGemmBK][kGemmBM];
+    __shared__ __align__(16) float Bs[2][kGemmBK][kGemmBN];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int row0 = blockIdx.y * kGemmBM, col0 = blockIdx.x * kGemmBN;
+    if (lower && col0 >= row0 + kGemmBM) return;  // the whole tile is above the diagonal
     const int lr = tid >> 1, lt = (tid & 1) * 4;  // loader: row lr, k offsets lt..lt+3
+    const int ga = row0 + lr, gb = col0 + lr;
+    const float *pa = A + int64_t(ga < m ? ga : 0) * lda;
+    const float *pb = B + int64_t(gb < n ? gb : 0) * ldb;
+    float ra[4], rb[4];
+    auto load = [&](int t0) {
+        const int gt = t0 + lt;
+        if constexpr (VEC) {
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 va = (ga < m && gt < kk) ? *reinterpret_cast<const float4 *>(pa + gt) : z;
+            const float4 vb = (gb < n && gt < kk) ? *reinterpret_cast<const float4 *>(pb + gt) : z;
+            ra[0] = va.x; ra[1] = va.y; ra[2] = va.z; ra[3] = va.w;
+            rb[0] = vb.x; rb[1] = vb.y; rb[2] = vb.z; rb[3] = vb.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ra[q] = (ga < m && gt + q < kk) ? pa[gt + q] : 0.f;
+                rb[q] = (gb < n && gt + q < kk) ? pb[gt + q] : 0.f;
+            }
+        }
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            As[buf][lt + q][lr] = ra[q];
+            Bs[buf][lt + q][lr] = rb[q];
+        }
+    };
     float acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-    const int ga = row0 + lr, gb = col0 + lr;
-    for (int t0 = 0; t0 < kk; t0 += kGemmBK) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int gt = t0 + lt + q;
-            As[lt + q][lr] = (ga < m && gt < kk) ? A[int64_t(ga) * lda + gt] : 0.f;
-            Bs[lt + q][lr] = (gb < n && gt < kk) ? B[int64_t(gb) * ldb + gt] : 0.f;
-        }
-        __syncthreads();
+    load(0);
+    store(0);
+    __syncthreads();
+    int buf = 0;
+    for (int t0 = 0; t0 < kk; t0 += kGemmBK, buf ^= 1) {
+        const bool more = t0 + kGemmBK < kk;
+        if (more) load(t0 + kGemmBK);
 #pragma unroll
         for (int t = 0; t < kGemmBK; ++t) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&As[t][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&As[t][64 + ty * 4]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[t][tx * 4]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[t][64 + tx * 4]);
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][t][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][t][64 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][t][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][t][64 + tx * 4]);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -81,6 +114,7 @@ __global__ void __launch_bounds__(256) fz_gemm_nt_kernel(int m, int n, int kk, f
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
+        if (more) store(buf ^ 1);  // that buffer was last read before the previous barrier
         __syncthreads();
     }
 #pragma unroll
@@ -95,6 +129,24 @@ __global__ void __launch_bounds__(256) fz_gemm_nt_kernel(int m, int n, int kk, f
             const float v = alpha * acc[i][j];
             *c = (beta != 0.f) ? fmaf(beta, *c, v) : v;
         }
+    }
+}
+
+// X[r][c] = X[c][r] for c > r: the upper triangle of a k x k matrix copied
+// from its lower one through 32 x 32 tiles (block 32 x 8).  Tiles wholly in
+// the lower triangle exit; a diagonal tile reads before it writes.
+__global__ void fz_mirror_lower_kernel(float *X, int k) {
+    __shared__ float tile[32][33];
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    if (c0 < r0) return;
+    for (int dj = threadIdx.y; dj < 32; dj += 8) {
+        const int c = c0 + dj, r = r0 + threadIdx.x;
+        if (c < k && r < k) tile[dj][threadIdx.x] = X[int64_t(c) * k + r];
+    }
+    __syncthreads();
+    for (int di = threadIdx.y; di < 32; di += 8) {
+        const int r = r0 + di, c = c0 + threadIdx.x;
+        if (r < k && c < k && c > r) X[int64_t(r) * k + c] = tile[threadIdx.x][di];
     }
 }
 
@@ -157,33 +209,47 @@ __global__ void __launch_bounds__(1024) fz_ridge_kernel(float *G, int k, float r
     if (threadIdx.x == 0) *rho_out = rho;
 }
 
-// Cholesky of the nb x nb diagonal block at (j0, j0) in place (one warp, lane
-// = row); the strict upper triangle of the block is zeroed.  A pivot that is
-// not positive records DBF_ERR_NUMERIC and continues with FLT_MIN.
-__global__ void fz_chol_diag_kernel(float *G, int k, int j0, int nb, int *status) {
-    __shared__ float L[kCholNB][kCholNB + 1];
+// Cholesky of the nb x nb diagonal block at (j0, j0) in place (one warp):
+// lane = row, the row held in registers, column c passed between lanes by
+// shuffles (right-looking: pivot, scale column c, update the columns right of
+// it); the strict upper triangle of the block is zeroed.  A pivot that is not
+// positive records DBF_ERR_NUMERIC and continues with FLT_MIN.
+__global__ void __launch_bounds__(32) fz_chol_diag_kernel(float *G, int k, int j0, int nb, int *status) {
+    __shared__ float T[kCholNB][kCholNB + 1];
     const int lane = threadIdx.x;
     if (lane < nb)
-        for (int c = 0; c < nb; ++c) L[lane][c] = G[int64_t(j0 + lane) * k + j0 + c];
+#pragma unroll 8
+        for (int a = 0; a < nb; ++a) T[a][lane] = G[int64_t(j0 + a) * k + j0 + lane];  // row a, coalesced
     __syncwarp();
-    for (int c = 0; c < nb; ++c) {
-        if (lane == c) {
-            float d = L[c][c];
+    float row[kCholNB];
+#pragma unroll
+    for (int c = 0; c < kCholNB; ++c) row[c] = (lane < nb && c < nb) ? T[lane][c] : 0.f;
+#pragma unroll
+    for (int c = 0; c < kCholNB; ++c) {
+        if (c < nb) {  // warp-uniform
+            float d = __shfl_sync(0xffffffffu, row[c], c);
             if (!(d > 0.f)) {
-                record_status(status, DBF_ERR_NUMERIC);
+                if (lane == 0) record_status(status, DBF_ERR_NUMERIC);
                 d = FLT_MIN;
             }
-            L[c][c] = sqrtf(d);
+            const float sd = sqrtf(d);
+            if (lane == c) row[c] = sd;
+            else if (lane > c) row[c] = row[c] / sd;
+            const float lc = row[c];
+#pragma unroll
+            for (int cc = c + 1; cc < kCholNB; ++cc) {
+                const float lcc = __shfl_sync(0xffffffffu, lc, cc);  // L[cc][c]
+                if (lane >= cc) row[cc] = fmaf(-lc, lcc, row[cc]);
+            }
         }
-        __syncwarp();
-        if (lane > c && lane < nb) L[lane][c] = L[lane][c] / L[c][c];
-        __syncwarp();
-        if (lane > c && lane < nb)
-            for (int cc = c + 1; cc <= lane; ++cc) L[lane][cc] -= L[lane][c] * L[cc][c];
-        __syncwarp();
     }
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < kCholNB; ++c) T[lane][c] = row[c];
+    __syncwarp();
     if (lane < nb)
-        for (int c = 0; c < nb; ++c) G[int64_t(j0 + lane) * k + j0 + c] = (c <= lane) ? L[lane][c] : 0.f;
+#pragma unroll 8
+        for (int a = 0; a < nb; ++a) G[int64_t(j0 + a) * k + j0 + lane] = (lane <= a) ? T[a][lane] : 0.f;
 }
 
 // Panel below the diagonal block: row r >= j0 + nb solves x L_jj^T = G[r, j0:j0+nb]
@@ -214,21 +280,47 @@ __global__ void __launch_bounds__(128) fz_chol_panel_kernel(float *G, int k, int
 }
 
 // Row r of L^-T (= column r of L^-1): solve L x = e_r by forward substitution,
-// one warp per row, x staged in dynamic shared memory (k floats).
-__global__ void fz_tri_inv_rows_kernel(const float *__restrict__ L, int k, float *__restrict__ LinvT) {
+// one warp per row, x staged in dynamic shared memory (k floats).  Rows of L
+// are taken 32 at a time: first the part of each row's sum over the x already
+// known (independent dot products, four rows per pass, loads overlapped),
+// then a 32-step solve with the diagonal block held one row per lane.
+__global__ void __launch_bounds__(32) fz_tri_inv_rows_kernel(const float *__restrict__ L, int k,
+                                                             float *__restrict__ LinvT) {
     extern __shared__ float xs[];
     const int r = blockIdx.x, lane = threadIdx.x;
     float *out = LinvT + int64_t(r) * k;
     for (int c = lane; c < r; c += 32) out[c] = 0.f;
-    if (lane == 0) xs[r] = 1.f / L[int64_t(r) * k + r];
-    __syncwarp();
-    for (int c = r + 1; c < k; ++c) {
-        const float *lc = L + int64_t(c) * k;
-        float s = 0.f;
-        for (int t = r + lane; t < c; t += 32) s += lc[t] * xs[t];
+    for (int c0 = r; c0 < k; c0 += 32) {
+        const int nb = min(32, k - c0);
+        float s = (c0 == r && lane == 0) ? 1.f : 0.f;  // e_r restricted to rows c0 .. c0 + 31
+        for (int j0 = 0; j0 < nb; j0 += 4) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int t = r + lane; t < c0; t += 32) {
+                const float xt = xs[t];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) xs[c] = -s / lc[c];
+                for (int q = 0; q < 4; ++q)
+                    if (j0 + q < nb) d[q] = fmaf(L[int64_t(c0 + j0 + q) * k + t], xt, d[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float v = d[q];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == j0 + q) s -= v;
+            }
+        }
+        float lrow[32];  // L[c0 + lane][c0 .. c0 + lane]
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj)
+            lrow[jj] = (lane < nb && jj <= lane) ? L[int64_t(c0 + lane) * k + c0 + jj] : 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            if (jj < nb) {
+                const float xj = __shfl_sync(0xffffffffu, lane == jj ? s / lrow[jj] : 0.f, jj);
+                if (lane > jj) s = fmaf(-lrow[jj], xj, s);
+                if (lane == jj) xs[c0 + jj] = xj;
+            }
+        }
         __syncwarp();
     }
     for (int c = r + lane; c < k; c += 32) out[c] = xs[c];
@@ -318,10 +410,15 @@ inline unsigned cdiv(int64_t a, int64_t b) { return unsigned((a + b - 1) / b); }
 inline size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
 cudaError_t gemm_nt(int m, int n, int kk, float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
-                    float beta, float *C, int64_t ldc, cudaStream_t s) {
+                    float beta, float *C, int64_t ldc, cudaStream_t s, int lower = 0) {
     if (m <= 0 || n <= 0) return cudaSuccess;
-    fz_gemm_nt_kernel<<<dim3(cdiv(n, kGemmBN), cdiv(m, kGemmBM)), 256, 0, s>>>(m, n, kk, alpha, A, lda, B, ldb, beta,
-                                                                               C, ldc);
+    const dim3 grid(cdiv(n, kGemmBN), cdiv(m, kGemmBM));
+    const bool vec = (lda % 4 == 0) && (ldb % 4 == 0) && (kk % 4 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) == 0;
+    if (vec)
+        fz_gemm_nt_kernel<true><<<grid, 256, 0, s>>>(m, n, kk, alpha, A, lda, B, ldb, beta, C, ldc, lower);
+    else
+        fz_gemm_nt_kernel<false><<<grid, 256, 0, s>>>(m, n, kk, alpha, A, lda, B, ldb, beta, C, ldc, lower);
     return cudaGetLastError();
 }
 
@@ -364,9 +461,9 @@ int step_launches(int k, int inner, int power_iters) {
     if (inner <= 0) return 0;
     const int chol = 3 * chol_steps(k) - 2;  // the last block has no panel and no trailing update
     const int svid = (power_iters > 0 ? 3 * power_iters : 1) + 1;
-    // F, F F^T, ridge; Cholesky; L^-T rows, inverse, T F^T, first dual pass;
+    // F, F F^T, ridge; Cholesky; L^-T rows, inverse and its mirror, T F^T, first dual pass;
     // per iteration the P-update GEMM, the SVID passes and (but the last) a dual pass
-    return 3 + chol + 4 + inner * (1 + svid) + (inner - 1);
+    return 3 + chol + 5 + inner * (1 + svid) + (inner - 1);
 }
 
 // SVID of Y [n x k]: c (= v) by power iteration, then r = |Y| c; S_out optional.
@@ -398,7 +495,8 @@ cudaError_t admm_step(const float *T, int n, int p, int k, const float *r2, cons
     cudaError_t e;
     fz_build_f_kernel<<<dim3(cdiv(k, 32), cdiv(p, 32)), dim3(32, 8), 0, s>>>(r2, S2, c2, p, k, w.F);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = gemm_nt(k, k, p, 1.f, w.F, p, w.F, p, 0.f, w.G, k, s)) != cudaSuccess) return e;
+    // F F^T: the Cholesky steps read only its lower triangle (and the diagonal)
+    if ((e = gemm_nt(k, k, p, 1.f, w.F, p, w.F, p, 0.f, w.G, k, s, 1)) != cudaSuccess) return e;
     fz_ridge_kernel<<<1, 1024, 0, s>>>(w.G, k, prm.rho_rel, w.rho);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     for (int j0 = 0; j0 < k; j0 += kCholNB) {
@@ -408,14 +506,17 @@ cudaError_t admm_step(const float *T, int n, int p, int k, const float *r2, cons
         if (j1 < k) {
             fz_chol_panel_kernel<<<cdiv(k - j1, 128), 128, 0, s>>>(w.G, k, j0, nb);
             if ((e = gemm_nt(k - j1, k - j1, nb, -1.f, w.G + int64_t(j1) * k + j0, k, w.G + int64_t(j1) * k + j0, k,
-                             1.f, w.G + int64_t(j1) * k + j1, k, s)) != cudaSuccess)
+                             1.f, w.G + int64_t(j1) * k + j1, k, s, 1)) != cudaSuccess)
                 return e;
         }
     }
     const size_t tri_smem = sizeof(float) * size_t(k);
     fz_tri_inv_rows_kernel<<<k, 32, tri_smem, s>>>(w.G, k, w.LinvT);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = gemm_nt(k, k, k, 1.f, w.LinvT, k, w.LinvT, k, 0.f, w.Ginv, k, s)) != cudaSuccess) return e;
+    // L^-T (L^-T)^T: the lower triangle, then the upper one copied from it
+    if ((e = gemm_nt(k, k, k, 1.f, w.LinvT, k, w.LinvT, k, 0.f, w.Ginv, k, s, 1)) != cudaSuccess) return e;
+    fz_mirror_lower_kernel<<<dim3(cdiv(k, 32), cdiv(k, 32)), dim3(32, 8), 0, s>>>(w.Ginv, k);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = gemm_nt(n, k, p, 1.f, T, p, w.F, p, 0.f, w.Cw, k, s)) != cudaSuccess) return e;
     const dim3 ew(cdiv(k, 256), n);
     fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS, S, r, c, w.rho, k, 1);

@@ -141,11 +141,11 @@ def test_factorize_sizes_and_launch_counts(lib):
     assert lib.factorize_workspace_bytes(0, 4, 4) == 0
     assert lib.factorize_workspace_bytes(4, 4, 16385) == 0
     # per step: F, F F^T, ridge; 3 per 32-column Cholesky block less 2; L^-T, inverse,
-    # T F^T, first dual; per iteration 1 GEMM + 3q + 1 SVID passes, dual between iterations
+    # its mirror, T F^T, first dual; per iteration 1 GEMM + 3q + 1 SVID passes, dual between iterations
     k, inner, q = 70, 4, 5
-    step = 3 + (3 * 3 - 2) + 4 + inner * (1 + 3 * q + 1) + (inner - 1)
+    step = 3 + (3 * 3 - 2) + 5 + inner * (1 + 3 * q + 1) + (inner - 1)
     assert lib.factorize_launch_count(100, 80, k, 3, inner, q, 1.0) == 2 + 3 * 2 * step + 1
-    step0 = 3 + (3 * 3 - 2) + 4 + inner * (1 + 1 + 1) + (inner - 1)   # power_iters = 0: fill + rows
+    step0 = 3 + (3 * 3 - 2) + 5 + inner * (1 + 1 + 1) + (inner - 1)   # power_iters = 0: fill + rows
     assert lib.factorize_launch_count(100, 80, k, 1, inner, 0, 1.0) == 2 + 2 * step0 + 1
     assert lib.factorize_launch_count(100, 80, k, 0, inner, q, 1.0) == 0
     assert lib.factorize_launch_count(100, 80, k, 1, 0, q, 1.0) == 0
