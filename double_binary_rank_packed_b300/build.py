@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libdbf.so")
 SOURCES = ["dbf_api.cu", "decode.cu", "prefill.cu", "misc.cu", "noalloc.cu", "factorize.cu"]
-HEADERS = ["common.cuh", "kernels.h"]
+HEADERS = ["common.cuh", "kernels.h", "factorize.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

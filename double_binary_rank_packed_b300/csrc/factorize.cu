@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "factorize.h"
 
 namespace dbfk {
 

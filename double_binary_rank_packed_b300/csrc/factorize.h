@@ -1,0 +1,20 @@
+// Host-side launchers of the dense double binary factorization (factorize.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dbf.h"
+
+namespace dbfk {
+
+// Workspace, launch count and launches of dbf_factorize.
+size_t factorize_workspace_bytes(int64_t N, int64_t M, int64_t k);
+int factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_params &p);
+size_t factorize_tri_smem(int64_t k);
+cudaError_t prepare_factorize(int64_t k);
+cudaError_t launch_factorize(const float *W, int N, int M, int k, const dbf_factorize_params &p, float *a,
+                             int8_t *A, float *m_left, float *m_right, int8_t *B, float *b, void *workspace,
+                             int *status, cudaStream_t s);
+
+}  // namespace dbfk

@@ -174,17 +174,6 @@ cudaError_t launch_prefill_gemm(int stage, const CUtensorMap &act_map, const PfA
 int prefill_pick_bn(int ell, int rows_cover, int64_t C, int nk, int num_sms);
 bool encode_act_map(CUtensorMap *map, const __half *base, int rows, int cols_pad, int ld, int box_rows);
 
-// ------------------------------------------------- dense factorization
-
-// Workspace, launch count and launches of dbf_factorize (factorize.cu).
-size_t factorize_workspace_bytes(int64_t N, int64_t M, int64_t k);
-int factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_params &p);
-size_t factorize_tri_smem(int64_t k);
-cudaError_t prepare_factorize(int64_t k);
-cudaError_t launch_factorize(const float *W, int N, int M, int k, const dbf_factorize_params &p, float *a,
-                             int8_t *A, float *m_left, float *m_right, int8_t *B, float *b, void *workspace,
-                             int *status, cudaStream_t s);
-
 // --------------------------------------------------------------- misc
 
 cudaError_t launch_pack(const int8_t *signs, int64_t rows, int64_t cols, uint32_t *words, int64_t ldw,
