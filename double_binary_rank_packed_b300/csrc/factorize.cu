@@ -37,56 +37,58 @@ namespace dbfk {
 
 namespace {
 
-constexpr int kGemmBM = 128, kGemmBN = 128, kGemmBK = 8;
+constexpr int kGemmBM = 128, kGemmBN = 128, kGemmBK = 16, kGemmStages = 3;
+constexpr int kGemmPitch = kGemmBM + 4;  // floats per k row of a staged tile
+constexpr size_t kGemmSmem = sizeof(float) * 2 * kGemmStages * kGemmBK * kGemmPitch;  // 50,688 B
 constexpr int kCholNB = 32;
 constexpr int kColsThreads = 256;
 constexpr int kMaxColChunks = 32;
 
+// 4-byte asynchronous copy global -> shared; valid == false writes a zero
+// (source size 0) and reads nothing.
+__device__ __forceinline__ void fz_cp_async_4(float *dst, const float *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void fz_cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // C = alpha * A B^T + beta * C; A [m x kk] (lda), B [n x kk] (ldb), C [m x n]
 // (ldc), all row-major fp32.  C is not read when beta == 0.  A 128 x 128 tile
-// per CTA, 8 x 8 outputs per thread, k-steps of 8 staged transposed in two
-// shared-memory buffers: the next step's global loads are in flight while the
-// current one is multiplied.  Out-of-range rows and k are zero-filled.  VEC:
-// lda, ldb and kk are multiples of 4 and A, B 16-byte aligned, so each
-// thread's four k values are one float4 load.  lower: only the tiles that
-// touch the lower triangle (col <= row) are computed; the others are left as
-// they are (for products whose upper triangle nothing reads).
-template <bool VEC>
+// per CTA, 8 x 8 outputs per thread.  Operand tiles of 16 k-steps are copied
+// straight into shared memory, transposed (k-major, row pitch 132 floats so
+// the copies conflict at most 2-way and the fragment reads stay 16-byte
+// aligned), by 4-byte asynchronous copies three stages deep: two stages are
+// in flight while one is multiplied, one barrier per stage.  Out-of-range
+// rows and k are zero-filled.  lower: only the tiles that touch the lower
+// triangle (col <= row) are computed; the others are left as they are (for
+// products whose upper triangle nothing reads).
 __global__ void __launch_bounds__(256, 2) fz_gemm_nt_kernel(int m, int n, int kk, float alpha,
                                                             const float *__restrict__ A, int64_t lda,
                                                             const float *__restrict__ B, int64_t ldb, float beta,
                                                             float *C, int64_t ldc, int lower) {
-    __shared__ __align__(16) float As[2][kGemmBK][kGemmBM];
-    __shared__ __align__(16) float Bs[2][kGemmBK][kGemmBN];
+    extern __shared__ __align__(16) float fz_gemm_smem[];
+    float *As = fz_gemm_smem;                                       // [stage][k][kGemmPitch]
+    float *Bs = fz_gemm_smem + kGemmStages * kGemmBK * kGemmPitch;  // same
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int row0 = blockIdx.y * kGemmBM, col0 = blockIdx.x * kGemmBN;
     if (lower && col0 >= row0 + kGemmBM) return;  // the whole tile is above the diagonal
-    const int lr = tid >> 1, lt = (tid & 1) * 4;  // loader: row lr, k offsets lt..lt+3
-    const int ga = row0 + lr, gb = col0 + lr;
-    const float *pa = A + int64_t(ga < m ? ga : 0) * lda;
-    const float *pb = B + int64_t(gb < n ? gb : 0) * ldb;
-    float ra[4], rb[4];
-    auto load = [&](int t0) {
-        const int gt = t0 + lt;
-        if constexpr (VEC) {
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 va = (ga < m && gt < kk) ? *reinterpret_cast<const float4 *>(pa + gt) : z;
-            const float4 vb = (gb < n && gt < kk) ? *reinterpret_cast<const float4 *>(pb + gt) : z;
-            ra[0] = va.x; ra[1] = va.y; ra[2] = va.z; ra[3] = va.w;
-            rb[0] = vb.x; rb[1] = vb.y; rb[2] = vb.z; rb[3] = vb.w;
-        } else {
+    const int lk = tid & 15, lr0 = tid >> 4;       // copies: k offset lk, rows lr0 + 16 i
+    auto issue = [&](int stage, int t0) {
+        float *as = As + stage * kGemmBK * kGemmPitch + lk * kGemmPitch;
+        float *bs = Bs + stage * kGemmBK * kGemmPitch + lk * kGemmPitch;
+        const int gt = t0 + lk;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                ra[q] = (ga < m && gt + q < kk) ? pa[gt + q] : 0.f;
-                rb[q] = (gb < n && gt + q < kk) ? pb[gt + q] : 0.f;
-            }
-        }
-    };
-    auto store = [&](int buf) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            As[buf][lt + q][lr] = ra[q];
-            Bs[buf][lt + q][lr] = rb[q];
+        for (int i = 0; i < 8; ++i) {
+            const int r = lr0 + 16 * i;
+            const int ga = row0 + r, gb = col0 + r;
+            const bool va = ga < m && gt < kk, vb = gb < n && gt < kk;
+            fz_cp_async_4(as + r, va ? A + int64_t(ga) * lda + gt : A, va);
+            fz_cp_async_4(bs + r, vb ? B + int64_t(gb) * ldb + gt : B, vb);
         }
     };
     float acc[8][8];
@@ -95,19 +97,24 @@ __global__ void __launch_bounds__(256, 2) fz_gemm_nt_kernel(int m, int n, int kk
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-    load(0);
-    store(0);
-    __syncthreads();
-    int buf = 0;
-    for (int t0 = 0; t0 < kk; t0 += kGemmBK, buf ^= 1) {
-        const bool more = t0 + kGemmBK < kk;
-        if (more) load(t0 + kGemmBK);
+    const int nsteps = (kk + kGemmBK - 1) / kGemmBK;
+    issue(0, 0);
+    cp_async_commit();
+    if (nsteps > 1) issue(1, kGemmBK);
+    cp_async_commit();
+    for (int st = 0; st < nsteps; ++st) {
+        fz_cp_async_wait<1>();  // this thread's copies of stage st have landed
+        __syncthreads();        // everyone's have; stage (st + 2) % 3 was last read in st - 1
+        if (st + 2 < nsteps) issue((st + 2) % kGemmStages, (st + 2) * kGemmBK);
+        cp_async_commit();      // possibly empty: keeps one group per stage
+        const float *as = As + (st % kGemmStages) * kGemmBK * kGemmPitch;
+        const float *bs = Bs + (st % kGemmStages) * kGemmBK * kGemmPitch;
 #pragma unroll
         for (int t = 0; t < kGemmBK; ++t) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][t][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][t][64 + ty * 4]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][t][tx * 4]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][t][64 + tx * 4]);
+            const float4 a0 = *reinterpret_cast<const float4 *>(as + t * kGemmPitch + ty * 4);
+            const float4 a1 = *reinterpret_cast<const float4 *>(as + t * kGemmPitch + 64 + ty * 4);
+            const float4 b0 = *reinterpret_cast<const float4 *>(bs + t * kGemmPitch + tx * 4);
+            const float4 b1 = *reinterpret_cast<const float4 *>(bs + t * kGemmPitch + 64 + tx * 4);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -115,9 +122,8 @@ __global__ void __launch_bounds__(256, 2) fz_gemm_nt_kernel(int m, int n, int kk
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
-        if (more) store(buf ^ 1);  // that buffer was last read before the previous barrier
-        __syncthreads();
     }
+    fz_cp_async_wait<0>();
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int gr = row0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
@@ -414,12 +420,7 @@ cudaError_t gemm_nt(int m, int n, int kk, float alpha, const float *A, int64_t l
                     float beta, float *C, int64_t ldc, cudaStream_t s, int lower = 0) {
     if (m <= 0 || n <= 0) return cudaSuccess;
     const dim3 grid(cdiv(n, kGemmBN), cdiv(m, kGemmBM));
-    const bool vec = (lda % 4 == 0) && (ldb % 4 == 0) && (kk % 4 == 0) &&
-                     ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) == 0;
-    if (vec)
-        fz_gemm_nt_kernel<true><<<grid, 256, 0, s>>>(m, n, kk, alpha, A, lda, B, ldb, beta, C, ldc, lower);
-    else
-        fz_gemm_nt_kernel<false><<<grid, 256, 0, s>>>(m, n, kk, alpha, A, lda, B, ldb, beta, C, ldc, lower);
+    fz_gemm_nt_kernel<<<grid, 256, kGemmSmem, s>>>(m, n, kk, alpha, A, lda, B, ldb, beta, C, ldc, lower);
     return cudaGetLastError();
 }
 
@@ -549,6 +550,9 @@ int factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_
 size_t factorize_tri_smem(int64_t k) { return sizeof(float) * size_t(k); }
 
 cudaError_t prepare_factorize(int64_t k) {
+    cudaError_t e = cudaFuncSetAttribute(fz_gemm_nt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kGemmSmem));
+    if (e != cudaSuccess) return e;
     const size_t smem = factorize_tri_smem(k);
     if (smem <= 48 * 1024) return cudaSuccess;
     return cudaFuncSetAttribute(fz_tri_inv_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
