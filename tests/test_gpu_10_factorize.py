@@ -161,6 +161,22 @@ def test_argument_errors(cuda_lib):
     assert e.value.code == cuda_lib.DBF_ERR_WORKSPACE
 
 
+def test_nan_in_the_fixed_factor_reports_a_numeric_status(cuda_lib):
+    # A NaN scale makes every pivot of F F^T + rho I NaN, which fails the
+    # positivity check: the call still completes (no value decides an
+    # address) and the status word says DBF_ERR_NUMERIC; reading it clears it.
+    N, M, k = 40, 36, 8
+    w = G.make_dense_weight(N, M, 9)
+    start = list(G.make_factorize_start(N, M, k, 9))
+    start[3] = start[3].copy()
+    start[3][2] = np.nan
+    fs = _dev(start)
+    cuda_lib.factorize(torch.from_numpy(w).cuda(), *fs, outer=1, inner=2, power_iters=3, rho_rel=1.0)
+    assert cuda_lib.check_status() == cuda_lib.DBF_ERR_NUMERIC
+    assert cuda_lib.check_status() == 0
+    assert cuda_lib.status_string(cuda_lib.DBF_ERR_NUMERIC) != "unknown status"
+
+
 def _balanced_fp16(a, m, b):
     # fp16 scales for the matmul: equalise the geometric means of alpha, beta
     # and gamma (their product per entry of W_hat is unchanged).
