@@ -48,15 +48,24 @@ Readings where the pages are silent (each stated once here):
     starts the first step at Z = 0); the initial factors are inputs;
   * sign(0) = +1, as when packing signs;
   * the middle scale of the result is m = mL . mR (each step owns one side);
-  * the importance weighting by activation norms and output gradients
-    (same section) needs calibration data and is not part of this oracle.
+  * importance (same section: input activation norms and output gradient
+    norms weight the approximation error): the objective becomes
+    ||diag(d_out) (W - W_hat) diag(d_in)||_F with positive weights d_out [N],
+    d_in [M].  Since diag(d_out) P and Q diag(d_in) are again of the
+    factored form (the weights fold into a and b), this is the unweighted
+    problem for W' = diag(d_out) W diag(d_in): factorize W' from the start
+    (d_out . a, A, mL; mR, B, b . d_in), then divide d_out out of a and d_in
+    out of b.  The weights themselves are inputs (no calibration data here).
 
 Pins (tests/test_oracle_factorize_pins.py): SVID is exact and idempotent on its set;
 its rank-1 part converges to the leading singular pair of |Y| (library SVD);
 the P-update equals the ridge least-squares solution of a stacked system
 (library least squares); the exact factors of an exactly representable W
 are a fixed point of both ADMM steps; ADMM started from zero recovers the
-left factor of such a W; a planted dual-sign mistake fails that recovery.
+left factor of such a W; a planted dual-sign mistake fails that recovery;
+unit importance weights change nothing; the weighted error of the result is
+the plain error of the scaled problem; weighting a set of input columns
+lowers their error.
 """
 
 from __future__ import annotations
@@ -155,6 +164,31 @@ def factorize(w, left, right, outer: int, inner: int, power_iters: int, rho_rel:
         b, bt, mR = admm_left(w.T, pt, b, B.T, mR, inner, power_iters, rho_rel)
         B = np.ascontiguousarray(bt.T)
     return a, A, mL, mR, B, b
+
+
+def factorize_weighted(w, d_out, d_in, left, right, outer: int, inner: int, power_iters: int, rho_rel: float):
+    """Importance-weighted factorization (DBF page, section 2, Importancia de
+    Entradas y Salidas): minimise ||diag(d_out)(W - W_hat)diag(d_in)|| by the
+    same alternating steps on W' = diag(d_out) W diag(d_in) in the variables
+    a' = d_out . a, b' = b . d_in.  Returns (a, A, mL, mR, B, b)."""
+    w = np.asarray(w, np.float64)
+    d_out = np.asarray(d_out, np.float64)
+    d_in = np.asarray(d_in, np.float64)
+    wp = d_out[:, None] * w * d_in[None, :]
+    lp = (np.asarray(left[0], np.float64) * d_out, left[1], left[2])
+    rp = (right[0], right[1], np.asarray(right[2], np.float64) * d_in)
+    a, A, mL, mR, B, b = factorize(wp, lp, rp, outer, inner, power_iters, rho_rel)
+    return a / d_out, A, mL, mR, B, b / d_in
+
+
+def weighted_rel_error(w, d_out, d_in, a, A, mL, mR, B, b) -> float:
+    """||diag(d_out)(W - W_hat)diag(d_in)||_F / ||diag(d_out) W diag(d_in)||_F."""
+    w = np.asarray(w, np.float64)
+    d_out = np.asarray(d_out, np.float64)[:, None]
+    d_in = np.asarray(d_in, np.float64)[None, :]
+    d = d_out * (w - reconstruct(a, A, mL, mR, B, b)) * d_in
+    ref = d_out * w * d_in
+    return float(np.sqrt(np.sum(d * d) / np.sum(ref * ref)))
 
 
 def reconstruct(a, A, mL, mR, B, b) -> np.ndarray:

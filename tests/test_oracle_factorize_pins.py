@@ -146,3 +146,55 @@ def test_alternation_reduces_the_error_on_a_random_matrix():
     one_bit = np.linalg.norm(w - fz.svid_dense(r, S, c)) / np.linalg.norm(w)
     assert e6 < e1
     assert e6 < one_bit
+
+
+def _weighted_case(seed, N=96, M=80, k=64):
+    g = _rng(seed)
+    w = g.standard_normal((N, M)) * 0.02
+    left = (np.zeros(N), np.ones((N, k), np.int8), np.zeros(k))
+    right = (np.ones(k), fz.sign_pm1(g.standard_normal((k, M))), np.ones(M))
+    return w, left, right
+
+
+def test_unit_importance_weights_change_nothing():
+    w, left, right = _weighted_case(10)
+    plain = fz.factorize(w, left, right, 2, 4, 5, 1.0)
+    weighted = fz.factorize_weighted(w, np.ones(w.shape[0]), np.ones(w.shape[1]), left, right, 2, 4, 5, 1.0)
+    for x, y in zip(plain, weighted):
+        assert np.array_equal(x, y)
+
+
+def test_weighted_result_is_the_scaled_problem_solved_and_unscaled():
+    # The weighted error of the returned factors equals the plain error of
+    # factorizing W' = diag(d_out) W diag(d_in) from the explicitly scaled
+    # start; a result left in the scaled variables (a planted mistake) or
+    # scaled the wrong way does not.
+    w, left, right = _weighted_case(11)
+    g = _rng(12)
+    d_out = np.exp(0.5 * g.standard_normal(w.shape[0]))
+    d_in = np.exp(0.5 * g.standard_normal(w.shape[1]))
+    res = fz.factorize_weighted(w, d_out, d_in, left, right, 2, 4, 5, 1.0)
+    wp = d_out[:, None] * w * d_in[None, :]
+    direct = fz.factorize(wp, (left[0] * d_out, left[1], left[2]), (right[0], right[1], right[2] * d_in),
+                          2, 4, 5, 1.0)
+    e_direct = fz.rel_error(wp, *direct)
+    assert fz.weighted_rel_error(w, d_out, d_in, *res) == pytest.approx(e_direct, rel=1e-10)
+    left_scaled = (direct[0],) + tuple(res[1:])
+    assert abs(fz.weighted_rel_error(w, d_out, d_in, *left_scaled) - e_direct) > 1e-2
+    wrong_way = (res[0] / d_out,) + tuple(res[1:5]) + (res[5] / d_in,)
+    assert abs(fz.weighted_rel_error(w, d_out, d_in, *wrong_way) - e_direct) > 1e-2
+
+
+def test_weighting_input_columns_lowers_their_error():
+    w, left, right = _weighted_case(13, N=128, M=96, k=96)
+    heavy = np.arange(0, w.shape[1], 8)
+    d_in = np.ones(w.shape[1])
+    d_in[heavy] = 10.0
+    plain = fz.factorize(w, left, right, 4, 8, 6, 1.0)
+    weighted = fz.factorize_weighted(w, np.ones(w.shape[0]), d_in, left, right, 4, 8, 6, 1.0)
+
+    def col_err(f):
+        d = w - fz.reconstruct(*f)
+        return np.sqrt(np.sum(d[:, heavy] ** 2) / np.sum(w[:, heavy] ** 2))
+
+    assert col_err(weighted) < 0.8 * col_err(plain)
