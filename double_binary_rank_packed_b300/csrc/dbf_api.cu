@@ -976,6 +976,40 @@ int dbf_factorize(const float *W, int64_t N, int64_t M, int64_t k, const dbf_fac
     return e == cudaSuccess ? DBF_OK : cuda_fail(e, "factorize");
 }
 
+size_t dbf_factorize_weighted_workspace_bytes(int64_t N, int64_t M, int64_t k) {
+    if (N < 1 || M < 1 || k < 1 || N > 65535 || M > 65535 || k > 16384) return 0;
+    return dbfk::factorize_weighted_workspace_bytes(N, M, k);
+}
+
+int dbf_factorize_weighted_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_params *p) {
+    if (check_factorize_args(N, M, k, p) != DBF_OK) return -1;
+    return dbfk::factorize_weighted_launch_count(N, M, k, *p);
+}
+
+int dbf_factorize_weighted(const float *W, int64_t N, int64_t M, int64_t k, const dbf_factorize_params *p,
+                           const float *d_out, const float *d_in, float *a, int8_t *A, float *m_left,
+                           float *m_right, int8_t *B, float *b, void *workspace, size_t ws_bytes, void *stream) {
+    int rc = check_factorize_args(N, M, k, p);
+    if (rc) return rc;
+    if (!W || !d_out || !d_in || !a || !A || !m_left || !m_right || !B || !b) return DBF_ERR_INVALID_ARG;
+    const size_t need = dbfk::factorize_weighted_workspace_bytes(N, M, k);
+    if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
+    const uintptr_t f4 = reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(d_out) |
+                         reinterpret_cast<uintptr_t>(d_in) | reinterpret_cast<uintptr_t>(a) |
+                         reinterpret_cast<uintptr_t>(m_left) | reinterpret_cast<uintptr_t>(m_right) |
+                         reinterpret_cast<uintptr_t>(b);
+    if (f4 & 3) return DBF_ERR_ALIGNMENT;
+    int *st = status_ptr();
+    if (!st) return cuda_fail(cudaGetLastError(), "status word");
+    cudaError_t e = dbfk::prepare_factorize(k);
+    if (e != cudaSuccess) return cuda_fail(e, "factorize: shared memory attribute");
+    if (p->outer == 0 || p->inner == 0) return DBF_OK;
+    e = dbfk::launch_factorize_weighted(W, int(N), int(M), int(k), *p, d_out, d_in, a, A, m_left, m_right, B, b,
+                                        workspace, st, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "factorize (weighted)");
+}
+
 int dbf_check_status(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "dbf_check_status sync");

@@ -413,6 +413,30 @@ __global__ void __launch_bounds__(256) fz_dual_rhs_kernel(const float *__restric
     }
 }
 
+// Importance weighting: W'[i][j] = d_out[i] * W[i][j] * d_in[j].  Grid: x over
+// column blocks of 256, y over rows.
+__global__ void __launch_bounds__(256) fz_weight_kernel(const float *__restrict__ W, const float *__restrict__ d_out,
+                                                        const float *__restrict__ d_in, int M,
+                                                        float *__restrict__ Wp) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= M) return;
+    const int64_t e = int64_t(blockIdx.y) * M + j;
+    Wp[e] = d_out[blockIdx.y] * W[e] * d_in[j];
+}
+
+// v[i] *= d[i] (divide == 0) or v[i] /= d[i]; a weight that is not positive
+// and finite records DBF_ERR_DEVICE_ARG and leaves v[i] as it is.
+__global__ void fz_scale_vec_kernel(float *v, const float *__restrict__ d, int n, int divide, int *status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float w = d[i];
+    if (!(w > 0.f && w <= FLT_MAX)) {
+        record_status(status, DBF_ERR_DEVICE_ARG);
+        return;
+    }
+    v[i] = divide ? v[i] / w : v[i] * w;
+}
+
 inline unsigned cdiv(int64_t a, int64_t b) { return unsigned((a + b - 1) / b); }
 inline size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -556,6 +580,34 @@ cudaError_t prepare_factorize(int64_t k) {
     const size_t smem = factorize_tri_smem(k);
     if (smem <= 48 * 1024) return cudaSuccess;
     return cudaFuncSetAttribute(fz_tri_inv_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+}
+
+size_t factorize_weighted_workspace_bytes(int64_t N, int64_t M, int64_t k) {
+    return carve(nullptr, N, M, k, nullptr) + align_up(sizeof(float) * size_t(N) * M);
+}
+
+int factorize_weighted_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_params &p) {
+    const int base = factorize_launch_count(N, M, k, p);
+    return base > 0 ? base + 5 : 0;  // W', the scales in, the factorization, the scales out
+}
+
+cudaError_t launch_factorize_weighted(const float *W, int N, int M, int k, const dbf_factorize_params &p,
+                                      const float *d_out, const float *d_in, float *a, int8_t *A, float *m_left,
+                                      float *m_right, int8_t *B, float *b, void *workspace, int *status,
+                                      cudaStream_t s) {
+    // The weighted problem is the plain one for W' = diag(d_out) W diag(d_in)
+    // in the variables d_out . a and b . d_in; W' lives after the scratch.
+    float *Wp = reinterpret_cast<float *>(static_cast<char *>(workspace) + carve(nullptr, N, M, k, nullptr));
+    fz_weight_kernel<<<dim3(cdiv(M, 256), N), 256, 0, s>>>(W, d_out, d_in, M, Wp);
+    fz_scale_vec_kernel<<<cdiv(N, 256), 256, 0, s>>>(a, d_out, N, 0, status);
+    fz_scale_vec_kernel<<<cdiv(M, 256), 256, 0, s>>>(b, d_in, M, 0, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if ((e = launch_factorize(Wp, N, M, k, p, a, A, m_left, m_right, B, b, workspace, status, s)) != cudaSuccess)
+        return e;
+    fz_scale_vec_kernel<<<cdiv(N, 256), 256, 0, s>>>(a, d_out, N, 1, status);
+    fz_scale_vec_kernel<<<cdiv(M, 256), 256, 0, s>>>(b, d_in, M, 1, status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_factorize(const float *W, int N, int M, int k, const dbf_factorize_params &p, float *a,

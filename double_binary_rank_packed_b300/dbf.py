@@ -42,6 +42,7 @@ EXPORTED = (
     "dbf_backward", "dbf_backward_workspace_bytes", "dbf_matmul_grouped", "dbf_grouped_workspace_bytes",
     "dbf_grouped_launch_count", "dbf_matmul_hostio_batch", "dbf_hostio_batch_workspace_bytes",
     "dbf_factorize", "dbf_factorize_workspace_bytes", "dbf_factorize_launch_count",
+    "dbf_factorize_weighted", "dbf_factorize_weighted_workspace_bytes", "dbf_factorize_weighted_launch_count",
 )
 
 
@@ -111,6 +112,10 @@ def _load():
                                vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "dbf_factorize_workspace_bytes": (sz, [i64, i64, i64]),
         "dbf_factorize_launch_count": (ci, [i64, i64, i64, ctypes.POINTER(DbfFactorizeParams)]),
+        "dbf_factorize_weighted": (ci, [vp, i64, i64, i64, ctypes.POINTER(DbfFactorizeParams),
+                                        vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "dbf_factorize_weighted_workspace_bytes": (sz, [i64, i64, i64]),
+        "dbf_factorize_weighted_launch_count": (ci, [i64, i64, i64, ctypes.POINTER(DbfFactorizeParams)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -464,16 +469,7 @@ def factorize_launch_count(N: int, M: int, k: int, outer: int, inner: int, power
     return int(_lib.dbf_factorize_launch_count(N, M, k, ctypes.byref(prm)))
 
 
-def factorize(W: torch.Tensor, a: torch.Tensor, A: torch.Tensor, m_left: torch.Tensor, m_right: torch.Tensor,
-              B: torch.Tensor, b: torch.Tensor, outer: int = 6, inner: int = 10, power_iters: int = 8,
-              rho_rel: float = 1.0, workspace: torch.Tensor | None = None, stream=None):
-    """Double binary factorization W ~ (a . A . m^T)(B . b^T), m = m_left . m_right (dbf_factorize).
-
-    W fp32 [N, M]; the left factor a fp32 [N], A int8 [N, k], m_left fp32 [k] and the
-    right factor m_right fp32 [k], B int8 [k, M], b fp32 [M] are device tensors updated
-    in place (the left factor is the start of the first step; the right one is fixed
-    in it).  Returns (a, A, m_left, m_right, B, b).
-    """
+def _check_factor_tensors(W, a, A, m_left, m_right, B, b):
     if W.dtype != torch.float32 or W.dim() != 2:
         raise ValueError("W must be fp32 [N, M]")
     N, M = W.shape
@@ -484,6 +480,51 @@ def factorize(W: torch.Tensor, a: torch.Tensor, A: torch.Tensor, m_left: torch.T
         if t.dtype != dt or tuple(t.shape) != sh or not t.is_contiguous() or t.device != W.device:
             raise ValueError("factors: a fp32 [N], A int8 [N, k], m_left fp32 [k], m_right fp32 [k], "
                              "B int8 [k, M], b fp32 [M], contiguous, on W's device")
+    return N, M, k
+
+
+def factorize_weighted_workspace_bytes(N: int, M: int, k: int) -> int:
+    return int(_lib.dbf_factorize_weighted_workspace_bytes(N, M, k))
+
+
+def factorize_weighted_launch_count(N: int, M: int, k: int, outer: int, inner: int, power_iters: int,
+                                    rho_rel: float) -> int:
+    prm = DbfFactorizeParams(outer, inner, power_iters, rho_rel)
+    return int(_lib.dbf_factorize_weighted_launch_count(N, M, k, ctypes.byref(prm)))
+
+
+def factorize_weighted(W: torch.Tensor, d_out: torch.Tensor, d_in: torch.Tensor, a: torch.Tensor,
+                       A: torch.Tensor, m_left: torch.Tensor, m_right: torch.Tensor, B: torch.Tensor,
+                       b: torch.Tensor, outer: int = 6, inner: int = 10, power_iters: int = 8,
+                       rho_rel: float = 1.0, workspace: torch.Tensor | None = None, stream=None):
+    """factorize with importance weights d_out fp32 [N], d_in fp32 [M] (dbf_factorize_weighted):
+    the error ||diag(d_out)(W - W_hat)diag(d_in)|| is minimised.  Factors updated in place."""
+    N, M, k = _check_factor_tensors(W, a, A, m_left, m_right, B, b)
+    for t, n in ((d_out, N), (d_in, M)):
+        if t.dtype != torch.float32 or tuple(t.shape) != (n,) or not t.is_contiguous() or t.device != W.device:
+            raise ValueError("d_out, d_in: contiguous fp32 [N], [M] on W's device")
+    W = W.contiguous()
+    prm = DbfFactorizeParams(outer, inner, power_iters, rho_rel)
+    if workspace is None:
+        workspace = new_workspace(max(factorize_weighted_workspace_bytes(N, M, k), 256), W.device)
+    rc = _lib.dbf_factorize_weighted(_ptr(W), N, M, k, ctypes.byref(prm), _ptr(d_out), _ptr(d_in), _ptr(a),
+                                     _ptr(A), _ptr(m_left), _ptr(m_right), _ptr(B), _ptr(b), _ptr(workspace),
+                                     workspace.numel(), _stream_handle(stream))
+    _check(rc, "dbf_factorize_weighted")
+    return a, A, m_left, m_right, B, b
+
+
+def factorize(W: torch.Tensor, a: torch.Tensor, A: torch.Tensor, m_left: torch.Tensor, m_right: torch.Tensor,
+              B: torch.Tensor, b: torch.Tensor, outer: int = 6, inner: int = 10, power_iters: int = 8,
+              rho_rel: float = 1.0, workspace: torch.Tensor | None = None, stream=None):
+    """Double binary factorization W ~ (a . A . m^T)(B . b^T), m = m_left . m_right (dbf_factorize).
+
+    W fp32 [N, M]; the left factor a fp32 [N], A int8 [N, k], m_left fp32 [k] and the
+    right factor m_right fp32 [k], B int8 [k, M], b fp32 [M] are device tensors updated
+    in place (the left factor is the start of the first step; the right one is fixed
+    in it).  Returns (a, A, m_left, m_right, B, b).
+    """
+    N, M, k = _check_factor_tensors(W, a, A, m_left, m_right, B, b)
     W = W.contiguous()
     prm = DbfFactorizeParams(outer, inner, power_iters, rho_rel)
     need = factorize_workspace_bytes(N, M, k)

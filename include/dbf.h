@@ -394,6 +394,35 @@ size_t dbf_factorize_workspace_bytes(int64_t N, int64_t M, int64_t k);
 /* Kernels one dbf_factorize call launches; -1 for arguments out of range. */
 int dbf_factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_params *params);
 
+/*
+ * dbf_factorize_weighted: the factorization with importance weights (the
+ * DBF page, section 2, Importancia de Entradas y Salidas: input activation
+ * norms and output gradient norms weight the approximation error), i.e.
+ * the same steps for the objective
+ *     || diag(d_out) (W - W_hat) diag(d_in) ||_F.
+ * Because diag(d_out) P and Q diag(d_in) keep the factored form, it runs
+ * dbf_factorize on W' = diag(d_out) W diag(d_in) from the start
+ * (d_out . a, A, m_left; m_right, B, b . d_in) and divides the weights out
+ * of a and b at the end.
+ *   d_out, d_in  device fp32 [N], [M], positive and finite; an entry that is
+ *                not leaves its scale unconverted and records
+ *                DBF_ERR_DEVICE_ARG for dbf_check_status
+ * Other arguments, limits and errors as dbf_factorize; the workspace is
+ * dbf_factorize_weighted_workspace_bytes(N, M, k) (W' after the plain
+ * scratch).  Unit weights give the bits of dbf_factorize.
+ */
+int dbf_factorize_weighted(const float *W, int64_t N, int64_t M, int64_t k, const dbf_factorize_params *params,
+                           const float *d_out, const float *d_in, float *a, int8_t *A, float *m_left,
+                           float *m_right, int8_t *B, float *b, void *workspace, size_t ws_bytes,
+                           void *stream);
+
+/* Device workspace (bytes) dbf_factorize_weighted needs; 0 for sizes out of range. */
+size_t dbf_factorize_weighted_workspace_bytes(int64_t N, int64_t M, int64_t k);
+
+/* Kernels one dbf_factorize_weighted call launches (dbf_factorize's + 5); -1 for
+ * arguments out of range. */
+int dbf_factorize_weighted_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_params *params);
+
 /* Human-readable text for a DBF_* code (static string). */
 const char *dbf_status_string(int code);
 

@@ -150,3 +150,26 @@ def test_factorize_sizes_and_launch_counts(lib):
     assert lib.factorize_launch_count(100, 80, k, 0, inner, q, 1.0) == 0
     assert lib.factorize_launch_count(100, 80, k, 1, 0, q, 1.0) == 0
     assert lib.factorize_launch_count(100, 80, 0, 1, 1, q, 1.0) == -1
+
+
+def test_factorize_weighted_host_checks(lib):
+    vp = ctypes.c_void_p
+    p = lib.DbfFactorizeParams(1, 2, 3, 1.0)
+
+    def call(d_out=FAKE + 0x9000, d_in=FAKE + 0xA000, ws_bytes=1 << 30, N=64, M=48, k=16):
+        return lib._lib.dbf_factorize_weighted(vp(FAKE), N, M, k, ctypes.byref(p), vp(d_out), vp(d_in),
+                                               vp(FAKE + 0x1000), vp(FAKE + 0x2000), vp(FAKE + 0x3000),
+                                               vp(FAKE + 0x4000), vp(FAKE + 0x5000), vp(FAKE + 0x6000),
+                                               vp(FAKE + 0x8000), ws_bytes, None)
+
+    assert call(d_out=0) == lib.DBF_ERR_INVALID_ARG
+    assert call(d_in=0) == lib.DBF_ERR_INVALID_ARG
+    assert call(d_in=FAKE + 0xA002) == lib.DBF_ERR_ALIGNMENT
+    assert call(N=70000) == lib.DBF_ERR_UNSUPPORTED
+    plain = lib.factorize_workspace_bytes(64, 48, 16)
+    weighted = lib.factorize_weighted_workspace_bytes(64, 48, 16)
+    assert weighted >= plain + 4 * 64 * 48 and weighted % 256 == 0
+    assert call(ws_bytes=plain) == lib.DBF_ERR_WORKSPACE
+    assert lib.factorize_weighted_launch_count(64, 48, 16, 2, 3, 4, 1.0) == \
+        lib.factorize_launch_count(64, 48, 16, 2, 3, 4, 1.0) + 5
+    assert lib.factorize_weighted_launch_count(64, 48, 16, 0, 3, 4, 1.0) == 0

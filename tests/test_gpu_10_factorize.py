@@ -177,6 +177,71 @@ def test_nan_in_the_fixed_factor_reports_a_numeric_status(cuda_lib):
     assert cuda_lib.status_string(cuda_lib.DBF_ERR_NUMERIC) != "unknown status"
 
 
+def _weights(N, M, seed):
+    g = np.random.default_rng(seed)
+    return (np.exp(0.5 * g.standard_normal(N)).astype(np.float32),
+            np.exp(0.5 * g.standard_normal(M)).astype(np.float32))
+
+
+def _run_weighted(cuda_lib, w, d_out, d_in, start, outer, inner, q, rho):
+    fs = _dev(start)
+    cuda_lib.factorize_weighted(torch.from_numpy(w).cuda(), torch.from_numpy(d_out).cuda(),
+                                torch.from_numpy(d_in).cuda(), *fs, outer=outer, inner=inner, power_iters=q,
+                                rho_rel=rho)
+    st = cuda_lib.check_status()
+    assert st == 0, cuda_lib.status_string(st)
+    return _host(fs)
+
+
+def test_unit_weights_give_the_plain_bits(cuda_lib):
+    N, M, k = 200, 136, 40
+    w = G.make_dense_weight(N, M, 31)
+    start = G.make_factorize_start(N, M, k, 31)
+    plain = _run(cuda_lib, w, start, 2, 3, 4, 1.0)
+    weighted = _run_weighted(cuda_lib, w, np.ones(N, np.float32), np.ones(M, np.float32), start, 2, 3, 4, 1.0)
+    for x, y in zip(plain, weighted):
+        assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("shape", [(200, 136, 40), (97, 300, 70), (300, 260, 130)])
+def test_weighted_factorization_matches_oracle(cuda_lib, shape):
+    # Same checks as the plain rounds, on the weighted objective; the first
+    # step's signs and scales are those of the scaled problem.
+    N, M, k = shape
+    seed = 7500 + N + k
+    w = G.make_dense_weight(N, M, seed)
+    d_out, d_in = _weights(N, M, seed)
+    start = G.make_factorize_start(N, M, k, seed)
+    got = _run_weighted(cuda_lib, w, d_out, d_in, start, 1, 1, 4, 1.0)
+    wp = d_out.astype(np.float64)[:, None] * w * d_in.astype(np.float64)[None, :]
+    sstart = (start[0] * d_out, start[1], start[2], start[3], start[4], start[5] * d_in)
+    scaled_got = [got[0] * d_out.astype(np.float64)] + list(got[1:5]) + [got[5] * d_in.astype(np.float64)]
+    _check_first_step(wp, sstart, scaled_got, 4)
+    want = FZ.factorize_weighted(w, d_out, d_in, start[:3], start[3:], 1, 1, 4, 1.0)
+    assert np.mean(got[1] == want[1]) >= 0.995 and np.mean(got[4] == want[4]) >= 0.995
+    eg = FZ.weighted_rel_error(w, d_out, d_in, *got)
+    ew = FZ.weighted_rel_error(w, d_out, d_in, *want)
+    assert abs(eg - ew) <= 5e-3 * ew, (eg, ew)
+    got = _run_weighted(cuda_lib, w, d_out, d_in, start, 2, 5, 6, 1.0)
+    want = FZ.factorize_weighted(w, d_out, d_in, start[:3], start[3:], 2, 5, 6, 1.0)
+    assert np.mean(got[1] == want[1]) >= 0.99 and np.mean(got[4] == want[4]) >= 0.99
+    eg = FZ.weighted_rel_error(w, d_out, d_in, *got)
+    ew = FZ.weighted_rel_error(w, d_out, d_in, *want)
+    assert abs(eg - ew) <= 5e-3 * ew, (eg, ew)
+
+
+def test_a_non_positive_weight_is_reported(cuda_lib):
+    N, M, k = 40, 36, 8
+    w = G.make_dense_weight(N, M, 8)
+    d_out, d_in = _weights(N, M, 8)
+    d_in[5] = 0.0
+    fs = _dev(G.make_factorize_start(N, M, k, 8))
+    cuda_lib.factorize_weighted(torch.from_numpy(w).cuda(), torch.from_numpy(d_out).cuda(),
+                                torch.from_numpy(d_in).cuda(), *fs, outer=1, inner=1, power_iters=2)
+    assert cuda_lib.check_status() == cuda_lib.DBF_ERR_DEVICE_ARG
+    assert cuda_lib.check_status() == 0
+
+
 def _balanced_fp16(a, m, b):
     # fp16 scales for the matmul: equalise the geometric means of alpha, beta
     # and gamma (their product per entry of W_hat is unchanged).
