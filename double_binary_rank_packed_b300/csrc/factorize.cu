@@ -30,7 +30,6 @@
 #include <algorithm>
 
 #include "common.cuh"
-#include "kernels.h"
 #include "factorize.h"
 
 namespace dbfk {
