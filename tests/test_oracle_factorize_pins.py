@@ -198,3 +198,30 @@ def test_weighting_input_columns_lowers_their_error():
         return np.sqrt(np.sum(d[:, heavy] ** 2) / np.sum(w[:, heavy] ** 2))
 
     assert col_err(weighted) < 0.8 * col_err(plain)
+
+
+def test_scalar_step_closed_form():
+    # n = 1, k = 1, p = 3, one iteration from Z = 0: rho = rho_rel |f|^2 (the
+    # mean diagonal of a 1 x 1 F F^T), P = t.f / ((1 + rho_rel) |f|^2), and
+    # SVID of a 1 x 1 matrix is exact: r = |P|, S = sign(P), c = 1.
+    t = np.array([[0.3, -1.2, 0.5]])
+    f = np.array([[2.0, 1.0, -0.5]])
+    for rho_rel in (0.25, 1.0, 3.0):
+        r, S, c = fz.admm_left(t, f, np.zeros(1), np.ones((1, 1), np.int8), np.zeros(1), 1, 3, rho_rel)
+        tf, ff = (t @ f.T).item(), (f @ f.T).item()
+        p = tf / ((1.0 + rho_rel) * ff)
+        assert r[0] == pytest.approx(abs(p), rel=1e-14)
+        assert S[0, 0] == (1 if p >= 0 else -1)
+        assert c[0] == pytest.approx(1.0, rel=1e-15)
+
+
+def test_rank_one_step_converges_to_least_squares():
+    # With k = 1 every n x 1 matrix is of the SVID form (r_i = |y_i|, c = 1),
+    # so the constraint is vacuous and ADMM must converge to the plain
+    # least-squares factor T F^T / (F F^T).
+    g = _rng(21)
+    t = g.standard_normal((7, 5))
+    f = g.standard_normal((1, 5))
+    r, S, c = fz.admm_left(t, f, np.zeros(7), np.ones((7, 1), np.int8), np.zeros(1), 200, 2, 1.0)
+    want = (t @ f.T) / (f @ f.T).item()
+    np.testing.assert_allclose(fz.svid_dense(r, S, c), want, rtol=1e-10, atol=1e-14)
