@@ -5,8 +5,11 @@ library.  PyTorch supplies device memory and the current stream.  Importing
 this module loads libdbf.so and fails loudly when it is missing; there is no
 fallback implementation.
 
-Names follow the C ABI in include/dbf.h: pack, unpack, workspace_bytes,
-matmul, matmul_path, matmul_hostio, matmul_segmented, check_status.
+Names follow the C ABI in include/dbf.h (dbf_<name>): pack, unpack,
+transpose_packed; matmul, matmul_path, matmul_decode_noalloc, matmul_hostio,
+matmul_hostio_batch, matmul_segmented, matmul_grouped; backward; factorize,
+factorize_weighted; the matching *_workspace_bytes and *_launch_count calls;
+check_status, status_string, last_cuda_error, selftest_bounded_wait.
 """
 
 from __future__ import annotations
