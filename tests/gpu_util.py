@@ -14,15 +14,37 @@ from oracle import dbf_oracle as O
 # this product): max|y - y_ref| <= 1e-2 * max|y_ref| and relative Frobenius
 # error <= 2e-3, y_ref the exact (float64) result.
 #
-# The exactly rounded bf16 result already carries a relative Frobenius error
-# of about 1.6e-3 (half an ulp of an 8-bit significand, RMS); on outputs of
-# only a few dozen elements that figure scatters above 2e-3 on its own.  So
-# the Frobenius bound is max(2e-3, floor + 5e-4), floor = the error of the
-# exactly rounded result, 5e-4 = the budget of the two fp16 intermediates
-# (2^-11 relative each, RMS 2.8e-4, added linearly).
+# Every output of at least SMALL_OUTPUT elements is held to those two bounds
+# as stated.  The exactly rounded bf16 result alone carries a relative
+# Frobenius error of about 1.6e-3 (half an ulp of an 8-bit significand, RMS),
+# and on outputs of only a few dozen elements that figure scatters above 2e-3
+# by itself (a 33 x 2 output: 2.36e-3 for the correctly rounded result).  Only
+# below SMALL_OUTPUT elements is the Frobenius bound max(2e-3, floor + 5e-4),
+# floor = the error of the exactly rounded result, 5e-4 = the budget of the
+# two fp16 intermediates (2^-11 relative each, RMS 2.8e-4, added linearly).
 MAX_REL_TOL = 1e-2
 FROB_TOL = 2e-3
 INTERMEDIATE_BUDGET = 5e-4
+SMALL_OUTPUT = 1000
+
+
+# Activation rows per tile that the prefill GEMMs can be launched with (the
+# launch picks one per GEMM from the shape); activation row t*ell + i holds
+# token t, term i, so a tile of BN rows spans BN / ell tokens.
+PREFILL_TILE_ROWS = (192, 224, 240, 256)
+
+
+def tile_boundary_tokens(T, ell):
+    """Token rows on both sides of every token-tile boundary of every prefill
+    tile layout, plus the first two and last two rows (sorted, unique)."""
+    rows = {0, 1, T - 2, T - 1}
+    for bn in PREFILL_TILE_ROWS:
+        if bn % ell:
+            continue
+        step = bn // ell
+        for b in range(step, T, step):
+            rows.update((b - 1, b))
+    return sorted(r for r in rows if 0 <= r < T)
 
 
 def dbf():
@@ -60,6 +82,8 @@ def errors(y_bits, y_ref):
 
 
 def frob_tolerance(y_ref):
+    if np.asarray(y_ref).size >= SMALL_OUTPUT:
+        return FROB_TOL
     floor = O.rel_frobenius(O.bf16_bits_to_f64(O.round_to_bf16_bits(y_ref)), y_ref)
     return max(FROB_TOL, floor + INTERMEDIATE_BUDGET)
 
@@ -68,6 +92,9 @@ def assert_close(y_bits, y_ref, what=""):
     assert np.isfinite(O.bf16_bits_to_f64(y_bits)).all(), f"{what}: non-finite output"
     max_rel, frob = errors(y_bits, y_ref)
     tol = frob_tolerance(y_ref)
+    # achieved errors go to the test log (pytest -s, or the captured output of a failure)
+    print(f"[parity] {what}: n={np.asarray(y_ref).size} max_rel={max_rel:.3e} frob={frob:.3e} "
+          f"(tol {MAX_REL_TOL:.0e} / {tol:.3e})")
     assert max_rel <= MAX_REL_TOL and frob <= tol, \
         f"{what}: max_rel={max_rel:.3e} frob={frob:.3e} (frob tol {tol:.3e})"
     return max_rel, frob

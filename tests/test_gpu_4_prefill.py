@@ -109,6 +109,6 @@ def test_dbf_mlp_full_size_sampled(cuda_lib, proj):
     got = run(cuda_lib, f, xb)
     y_all = O.bf16_bits_to_f64(got)
     assert np.isfinite(y_all).all()
-    toks = [0, 1, 127, 128, 1000, 2046, 2047]
+    toks = U.tile_boundary_tokens(T, p.ell)
     ref = O.y_sampled(O.bf16_bits_to_f64(xb), f, toks, np.arange(p.N))
     U.assert_close(got[toks], ref, f"dbf mlp {p.name} sampled rows")

@@ -75,7 +75,7 @@ def test_dx_mlp_up_projection_full_size_sampled(cuda_lib):
     dyb = G.make_x(T, p.N, p.seed + 7)
     got = _dx(cuda_lib, f, dyb, 2)
     assert np.isfinite(O.bf16_bits_to_f64(got)).all()
-    toks = [0, 1, 255, 256, 2047]
+    toks = U.tile_boundary_tokens(T, p.ell)
     # sampled rows: dx[t] = dy[t] dW (the dense update restricted to the needed rows is too large; use the
     # factored route on the sampled tokens only)
     dx = O.dx_factored(O.bf16_bits_to_f64(dyb[toks]), f)
