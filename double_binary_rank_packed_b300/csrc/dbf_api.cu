@@ -424,6 +424,19 @@ int run_backward(const dbf_factors *f, const dbf_factors *ft, const uint16_t *x,
 
 namespace dbfk {
 void set_last_error(const char *msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
+int check_matmul_args(const dbf_factors *f, const uint16_t *x, int64_t T, const uint16_t *y, int accumulate,
+                      int path) {
+    const int rc = check_factors(f);
+    if (rc) return rc;
+    if (T < 0 || (accumulate != 0 && accumulate != 1)) return DBF_ERR_INVALID_ARG;
+    if (path < DBF_PATH_AUTO || path > DBF_PATH_PREFILL) return DBF_ERR_INVALID_ARG;
+    if (T == 0) return DBF_OK;
+    if (T > (int64_t(1) << 26)) return DBF_ERR_UNSUPPORTED;
+    if (!x || !y) return DBF_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return DBF_ERR_ALIGNMENT;
+    return DBF_OK;
+}
 }  // namespace dbfk
 
 extern "C" {
@@ -514,14 +527,8 @@ size_t dbf_workspace_bytes(const dbf_factors *f, int64_t T) {
 
 int dbf_matmul_path(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *workspace,
                     size_t ws_bytes, void *stream, int path) {
-    int rc = check_factors(f);
-    if (rc) return rc;
-    if (T < 0 || (accumulate != 0 && accumulate != 1)) return DBF_ERR_INVALID_ARG;
-    if (path < DBF_PATH_AUTO || path > DBF_PATH_PREFILL) return DBF_ERR_INVALID_ARG;
-    if (T == 0) return DBF_OK;
-    if (T > (int64_t(1) << 26)) return DBF_ERR_UNSUPPORTED;
-    if (!x || !y) return DBF_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(y)) return DBF_ERR_ALIGNMENT;
+    const int rc = dbfk::check_matmul_args(f, x, T, y, accumulate, path);
+    if (rc != DBF_OK || T == 0) return rc;
     path = resolve_path(path, T);
     const size_t need = ws_for(f, T, path);
     if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;

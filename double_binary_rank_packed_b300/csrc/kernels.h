@@ -187,4 +187,9 @@ cudaError_t launch_selftest_wait(int *status, uint64_t limit_ns, cudaStream_t st
 // Text returned by dbf_last_cuda_error() on this thread.
 void set_last_error(const char *msg);
 
+// Host-side argument checks of dbf_matmul_path (no device work): DBF_OK or
+// the DBF_ERR_* code the call returns.  T = 0 passes (the call is a no-op).
+int check_matmul_args(const dbf_factors *f, const uint16_t *x, int64_t T, const uint16_t *y, int accumulate,
+                      int path);
+
 }  // namespace dbfk

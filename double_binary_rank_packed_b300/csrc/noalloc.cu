@@ -1,24 +1,25 @@
 // dbf_matmul_decode_noalloc: the decode-path product for callers that cannot
 // hand the library any device scratch memory.
 //
-// Some callers have no way to allocate: code running while a CUDA graph is
-// being captured (cudaMalloc is not a stream operation and cannot be
-// recorded), latency-critical serving loops where cudaMalloc's implicit
-// device synchronisation is not acceptable, and runtimes whose device memory
-// is planned up front in a fixed arena with nothing left to lend.  For them
-// this entry point keeps the decode kernels' only scratch buffer (the fp16
-// intermediate V, ell*T rows of round_up(R, 64) halves) in a file-scope
-// device array of fixed size.  The caller still passes x, y and the factors.
+// Some callers have no way to allocate device memory for a call: serving
+// loops that must never take cudaMalloc's implicit device synchronisation on
+// the token path, runtimes whose device memory is one arena planned at
+// start-up with nothing left to lend, and plug-in hosts that pass a library
+// only its inputs and outputs.  For them this entry point runs the decode
+// path of dbf_matmul (the same kernels, chosen the same way) with its
+// workspace -- the fp16 intermediate V of the two-stage kernels, ell*T rows of
+// round_up(R, 64) halves -- in a file-scope device array of fixed size.  The
+// caller still passes x, y and the factors.  The papers have no counterpart:
+// this is a deployment variant, not a step of the method.
 //
 // The array is a static __device__ object: every GPU that loads this library
 // holds its kNoAllocScratchBytes until the process exits.  In host code the
 // name g_noalloc_scratch only stands for the symbol, it is not a device
 // address; the address is looked up once per device with
-// cudaGetSymbolAddress (on the first call made on that device) and then
-// passed to the kernels.
+// cudaGetSymbolAddress (on the first call made on that device, with that
+// device current) and then handed to the kernels as their workspace.
 #include <stdio.h>
 
-#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -39,85 +40,51 @@ std::mutex g_scratch_mutex;
 void *scratch_for_current_device(cudaError_t *err) {
     int dev = 0;
     *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
     if (!g_scratch_addr[dev]) {
         void *p = nullptr;
         *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (*err != cudaSuccess || !p) return nullptr;
+        if (*err != cudaSuccess || !p) {
+            if (*err == cudaSuccess) *err = cudaErrorInvalidSymbol;
+            cudaGetLastError();  // leave no error behind for the caller's next launch check
+            return nullptr;
+        }
         g_scratch_addr[dev] = p;
     }
     return g_scratch_addr[dev];
 }
 
-inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
-
 }  // namespace
 
 extern "C" int dbf_matmul_decode_noalloc(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
                                          int accumulate, void *stream) {
-    using namespace dbfk;
-    if (!f) return DBF_ERR_INVALID_ARG;
-    if (f->N < 1 || f->M < 1 || f->R < 1 || f->ell < 1 || f->ell > 4) return DBF_ERR_INVALID_ARG;
-    if (!f->B1 || !f->B2 || !f->alpha || !f->beta || !f->gamma) return DBF_ERR_INVALID_ARG;
-    if (f->ldw1 < ceil_div(f->R, 32) || f->ldw2 < ceil_div(f->M, 32)) return DBF_ERR_INVALID_ARG;
-    if (!aligned16(f->B1) || !aligned16(f->B2) || !aligned16(f->alpha) || !aligned16(f->beta) ||
-        !aligned16(f->gamma))
-        return DBF_ERR_ALIGNMENT;
-    if (T < 0 || (accumulate != 0 && accumulate != 1)) return DBF_ERR_INVALID_ARG;
-    if (T == 0) return DBF_OK;
-    if (!x || !y) return DBF_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(y)) return DBF_ERR_ALIGNMENT;
-
-    // scratch needed by the decode kernels: V [ell*T][round_up(R, 64)] fp16
-    const int64_t ldv = round_up(f->R, 64);
-    const double need = double(f->ell) * double(T) * double(ldv) * 2.0;
-    if (need > double(kNoAllocScratchBytes)) {
-        set_last_error("dbf_matmul_decode_noalloc: ell*T*round_up(R,64)*2 bytes of scratch exceed the "
-                       "2 MiB static array");
+    // the argument checks of dbf_matmul_path, so both entry points reject the same calls with the same codes
+    const int rc = dbfk::check_matmul_args(f, x, T, y, accumulate, DBF_PATH_DECODE);
+    if (rc != DBF_OK || T == 0) return rc;
+    const size_t need = dbf_workspace_bytes_path(f, T, DBF_PATH_DECODE);
+    if (need > kNoAllocScratchBytes) {
+        char msg[200];
+        snprintf(msg, sizeof(msg),
+                 "dbf_matmul_decode_noalloc: %zu bytes of scratch (ell*T*round_up(R,64)*2) exceed the 2 MiB "
+                 "static array",
+                 need);
+        dbfk::set_last_error(msg);
         return DBF_ERR_WORKSPACE;
     }
-
     cudaError_t err = cudaSuccess;
     void *scratch = scratch_for_current_device(&err);
     if (!scratch) {
-        set_last_error("dbf_matmul_decode_noalloc: cudaGetSymbolAddress of the static scratch failed");
-        return DBF_ERR_CUDA;
-    }
-
-    // the two-stage decode kernels of dbf_matmul's decode path, with V in the static array
-    int sms = 148;
-    {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 148;
-    }
-    DecodeCall c = {};
-    c.f = f;
-    c.N = f->N;
-    c.M = f->M;
-    c.R = f->R;
-    c.ell = f->ell;
-    c.T = static_cast<int>(T);
-    c.tokens_per_problem = static_cast<int>(T);
-    c.x = reinterpret_cast<const __nv_bfloat16 *>(x);
-    c.y = reinterpret_cast<__nv_bfloat16 *>(y);
-    c.accumulate = accumulate;
-    c.status = nullptr;
-    err = launch_decode_two_stage(c, static_cast<__half *>(scratch), static_cast<int>(ldv), sms,
-                                  static_cast<cudaStream_t>(stream));
-    if (err == cudaErrorNotSupported) {
-        set_last_error("dbf_matmul_decode_noalloc: no decode tile plan fits this shape");
-        return DBF_ERR_UNSUPPORTED;
-    }
-    if (err != cudaSuccess) {
         char msg[200];
-        snprintf(msg, sizeof(msg), "dbf_matmul_decode_noalloc: %s", cudaGetErrorString(err));
-        set_last_error(msg);
+        snprintf(msg, sizeof(msg), "dbf_matmul_decode_noalloc: cudaGetSymbolAddress of the static scratch: %s",
+                 cudaGetErrorString(err));
+        dbfk::set_last_error(msg);
         return DBF_ERR_CUDA;
     }
-    return DBF_OK;
+    // the decode path of dbf_matmul_path: the same argument checks, kernels and device status word
+    return dbf_matmul_path(f, x, T, y, accumulate, scratch, kNoAllocScratchBytes, stream, DBF_PATH_DECODE);
 }

@@ -232,10 +232,15 @@ int dbf_decode_max_tokens(void);
  *   x          device bf16 [T][M] row-major, 16-byte aligned
  *   y          device bf16 [T][N] row-major, 16-byte aligned
  *   accumulate 0: y = branch;  1: y = bf16(y + branch) (y read, then written)
- * Arithmetic: fp32 accumulation of the sign sums, intermediates fp32
- * (decode) or fp16 (prefill), one round-to-nearest-even to bf16 at the end.
+ * Arithmetic (both kernel paths): gamma_i * x is formed in fp32 and rounded
+ * once to fp16; the sign sums u = B2 (gamma_i * x) accumulate in fp32;
+ * beta_i * u is formed in fp32 and rounded once to fp16; the sums
+ * B1 (beta_i * u) accumulate in fp32; sum_i alpha_i * (...) (+ y) is formed
+ * in fp32 and rounded once to bf16 (round to nearest even).
  * Preconditions: |gamma_i * x| and |beta_i * u| stay below 65504 (fp16 range
- * of the intermediates).
+ * of the intermediates).  Integer inputs (integer x, unit scales) give the
+ * exactly rounded result only while |x| <= 2048 and |u| <= 2048, the range
+ * in which fp16 holds every integer; |y| needs no bound beyond fp32's 2^24.
  */
 int dbf_matmul(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
                int accumulate, void *workspace, size_t ws_bytes, void *stream);
@@ -312,25 +317,29 @@ int dbf_check_status(void *stream);
 int dbf_selftest_bounded_wait(int64_t limit_us, void *stream);
 
 /*
- * dbf_matmul_decode_noalloc: the decode-path dbf_matmul for callers that
- * cannot allocate device memory -- code recording a CUDA graph (cudaMalloc
- * cannot be captured), serving loops that must not take cudaMalloc's
- * implicit device synchronisation, and runtimes whose device memory is a
- * fixed, pre-planned arena.  The papers have no counterpart; this is a
- * deployment variant of the same two decode kernels.
+ * dbf_matmul_decode_noalloc: dbf_matmul_path(..., DBF_PATH_DECODE) for
+ * callers that cannot allocate device memory for a call: serving loops that
+ * must never take cudaMalloc's implicit device synchronisation on the token
+ * path, runtimes whose device memory is one arena planned at start-up, and
+ * plug-in hosts that hand a library only its inputs and outputs.  The papers
+ * have no counterpart; this is a deployment variant of the decode path.
  *   Arguments as dbf_matmul (f, x, T, y, accumulate, stream); no workspace.
+ *   Result: bit for bit the result of dbf_matmul_path with DBF_PATH_DECODE
+ *   (the same argument checks, kernels and device status word).
  *   Scratch: a 2 MiB static device array inside the library, held by every
  *   GPU that loads the library until the process exits.  Calls needing more
- *   than 2 MiB (ell * T * round_up(R, 64) * 2 bytes) are rejected with
+ *   than 2 MiB (dbf_workspace_bytes_path(f, T, DBF_PATH_DECODE), i.e.
+ *   ell * T * round_up(R, 64) * 2 bytes rounded up to 256) are rejected with
  *   DBF_ERR_WORKSPACE before any device work, with the reason in
  *   dbf_last_cuda_error().
- *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, no allocation); make that first call before any
- *   stream capture.
+ *   The first call on each device (with that device current) looks up the
+ *   array's device address (cudaGetSymbolAddress, no allocation); make that
+ *   first call before any stream capture.
  *   Every call shares the one array and the array keeps the last call's
- *   contents; the kernels overwrite every element they read, so nothing
- *   needs clearing, but calls that overlap on the GPU (concurrent streams,
- *   or several host threads on one device) race on it: serialise them.
+ *   contents; the kernels write every element of it they read before reading
+ *   it, so nothing needs clearing, but calls that overlap on the GPU
+ *   (concurrent streams, or several host threads on one device) race on it:
+ *   serialise them.
  *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 int dbf_matmul_decode_noalloc(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,

@@ -173,3 +173,29 @@ def test_factorize_weighted_host_checks(lib):
     assert lib.factorize_weighted_launch_count(64, 48, 16, 2, 3, 4, 1.0) == \
         lib.factorize_launch_count(64, 48, 16, 2, 3, 4, 1.0) + 5
     assert lib.factorize_weighted_launch_count(64, 48, 16, 0, 3, 4, 1.0) == 0
+
+
+def test_noalloc_host_checks_match_the_workspace_entry_point(lib):
+    """dbf_matmul_decode_noalloc rejects what dbf_matmul_path rejects, with the same codes,
+    before any device work (shape limits included)."""
+    fn = lib._lib.dbf_matmul_decode_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(lib.DbfFactors), ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                   ctypes.c_int, ctypes.c_void_p]
+
+    def call(f, x=FAKE + 0x5000, T=4, y=FAKE + 0x6000, acc=0):
+        return fn(ctypes.byref(f) if f is not None else None, ctypes.c_void_p(x), T, ctypes.c_void_p(y), acc, None)
+
+    for f, kw in [(None, {}), (_factors(lib, ell=0), {}), (_factors(lib, N=0), {}), (_factors(lib, ldw2=1), {}),
+                  (_factors(lib, base=FAKE + 4), {}), (_factors(lib), {"x": FAKE + 2}), (_factors(lib), {"y": 0}),
+                  (_factors(lib), {"T": -1}), (_factors(lib), {"acc": 2}),
+                  (_factors(lib, N=(1 << 24) + 1), {}), (_factors(lib, M=(1 << 24) + 1), {}),
+                  (_factors(lib, R=(1 << 20) + 1), {})]:
+        want = _call(lib, f, path=lib.PATH_DECODE, **kw)
+        assert want != lib.DBF_OK
+        assert call(f, **kw) == want
+    assert call(_factors(lib, N=(1 << 24) + 1)) == lib.DBF_ERR_UNSUPPORTED
+    assert call(_factors(lib), T=0, x=0, y=0) == lib.DBF_OK
+    # more than the 2 MiB static array: ell * T * round_up(R, 64) * 2 = 4 * 64 * 4160 * 2 bytes
+    assert call(_factors(lib, N=64, M=64, R=4150, ell=4), T=64) == lib.DBF_ERR_WORKSPACE
+    assert "2 MiB" in lib.last_cuda_error()
