@@ -15,6 +15,8 @@ check_status, status_string, last_cuda_error, selftest_bounded_wait.
 from __future__ import annotations
 
 import ctypes
+import functools
+import inspect
 import os
 
 import torch
@@ -149,6 +151,27 @@ def _stream_handle(stream=None):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _on_stream(fn):
+    """Run a wrapper with the caller's `stream` as torch's current stream.
+
+    The tensors a wrapper makes itself (workspace, contiguous copies, outputs)
+    are then allocated, filled and released on the stream the library works
+    on, so the caching allocator cannot hand their memory to other work while
+    the kernels may still use it, and copies are ordered before the kernels.
+    """
+    sig = inspect.signature(fn)
+
+    @functools.wraps(fn)
+    def wrapped(*args, **kwargs):
+        stream = sig.bind(*args, **kwargs).arguments.get("stream")
+        if stream is None:
+            return fn(*args, **kwargs)
+        with torch.cuda.stream(stream):
+            return fn(*args, **kwargs)
+
+    return wrapped
+
+
 def _ptr(t) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
@@ -159,6 +182,7 @@ def words_per_row(cols: int) -> int:
 
 # ------------------------------------------------------------------ packing
 
+@_on_stream
 def pack(signs: torch.Tensor, ldw: int | None = None, stream=None) -> torch.Tensor:
     """Pack a device int8 sign matrix [rows, cols] into uint32 words [rows, ldw] (dbf_pack)."""
     if signs.dtype != torch.int8 or signs.dim() != 2 or not signs.is_cuda:
@@ -172,6 +196,7 @@ def pack(signs: torch.Tensor, ldw: int | None = None, stream=None) -> torch.Tens
     return words
 
 
+@_on_stream
 def unpack(words: torch.Tensor, cols: int, stream=None) -> torch.Tensor:
     """Inverse of pack: int8 +1/-1 [rows, cols] (dbf_unpack)."""
     rows, ldw = words.shape
@@ -180,6 +205,7 @@ def unpack(words: torch.Tensor, cols: int, stream=None) -> torch.Tensor:
     return signs
 
 
+@_on_stream
 def transpose_packed(words: torch.Tensor, cols: int, ldw_t: int | None = None, stream=None) -> torch.Tensor:
     """Packed transpose of a rows x cols packed sign matrix (dbf_transpose_packed)."""
     rows, ldw = words.shape
@@ -270,6 +296,7 @@ def new_workspace(nbytes: int, device) -> torch.Tensor:
 
 # ------------------------------------------------------------------ matmul
 
+@_on_stream
 def matmul_path(f: PackedFactors, x: torch.Tensor, y: torch.Tensor | None = None, accumulate: bool = False,
                 workspace: torch.Tensor | None = None, path: int = PATH_AUTO, stream=None) -> torch.Tensor:
     """y = sum_i alpha_i . B1 (beta_i . (B2 (gamma_i . x))) for x bf16 [T, M] (dbf_matmul_path)."""
@@ -299,6 +326,7 @@ def backward_workspace_bytes(f: PackedFactors, T: int) -> int:
     return int(_lib.dbf_backward_workspace_bytes(ctypes.byref(f.struct), T))
 
 
+@_on_stream
 def backward(f: PackedFactors, ft: "TransposedFactors", x: torch.Tensor, dy: torch.Tensor, dx: bool = True,
              workspace: torch.Tensor | None = None, stream=None, out=None):
     """dx, dalpha, dbeta, dgamma of L = sum_t <dy_t, y_t> (dbf_backward).
@@ -355,6 +383,7 @@ def grouped_launch_count(fs, T: int) -> int:
     return int(_lib.dbf_grouped_launch_count(_group_structs(fs), len(fs), T))
 
 
+@_on_stream
 def matmul_grouped(fs, xs, ys=None, accumulate: bool = False, workspace: torch.Tensor | None = None, stream=None):
     """ys[p] = product of fs[p] applied to xs[p] for G independent projections (dbf_matmul_grouped).
 
@@ -388,6 +417,7 @@ def hostio_workspace_bytes(f: PackedFactors, T: int) -> int:
     return int(_lib.dbf_hostio_workspace_bytes(ctypes.byref(f.struct), T))
 
 
+@_on_stream
 def matmul_hostio(f: PackedFactors, x_host: torch.Tensor, y_host: torch.Tensor, accumulate: bool = False,
                   workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Host (pinned) bf16 x [T, M] in, host bf16 y [T, N] out (dbf_matmul_hostio); asynchronous."""
@@ -404,6 +434,7 @@ def hostio_batch_workspace_bytes(fs, T: int) -> int:
     return int(_lib.dbf_hostio_batch_workspace_bytes(_group_structs(fs), len(fs), T))
 
 
+@_on_stream
 def matmul_hostio_batch(fs, xs_host, ys_host, accumulate: bool = False, workspace: torch.Tensor | None = None,
                         stream=None):
     """L independent host-io calls, copies overlapped with the kernels (dbf_matmul_hostio_batch).
@@ -445,6 +476,7 @@ def segmented_workspace_bytes(N, M, R, ell, T, S) -> int:
     return int(_lib.dbf_segmented_workspace_bytes(N, M, R, ell, T, S))
 
 
+@_on_stream
 def matmul_segmented(table: torch.Tensor, n_adapters: int, N: int, M: int, R: int, ell: int, x: torch.Tensor,
                      seg_offsets: torch.Tensor, seg_adapter: torch.Tensor, y: torch.Tensor | None = None,
                      accumulate: bool = False, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
@@ -496,6 +528,7 @@ def factorize_weighted_launch_count(N: int, M: int, k: int, outer: int, inner: i
     return int(_lib.dbf_factorize_weighted_launch_count(N, M, k, ctypes.byref(prm)))
 
 
+@_on_stream
 def factorize_weighted(W: torch.Tensor, d_out: torch.Tensor, d_in: torch.Tensor, a: torch.Tensor,
                        A: torch.Tensor, m_left: torch.Tensor, m_right: torch.Tensor, B: torch.Tensor,
                        b: torch.Tensor, outer: int = 6, inner: int = 10, power_iters: int = 8,
@@ -517,6 +550,7 @@ def factorize_weighted(W: torch.Tensor, d_out: torch.Tensor, d_in: torch.Tensor,
     return a, A, m_left, m_right, B, b
 
 
+@_on_stream
 def factorize(W: torch.Tensor, a: torch.Tensor, A: torch.Tensor, m_left: torch.Tensor, m_right: torch.Tensor,
               B: torch.Tensor, b: torch.Tensor, outer: int = 6, inner: int = 10, power_iters: int = 8,
               rho_rel: float = 1.0, workspace: torch.Tensor | None = None, stream=None):
@@ -555,6 +589,7 @@ _lib.dbf_matmul_decode_noalloc.argtypes = [ctypes.POINTER(DbfFactors), ctypes.c_
                                            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
 
 
+@_on_stream
 def matmul_decode_noalloc(f: PackedFactors, x: torch.Tensor, y: torch.Tensor | None = None,
                           accumulate: bool = False, stream=None) -> torch.Tensor:
     """Decode-path product with the library's static scratch (dbf_matmul_decode_noalloc).
