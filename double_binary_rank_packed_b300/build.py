@@ -17,8 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libdbf.so")
-SOURCES = ["dbf_api.cu", "decode.cu", "prefill.cu", "misc.cu", "noalloc.cu", "factorize.cu"]
-HEADERS = ["common.cuh", "kernels.h", "factorize.h"]
+SOURCES = ["dbf_api.cu", "decode.cu", "decode_rs.cu", "prefill.cu", "misc.cu", "noalloc.cu", "factorize.cu"]
+HEADERS = ["common.cuh", "decode_frag.cuh", "kernels.h", "factorize.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

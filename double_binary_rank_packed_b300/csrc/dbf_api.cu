@@ -192,6 +192,37 @@ dbfk::FusedPlan fused_plan_for(int N, int M, int R, int ell, int64_t tokens, int
                             accumulate);
 }
 
+dbfk::RsPlan rs_plan_for(int N, int M, int R, int ell, int64_t tokens, int problems, bool accumulate) {
+    return dbfk::plan_rs(N, M, R, ell, static_cast<int>(decode_columns(ell, tokens)), num_sms(), problems,
+                         accumulate);
+}
+
+dbfk::RsArgs rs_args(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate,
+                     const dbfk::RsPlan &p) {
+    dbfk::RsArgs a = {};
+    a.B1 = f->B1;
+    a.B2 = f->B2;
+    a.ldw1 = f->ldw1;
+    a.ldw2 = f->ldw2;
+    a.alpha = reinterpret_cast<const __half *>(f->alpha);
+    a.beta = reinterpret_cast<const __half *>(f->beta);
+    a.gamma = reinterpret_cast<const __half *>(f->gamma);
+    a.N = f->N;
+    a.M = f->M;
+    a.R = f->R;
+    a.ell = f->ell;
+    a.T = static_cast<int>(T);
+    a.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    a.accumulate = accumulate;
+    a.C = p.C;
+    a.Wc = p.Wc;
+    a.RW = p.RW;
+    a.IPW = p.IPW;
+    a.status = status_ptr();
+    return a;
+}
+
 int map_launch_error(cudaError_t e, const char *where) {
     if (e == cudaErrorNotSupported) {
         snprintf(g_last_error, sizeof(g_last_error), "%s: no decode tile plan fits this shape", where);
@@ -200,11 +231,17 @@ int map_launch_error(cudaError_t e, const char *where) {
     return cuda_fail(e, where);
 }
 
-// decode path: the one-launch fused kernel when R is small and its plan fits,
-// else the two stages (x -> V, V -> y) through the workspace
+// decode path: one launch when R is small (the reduce-scatter kernel, else the
+// all-to-all fused kernel), else the two stages (x -> V, V -> y) through the
+// workspace
 int run_decode(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate, void *ws,
                cudaStream_t stream) {
     using namespace dbfk;
+    const RsPlan rp = rs_plan_for(f->N, f->M, f->R, f->ell, T, 1, accumulate != 0);
+    if (rp.CT != 0) {
+        cudaError_t e = launch_decode_rs(false, rp, rs_args(f, x, T, y, accumulate, rp), 1, stream);
+        return e == cudaSuccess ? DBF_OK : cuda_fail(e, "decode");
+    }
     const FusedPlan fp = fused_plan_for(f->N, f->M, f->R, f->ell, T, 1, accumulate != 0);
     if (fp.CT != 0) {
         cudaError_t e = launch_decode_fused(false, fp, fused_args(f, x, T, y, accumulate, fp), 1, stream, true);
@@ -894,13 +931,26 @@ int dbf_matmul_segmented(const dbf_factors *d_adapters, int32_t n_adapters, int3
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     const int64_t tok = segment_tokens(T, S);
+    dbf_factors shape = {};
+    shape.N = N;
+    shape.M = M;
+    shape.R = R;
+    shape.ell = ell;
+    // routed batches: the reduce-scatter kernel is planned per segment and
+    // measured slower there (70.6 against 22.6 us per 256-token batch of 64
+    // adapters), so only a batch of one segment takes it
+    const RsPlan rp = S == 1 ? rs_plan_for(N, M, R, ell, tok, S, accumulate != 0) : RsPlan{};
+    if (rp.CT != 0) {
+        RsArgs ra = rs_args(&shape, x, T, y, accumulate, rp);
+        ra.seg_off = d_seg_offsets;
+        ra.seg_ad = d_seg_adapter;
+        ra.adapters = d_adapters;
+        ra.n_adapters = n_adapters;
+        cudaError_t e = launch_decode_rs(true, rp, ra, S, s);
+        return e == cudaSuccess ? DBF_OK : cuda_fail(e, "segmented decode");
+    }
     FusedPlan p = fused_plan_for(N, M, R, ell, tok, S, accumulate != 0);
     if (p.CT != 0) {
-        dbf_factors shape = {};
-        shape.N = N;
-        shape.M = M;
-        shape.R = R;
-        shape.ell = ell;
         FusedArgs fa = fused_args(&shape, x, T, y, accumulate, p);
         fa.seg_off = d_seg_offsets;
         fa.seg_ad = d_seg_adapter;
@@ -935,11 +985,13 @@ int dbf_launch_count(const dbf_factors *f, int64_t T, int path) {
     if (path < DBF_PATH_AUTO || path > DBF_PATH_PREFILL) return 0;
     path = resolve_path(path, T);
     if (path == DBF_PATH_PREFILL) return 3;
+    if (rs_plan_for(f->N, f->M, f->R, f->ell, T, 1, false).CT != 0) return 1;
     return fused_plan_for(f->N, f->M, f->R, f->ell, T, 1, false).CT != 0 ? 1 : 2;
 }
 
 int dbf_segmented_launch_count(int32_t N, int32_t M, int32_t R, int32_t ell, int64_t T, int32_t S) {
     if (check_dims(N, M, R, ell) != DBF_OK || T <= 0 || S <= 0) return 0;
+    if (S == 1 && rs_plan_for(N, M, R, ell, segment_tokens(T, S), S, false).CT != 0) return 1;
     return fused_plan_for(N, M, R, ell, segment_tokens(T, S), S, false).CT != 0 ? 1 : 2;
 }
 

@@ -102,6 +102,36 @@ cudaError_t launch_decode_fused(bool segmented, const FusedPlan &plan, const Fus
 cudaError_t launch_decode_stage(int stage, bool segmented, const DecPlan &plan, const DecArgs &args,
                                 int grid_y, cudaStream_t stream, bool pdl);
 
+// One-launch decode with a reduce-scatter / all-gather cluster exchange
+// (decode_rs.cu), for R <= 128 and ell in {1, 2, 4}.
+struct RsArgs {
+    const uint32_t *B1, *B2;
+    int ldw1, ldw2;
+    const __half *alpha, *beta, *gamma;
+    int N, M, R, ell, T;
+    const __nv_bfloat16 *x;
+    __nv_bfloat16 *y;
+    int accumulate;
+    int C;    // cluster size (stage-1 split of M)
+    int Wc;   // stage-1 packed words per CTA
+    int RW;   // stage-2 output rows per CTA
+    int IPW;  // stage-2 items (16 rows x 8 columns) per warp
+    const int32_t *seg_off;
+    const int32_t *seg_ad;
+    const dbf_factors *adapters;
+    int n_adapters;
+    int *status;
+};
+
+struct RsPlan {
+    int CT, RB1, NW, C, RW, IPW, Wc, grid_x;  // CT = 0: no plan
+    size_t smem;
+};
+
+RsPlan plan_rs(int N, int M, int R, int ell, int columns, int num_sms, int problems, bool accumulate);
+cudaError_t launch_decode_rs(bool segmented, const RsPlan &plan, const RsArgs &args, int grid_y,
+                             cudaStream_t stream);
+
 // One decode call (f set, seg_off null) or a routed batch of S segments
 // (f null; seg_off, seg_ad, adapters set) for the two-stage kernels.
 struct DecodeCall {
