@@ -61,6 +61,7 @@ def parse_args(argv=None):
                     help="cap on calls per step (small profiling runs; breaks the > 4x L2 rule)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-io end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--no-single", action="store_true", help="skip the cold-L2 single-call latency leg")
     return ap.parse_args(argv)
 
 
@@ -276,6 +277,9 @@ class DecodeWorkload:
     def run_eager(self):
         for l in range(self.L):
             self.dbf.matmul(self.factors[l], self.x[l], self.y[l], workspace=self.ws)
+
+    def call_one(self, l):
+        self.dbf.matmul(self.factors[l], self.x[l], self.y[l], workspace=self.ws)
 
     def footprint_per_step(self):
         return self.L * self.fp_call
@@ -497,12 +501,15 @@ class GroupedWorkload:
 
     def run_eager(self):
         for l in range(self.L):
-            x = self.x[l]
-            if self.separate:
-                for pf, y in zip(self.groups[l], self.y[l]):
-                    self.dbf.matmul(pf, x, y, workspace=self.ws)
-            else:
-                self.dbf.matmul_grouped(self.groups[l], [x, x, x], self.y[l], workspace=self.ws)
+            self.call_one(l)
+
+    def call_one(self, l):
+        x = self.x[l]
+        if self.separate:
+            for pf, y in zip(self.groups[l], self.y[l]):
+                self.dbf.matmul(pf, x, y, workspace=self.ws)
+        else:
+            self.dbf.matmul_grouped(self.groups[l], [x, x, x], self.y[l], workspace=self.ws)
 
     capture = DecodeWorkload.capture
     step = DecodeWorkload.step
@@ -558,9 +565,12 @@ class SegmentedWorkload:
 
     def run_eager(self):
         for l in range(self.L):
-            ads, table = self.pools[l]
-            self.dbf.matmul_segmented(table, len(ads), self.N, self.M, self.R, self.ell, self.x[l], self.off,
-                                      self.ad, self.y[l], workspace=self.ws)
+            self.call_one(l)
+
+    def call_one(self, l):
+        ads, table = self.pools[l]
+        self.dbf.matmul_segmented(table, len(ads), self.N, self.M, self.R, self.ell, self.x[l], self.off,
+                                  self.ad, self.y[l], workspace=self.ws)
 
     def footprint_per_step(self):
         return self.L * self.fp_call
@@ -674,6 +684,39 @@ def measure_e2e(dbf, wl, steps):
             "path": "dbf_matmul_hostio_batch (pinned host x and y, the step's calls pipelined)"}
 
 
+# ------------------------------------------------ single-call latency, cold L2
+
+SINGLE_CALLS = 50
+
+
+def measure_single_call(wl, peaks, calls=SINGLE_CALLS):
+    """Latency of one call with nothing of it in L2: before each call a buffer of twice the L2
+    size is written (so every input comes from HBM), then CUDA events on the stream bracket the
+    one call (the flush kernel runs long enough for the host to enqueue the call behind it, so
+    the events time the device alone).  Median over `calls` calls on distinct factor sets."""
+    import torch
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(calls + 3):
+        flush.fill_(i & 0xFF)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        wl.call_one(i % wl.L)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1))
+    del flush
+    ms = statistics.median(times)
+    r = roofline_obj(wl, ms, peaks, None)
+    return {"protocol": f"cold L2: {2 * L2_BYTES // (1 << 20)} MiB written before each call, CUDA events "
+                        f"around one call, median of {calls}",
+            "us_per_call": round(ms * 1e3, 3), "tokens_per_s": round(wl.T / (ms * 1e-3), 1),
+            "roofline_frac": r["frac"], "roofline_achieved": r["achieved"], "roofline_unit": r["unit"]}
+
+
 # ----------------------------------------------------------- CPU oracle timing
 
 def oracle_threads():
@@ -703,6 +746,86 @@ def time_oracle(seconds=10.0, min_calls=2):
     return {"value": round(n * T / el, 2), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
             "sample": f"{n} oracle calls (fp64 numpy, factored route) on one N=M=4096 R=64 ell=1 factor set, "
                       f"T={T} tokens each, {el:.1f} s"}
+
+
+def _timed(fn, seconds, min_calls=1, max_calls=1000):
+    fn()  # warm
+    n = 0
+    t0 = time.perf_counter()
+    while n < min_calls or (time.perf_counter() - t0 < seconds and n < max_calls):
+        fn()
+        n += 1
+    return n, time.perf_counter() - t0
+
+
+def time_oracle_workload(key, seconds=2.0):
+    """The fp64 oracle as it stands on one workload, on the host cores: the factored route
+    (y_factored, what the library computes) for every workload, and the dense route (dW built,
+    then x dW^T) for the three single-projection decode workloads; the MLP in prefill on a
+    seeded 64-token subset (one call per projection); the routed batch as one call of the
+    segmented oracle.  Returns {"factored": ..., "dense": ...} of cpu_baseline objects."""
+    from oracle import dbf_oracle as O
+    cores = oracle_threads()
+    name, _, tok = key.rpartition("_T")
+    T = int(tok) if tok.isdigit() else 0
+    out = {}
+
+    def obj(tokens, n, el, route, sample):
+        return {"value": round(tokens * n / el, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "route": route, "sample": f"{n} oracle calls (fp64 numpy), {sample}, {el:.2f} s"}
+
+    if name in ("adapter4k", "dbf1p5", "tiny", "adapter4k_dx"):
+        w = {"adapter4k": CFG.ADAPTER_4K, "adapter4k_dx": CFG.ADAPTER_4K, "dbf1p5": CFG.DBF_1P5,
+             "tiny": CFG.TINY}[name]
+        p = w.projections[0]
+        f = G.make_factors(p.N, p.M, p.R, p.ell, p.seed, p.sign_mode, p.scale_mode)
+        if name == "adapter4k_dx":
+            dyb = G.make_x(T, p.N, p.seed + 7)
+            n, el = _timed(lambda: O.matmul_dx(dyb, f), seconds)
+            out["factored"] = obj(T, n, el, "factored (dx = dy dW)", f"{key}, T={T}")
+            return out
+        xb = G.make_x(T, p.M, p.seed, outlier_scale=w.outlier_scale)
+        n, el = _timed(lambda: O.matmul(xb, f), seconds)
+        out["factored"] = obj(T, n, el, "factored", f"{key}, T={T}")
+        x64 = O.bf16_bits_to_f64(xb)
+        n, el = _timed(lambda: O.round_to_bf16_bits(O.y_dense(x64, f)), seconds, max_calls=50)
+        out["dense"] = obj(T, n, el, "dense (dW = sum_i diag(alpha_i) B1 diag(beta_i) B2 diag(gamma_i), "
+                                     "then x dW^T)", f"{key}, T={T}")
+        return out
+    if name == "multiadapter":
+        w = CFG.MULTI_ADAPTER
+        fs = [G.make_factors(p.N, p.M, p.R, p.ell, p.seed) for p in w.projections]
+        off, ad, _ = G.make_routing(w.tokens[0], w.n_adapters, w.routing_seed)
+        xb = G.make_x(w.tokens[0], fs[0].B2.shape[1], w.routing_seed)
+        n, el = _timed(lambda: O.matmul_segmented(xb, fs, off, ad), seconds)
+        out["factored"] = obj(w.tokens[0], n, el, "factored, per segment", f"{key}, {len(ad)} segments")
+        return out
+    if name in ("dbfmlp", "dbfmlp_dx"):
+        sub = 64
+        tot_n, tot_el = 0, 0.0
+        for p in CFG.DBF_MLP.projections:
+            f = G.make_factors(p.N, p.M, p.R, p.ell, p.seed)
+            if name == "dbfmlp":
+                xb = G.make_x(sub, p.M, p.seed)
+                n, el = _timed(lambda: O.matmul(xb, f), 0.0)
+            else:
+                dyb = G.make_x(sub, p.N, p.seed + 7)
+                n, el = _timed(lambda: O.matmul_dx(dyb, f), 0.0)
+            tot_n, tot_el = n, tot_el + el / n
+            del f
+        # tokens/s of one call per projection, as the GPU line counts them
+        out["factored"] = {"value": round(sub * 2 / tot_el, 2), "unit": "tokens/s", "cores": cores,
+                           "kind": "oracle", "route": "factored" + (" (dx = dy dW)" if name == "dbfmlp_dx" else ""),
+                           "sample": f"seeded {sub}-token subset of the 2048 tokens (first {sub} rows of the "
+                                     f"same draw), one oracle call per projection, {tot_el:.2f} s"}
+        return out
+    if name in ("dbfqkv", "dbfqkv_sep"):
+        fs = [G.make_factors(N, M, R, 1, 6000 + k) for k, (N, M, R) in enumerate(QKV_SHAPES)]
+        xb = G.make_x(T, 4096, 6010)
+        n, el = _timed(lambda: O.matmul_grouped([xb, xb, xb], fs), seconds)
+        out["factored"] = obj(T, n, el, "factored, three projections", f"{key}, T={T}")
+        return out
+    return out
 
 
 def run_reference(args):
@@ -865,8 +988,14 @@ def main(argv=None):
 
     if rank == 0 and not args.no_e2e and isinstance(head, DecodeWorkload):
         line["e2e"] = measure_e2e(dbf, head, max(3, min(args.steps, 10)))
+    if rank == 0 and hasattr(head, "call_one") and not args.no_single:
+        line["single_call"] = measure_single_call(head, peaks)
+        line["roofline"]["protocol"] = "streamed: one CUDA graph of distinct calls, PDL, per-call = step / calls"
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = time_oracle()
+        extra = time_oracle_workload(head.key)
+        if "dense" in extra:
+            line["cpu_baseline_dense"] = extra["dense"]
 
     if world == 1 and not args.no_also:
         also = []
@@ -890,6 +1019,14 @@ def main(argv=None):
             d = workload_line(wl, ms_w / args.steps, args.steps, peaks)
             d["clocks"] = s2.summary()
             d["gpu_launches"] = args.steps * wl.calls * wl.launches_per_call
+            if hasattr(wl, "call_one") and not args.no_single:
+                d["single_call"] = measure_single_call(wl, peaks)
+            if not args.no_cpu:
+                cb = time_oracle_workload(key)
+                if "factored" in cb:
+                    d["cpu_baseline"] = cb["factored"]
+                if "dense" in cb:
+                    d["cpu_baseline_dense"] = cb["dense"]
             also.append(d)
             del wl
             torch.cuda.empty_cache()
