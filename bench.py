@@ -689,30 +689,48 @@ def measure_e2e(dbf, wl, steps):
 SINGLE_CALLS = 50
 
 
-def measure_single_call(wl, peaks, calls=SINGLE_CALLS):
-    """Latency of one call with nothing of it in L2: before each call a buffer of twice the L2
-    size is written (so every input comes from HBM), then CUDA events on the stream bracket the
-    one call (the flush kernel runs long enough for the host to enqueue the call behind it, so
-    the events time the device alone).  Median over `calls` calls on distinct factor sets."""
+def measure_single_call(wl, peaks, calls=SINGLE_CALLS, reps=5):
+    """Latency of one call with nothing of it in L2.  Two CUDA graphs are replayed: one holds
+    `calls` x [write a buffer of twice the L2 size, one call] (so every input of every call
+    comes from HBM), the other the same writes alone; the difference of their device times
+    (CUDA events), divided by `calls`, is the cold latency of one call -- the device's event
+    timer ticks in ~1 us steps, too coarse for a single call.  Median over `reps` replays."""
     import torch
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.current_stream()
-    times = []
-    for i in range(calls + 3):
-        flush.fill_(i & 0xFF)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        wl.call_one(i % wl.L)
-        e1.record(stream)
+    graphs = []
+    for with_call in (True, False):
+        for i in range(min(calls, wl.L)):  # eager warm-up of every call the graph holds
+            if with_call:
+                wl.call_one(i % wl.L)
         torch.cuda.synchronize()
-        if i >= 3:
-            times.append(e0.elapsed_time(e1))
-    del flush
-    ms = statistics.median(times)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(calls):
+                flush.fill_(i & 0xFF)
+                if with_call:
+                    wl.call_one(i % wl.L)
+        torch.cuda.synchronize()
+        graphs.append(g)
+    per = []
+    for _ in range(reps + 1):
+        t = []
+        for g in graphs:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1))
+        per.append((t[0] - t[1]) / calls)
+    del graphs, flush
+    torch.cuda.empty_cache()
+    ms = statistics.median(per[1:])
     r = roofline_obj(wl, ms, peaks, None)
-    return {"protocol": f"cold L2: {2 * L2_BYTES // (1 << 20)} MiB written before each call, CUDA events "
-                        f"around one call, median of {calls}",
+    return {"protocol": f"cold L2: {2 * L2_BYTES // (1 << 20)} MiB written before each call; device time of "
+                        f"{calls} x (write + call) minus {calls} x (write), per call, median of {reps} graph replays",
             "us_per_call": round(ms * 1e3, 3), "tokens_per_s": round(wl.T / (ms * 1e-3), 1),
             "roofline_frac": r["frac"], "roofline_achieved": r["achieved"], "roofline_unit": r["unit"]}
 
