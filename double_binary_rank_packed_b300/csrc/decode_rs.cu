@@ -40,8 +40,9 @@ namespace dbfk {
 
 namespace {
 
-constexpr int kRsThreads = 256;
-constexpr int kRsWarps = kRsThreads / 32;
+// Partials of stage 1 are kept per group of 8 warps along K (kKGroups); with 16
+// warps per CTA the two halves of the warps split the row blocks of u.
+constexpr int kKGroups = 8;
 
 __host__ __device__ inline size_t rs_align16(size_t v) { return (v + 15) & ~size_t(15); }
 
@@ -53,20 +54,20 @@ struct RsSmem {
 };
 
 // R2 = round_up(R, 32) rows of u, CPAD = 8*CT columns per chunk, NW words of
-// B2 per warp, IPW stage-2 items per warp.
-__host__ __device__ inline RsSmem rs_smem(int CPAD, int R2, int NW, int RW, int IPW, int ell) {
+// B2 per K group, WARPS warps per CTA, IPW stage-2 items per warp.
+__host__ __device__ inline RsSmem rs_smem(int CPAD, int R2, int NW, int RW, int IPW, int ell, int WARPS) {
     RsSmem L;
     size_t o = 0;
-    L.part = o;  // [8 warps][R2][CPAD] fp32 stage-1 partials
-    o += size_t(kRsWarps) * R2 * CPAD * 4;
+    L.part = o;  // [8 K groups][R2][CPAD] fp32 stage-1 partials
+    o += size_t(kKGroups) * R2 * CPAD * 4;
     L.rs = o;  // [2 buffers][C][R2/C][CPAD] fp32 partials received as owner
     o += size_t(2) * R2 * CPAD * 4;
     L.vs = o;  // [2 buffers][CPAD][R2 + 8] fp16 v in perm8 order
     o += rs_align16(size_t(2) * CPAD * (R2 + 8) * 2);
-    L.fa = o;  // [warp][NW][R2/16][8][32] stage-1 A fragments
-    o += size_t(kRsWarps) * NW * (R2 / 16) * 8 * 32 * 4;
+    L.fa = o;  // [K group][NW][R2/16][8][32] stage-1 A fragments (each warp owns its row blocks)
+    o += size_t(kKGroups) * NW * (R2 / 16) * 8 * 32 * 4;
     L.fb = o;  // [warp][IPW][R2/32][8][32] stage-2 A fragments
-    o += size_t(kRsWarps) * IPW * (R2 / 32) * 8 * 32 * 4;
+    o += size_t(WARPS) * IPW * (R2 / 32) * 8 * 32 * 4;
     L.alp = o;  // [ell][RW] fp16
     o += rs_align16(size_t(ell) * RW * 2);
     L.bet = o;  // [ell][R2] fp16, zero past R
@@ -81,9 +82,13 @@ __device__ __forceinline__ void wait_or_flag(uint64_t *bar, uint32_t parity, int
     if (!mbar_wait_bounded(bar, parity, nullptr)) record_status(status, DBF_ERR_TIMEOUT);
 }
 
-template <int CT, int RB1, int NW, bool SEG>
-__global__ void __launch_bounds__(kRsThreads, 2) dec_rs_kernel(const RsArgs a) {
+template <int CT, int RB1, int NW, bool SEG, int WARPS>
+__global__ void __launch_bounds__(32 * WARPS, WARPS == 8 ? 2 : 1) dec_rs_kernel(const RsArgs a) {
     constexpr int CPAD = 8 * CT, C4 = CPAD / 4, R2 = 16 * RB1, LDV = R2 + 8, KW2 = R2 / 32;
+    constexpr int kRsThreads = 32 * WARPS, kRsWarps = WARPS;
+    constexpr int RH = WARPS / kKGroups;  // row-block halves of stage 1
+    constexpr int RBH = RB1 / RH;         // row blocks of u per warp
+    static_assert(RB1 % RH == 0, "row blocks split evenly over the warp halves");
     extern __shared__ __align__(128) unsigned char smem[];
     // the next call's CTAs may start their own preparation at once
     pdl_trigger();
@@ -93,7 +98,7 @@ __global__ void __launch_bounds__(kRsThreads, 2) dec_rs_kernel(const RsArgs a) {
     const int ROWN = R2 / C;  // perm8 positions of u each CTA owns
     const int rank = static_cast<int>(cluster_ctarank());
     const int ell = a.ell, N = a.N, M = a.M, R = a.R;
-    const RsSmem L = rs_smem(CPAD, R2, NW, RW, IPW, ell);
+    const RsSmem L = rs_smem(CPAD, R2, NW, RW, IPW, ell, WARPS);
     float *part = reinterpret_cast<float *>(smem + L.part);
     float *rsb = reinterpret_cast<float *>(smem + L.rs);
     __half *vsb = reinterpret_cast<__half *>(smem + L.vs);
@@ -149,7 +154,8 @@ __global__ void __launch_bounds__(kRsThreads, 2) dec_rs_kernel(const RsArgs a) {
     const int Kw1 = (M + 31) >> 5;
     const int w0 = rank * a.Wc;
     const int Wslice = max(0, min(a.Wc, Kw1 - w0));
-    const int wb = min(Wslice, warp * NW), we = min(Wslice, wb + NW);
+    const int kg = warp % kKGroups, rh = warp / kKGroups;  // K group, row-block half
+    const int wb = min(Wslice, kg * NW), we = min(Wslice, wb + NW);
     int ctok[CT], cterm[CT];
 #pragma unroll
     for (int ct = 0; ct < CT; ++ct) {
@@ -165,14 +171,15 @@ __global__ void __launch_bounds__(kRsThreads, 2) dec_rs_kernel(const RsArgs a) {
         const int wl = wb + w;
         const bool wok = wl < we;
 #pragma unroll
-        for (int rb = 0; rb < RB1; ++rb) {
+        for (int rbl = 0; rbl < RBH; ++rbl) {
+            const int rb = rh * RBH + rbl;
             const int r0 = 16 * rb + g;
             const uint32_t lo = (wok && r0 < R) ? __ldg(B2 + size_t(r0) * ldw2 + w0 + wl) : 0u;
             const uint32_t hi = (wok && r0 + 8 < R) ? __ldg(B2 + size_t(r0 + 8) * ldw2 + w0 + wl) : 0u;
             uint32_t pa[4], pv[4];
             sign_pairs8(lo, c, pa);
             sign_pairs8(hi, c, pv);
-            uint32_t *fp = fa_s + ((warp * NW + w) * RB1 + rb) * 256 + lane;
+            uint32_t *fp = fa_s + ((kg * NW + w) * RB1 + rb) * 256 + lane;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 fp[32 * j] = (r0 < R) ? pa[j] : 0u;  // rows past R contribute nothing
@@ -277,9 +284,9 @@ __global__ void __launch_bounds__(kRsThreads, 2) dec_rs_kernel(const RsArgs a) {
                 else
                     xr[w][ct] = make_uint4(0u, 0u, 0u, 0u);
             }
-        float acc[RB1][CT][4];
+        float acc[RBH][CT][4];
 #pragma unroll
-        for (int rb = 0; rb < RB1; ++rb) zero_acc<CT>(acc[rb]);
+        for (int rbl = 0; rbl < RBH; ++rbl) zero_acc<CT>(acc[rbl]);
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
             if (wb + w >= we) break;
@@ -287,29 +294,29 @@ __global__ void __launch_bounds__(kRsThreads, 2) dec_rs_kernel(const RsArgs a) {
 #pragma unroll
             for (int ct = 0; ct < CT; ++ct) x_pairs(xr[w][ct], gv[w][ct], bx[ct]);
 #pragma unroll
-            for (int rb = 0; rb < RB1; ++rb) {
-                const uint32_t *fp = fa_s + ((warp * NW + w) * RB1 + rb) * 256 + lane;
+            for (int rbl = 0; rbl < RBH; ++rbl) {
+                const uint32_t *fp = fa_s + ((kg * NW + w) * RB1 + rh * RBH + rbl) * 256 + lane;
                 // fragment registers j = 0..3: row g, k pairs; 4..7: row g + 8
 #pragma unroll
                 for (int kh = 0; kh < 2; ++kh)
 #pragma unroll
                     for (int ct = 0; ct < CT; ++ct)
-                        mma_16816_nv(acc[rb][ct], fp[32 * (2 * kh)], fp[32 * (4 + 2 * kh)], fp[32 * (2 * kh + 1)],
+                        mma_16816_nv(acc[rbl][ct], fp[32 * (2 * kh)], fp[32 * (4 + 2 * kh)], fp[32 * (2 * kh + 1)],
                                      fp[32 * (5 + 2 * kh)], bx[ct][2 * kh], bx[ct][2 * kh + 1]);
             }
         }
 #pragma unroll
-        for (int rb = 0; rb < RB1; ++rb)
-            put_frag<CT>(smem_u32(part) + 4u * static_cast<uint32_t>((warp * R2 + 16 * rb) * CPAD), CPAD, acc[rb],
-                         lane, false, 0);
+        for (int rbl = 0; rbl < RBH; ++rbl)
+            put_frag<CT>(smem_u32(part) + 4u * static_cast<uint32_t>((kg * R2 + 16 * (rh * RBH + rbl)) * CPAD), CPAD,
+                         acc[rbl], lane, false, 0);
         __syncthreads();
 
-        // ---- reduce-scatter: the 8 warp parts in warp order, each row to its owner
+        // ---- reduce-scatter: the 8 K-group parts in order, each row to its owner
         for (int e = tid; e < R2 * C4; e += kRsThreads) {
             const int r = e / C4, q4 = e - r * C4;
             float4 u = *reinterpret_cast<const float4 *>(part + r * CPAD + 4 * q4);
 #pragma unroll
-            for (int wq = 1; wq < kRsWarps; ++wq)
+            for (int wq = 1; wq < kKGroups; ++wq)
                 add4(u, *reinterpret_cast<const float4 *>(part + (wq * R2 + r) * CPAD + 4 * q4));
             const int pos = perm8_pos(r);
             const int owner = pos / ROWN, lp = pos - owner * ROWN;
@@ -402,10 +409,10 @@ __global__ void __launch_bounds__(kRsThreads, 2) dec_rs_kernel(const RsArgs a) {
     // thread), so no peer can write into this CTA's shared memory after it exits.
 }
 
-template <int CT, int RB1, int NW, bool SEG>
+template <int CT, int RB1, int NW, bool SEG, int WARPS>
 cudaError_t launch_rs_one(const RsPlan &plan, const RsArgs &args, int grid_y, cudaStream_t stream) {
     static int configured_smem = 0;
-    auto kern = dec_rs_kernel<CT, RB1, NW, SEG>;
+    auto kern = dec_rs_kernel<CT, RB1, NW, SEG, WARPS>;
     if (plan.smem > 48 * 1024 && static_cast<int>(plan.smem) > configured_smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(plan.smem));
@@ -422,7 +429,7 @@ cudaError_t launch_rs_one(const RsPlan &plan, const RsArgs &args, int grid_y, cu
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid_x, grid_y, 1);
-    cfg.blockDim = dim3(kRsThreads, 1, 1);
+    cfg.blockDim = dim3(32 * WARPS, 1, 1);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -442,10 +449,14 @@ cudaError_t launch_rs_one(const RsPlan &plan, const RsArgs &args, int grid_y, cu
     return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
+// 8 warps per CTA: 16 (the two halves splitting the row blocks of u) measured
+// slower on B300 at every tile shape tried (adapter N=M=4096, R=64, T=16: 4.21 us
+// at best against 3.89)
 template <int CT, int RB1, bool SEG>
 cudaError_t launch_rs_nw(const RsPlan &plan, const RsArgs &args, int grid_y, cudaStream_t stream) {
-    return plan.NW == 1 ? launch_rs_one<CT, RB1, 1, SEG>(plan, args, grid_y, stream)
-                        : launch_rs_one<CT, RB1, 2, SEG>(plan, args, grid_y, stream);
+    if (plan.WARPS != 8) return cudaErrorInvalidValue;
+    return plan.NW == 1 ? launch_rs_one<CT, RB1, 1, SEG, 8>(plan, args, grid_y, stream)
+                        : launch_rs_one<CT, RB1, 2, SEG, 8>(plan, args, grid_y, stream);
 }
 
 // (CT, RB1) pairs with RB1 * CT <= 8 (the stage-1 accumulators stay in registers)
@@ -503,15 +514,18 @@ RsPlan plan_rs(int N, int M, int R, int ell, int columns, int num_sms, int probl
     const int Wc = (Kw1 + C - 1) / C;
     double best_cost = 1e300;
     for (int RW = 32; RW <= 128; RW *= 2) {
+        const int WARPS = 8;
         const int items = (RW / 16) * CT;
-        const int IPW = (items + kRsWarps - 1) / kRsWarps;
+        const int IPW = (items + WARPS - 1) / WARPS;
         if (IPW > 2) continue;
         const int used = (N + RW - 1) / RW;
         const int grid = ((used + C - 1) / C) * C;
-        const size_t smem = rs_smem(CPAD, R2, NW, RW, IPW, ell).total;
+        const size_t smem = rs_smem(CPAD, R2, NW, RW, IPW, ell, WARPS).total;
         if (smem > 200 * 1024) continue;
         const double ctas = double(grid) * problems;
-        const double cost = problems > 1 ? ctas : std::abs(ctas - 64.0) + (ctas < 64.0 ? 0.5 * RW : 0.0);
+        // one column tile: half the CTAs (measured at T = 1: 32 CTAs 3.00 us, 64 CTAs 3.12 us)
+        const double aim = CT == 1 ? 32.0 : 64.0;
+        const double cost = problems > 1 ? ctas : std::abs(ctas - aim) + (ctas < aim ? 0.5 * RW : 0.0);
         if (cost < best_cost) {
             best_cost = cost;
             best.CT = CT;
@@ -520,12 +534,17 @@ RsPlan plan_rs(int N, int M, int R, int ell, int columns, int num_sms, int probl
             best.C = C;
             best.RW = RW;
             best.IPW = IPW;
+            best.WARPS = WARPS;
             best.Wc = Wc;
             best.grid_x = grid;
             best.smem = smem;
         }
     }
     return best;
+}
+
+size_t rs_smem_bytes(int CT, int RB1, int NW, int RW, int IPW, int ell, int WARPS) {
+    return rs_smem(8 * CT, 16 * RB1, NW, RW, IPW, ell, WARPS).total;
 }
 
 cudaError_t launch_decode_rs(bool segmented, const RsPlan &plan, const RsArgs &args, int grid_y,

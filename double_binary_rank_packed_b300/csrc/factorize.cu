@@ -602,11 +602,13 @@ cudaError_t launch_factorize_weighted(const float *W, int N, int M, int k, const
     fz_scale_vec_kernel<<<cdiv(M, 256), 256, 0, s>>>(b, d_in, M, 0, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if ((e = launch_factorize(Wp, N, M, k, p, a, A, m_left, m_right, B, b, workspace, status, s)) != cudaSuccess)
-        return e;
+    const cudaError_t ef = launch_factorize(Wp, N, M, k, p, a, A, m_left, m_right, B, b, workspace, status, s);
+    // divide the weights out again, also after a failed launch inside (a launch error that leaves
+    // the context usable still lets these run); the first error is the one returned
     fz_scale_vec_kernel<<<cdiv(N, 256), 256, 0, s>>>(a, d_out, N, 1, status);
     fz_scale_vec_kernel<<<cdiv(M, 256), 256, 0, s>>>(b, d_in, M, 1, status);
-    return cudaGetLastError();
+    const cudaError_t ed = cudaGetLastError();
+    return ef != cudaSuccess ? ef : ed;
 }
 
 cudaError_t launch_factorize(const float *W, int N, int M, int k, const dbf_factorize_params &p, float *a,

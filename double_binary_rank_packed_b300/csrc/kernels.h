@@ -124,11 +124,12 @@ struct RsArgs {
 };
 
 struct RsPlan {
-    int CT, RB1, NW, C, RW, IPW, Wc, grid_x;  // CT = 0: no plan
+    int CT, RB1, NW, C, RW, IPW, WARPS, Wc, grid_x;  // CT = 0: no plan; WARPS: 8 or 16 per CTA
     size_t smem;
 };
 
 RsPlan plan_rs(int N, int M, int R, int ell, int columns, int num_sms, int problems, bool accumulate);
+size_t rs_smem_bytes(int CT, int RB1, int NW, int RW, int IPW, int ell, int WARPS);
 cudaError_t launch_decode_rs(bool segmented, const RsPlan &plan, const RsArgs &args, int grid_y,
                              cudaStream_t stream);
 

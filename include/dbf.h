@@ -419,6 +419,10 @@ int dbf_factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factor
  * Other arguments, limits and errors as dbf_factorize; the workspace is
  * dbf_factorize_weighted_workspace_bytes(N, M, k) (W' after the plain
  * scratch).  Unit weights give the bits of dbf_factorize.
+ * After an error return (DBF_ERR_CUDA from a launch), a, A, m_left,
+ * m_right, B and b are undefined: the weights are divided back out of a and
+ * b on that path too when the context still accepts launches, but the
+ * rounds may have stopped part-way.
  */
 int dbf_factorize_weighted(const float *W, int64_t N, int64_t M, int64_t k, const dbf_factorize_params *params,
                            const float *d_out, const float *d_in, float *a, int8_t *A, float *m_left,
