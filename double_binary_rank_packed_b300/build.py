@@ -1,6 +1,7 @@
 """Build libdbf.so (all CUDA kernels and the C ABI) in-tree for sm_103a.
 
 Usage: python -m double_binary_rank_packed_b300.build [--force] [--debug]
+(--debug builds libdbf_debug.so, the library with the kernels' bounds checks)
 Needs nvcc (CUDA 13) on PATH or under /usr/local/cuda/bin; no GPU is needed
 to compile.
 """
@@ -17,6 +18,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libdbf.so")
+# the debug build (bounds checks in the kernels, see in_range in csrc/common.cuh)
+LIB_DEBUG = os.path.join(HERE, "libdbf_debug.so")
 SOURCES = ["dbf_api.cu", "decode.cu", "decode_rs.cu", "prefill.cu", "misc.cu", "noalloc.cu", "factorize.cu"]
 HEADERS = ["common.cuh", "decode_frag.cuh", "kernels.h", "factorize.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -39,16 +42,19 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
 def build(force: bool = False, debug: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not debug and up_to_date():
-        return LIB
+    """Build libdbf.so (or, with debug=True, libdbf_debug.so: the same library with the kernels'
+    bounds checks compiled in) unless it is newer than every source; return its path."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
     nvcc = nvcc_path()
     flags = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-shared",
              "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")] + ARCH
@@ -56,7 +62,7 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False, ptxas
         flags += ["-DDBF_DEBUG=1"]
     if ptxas_info:
         flags += ["-Xptxas", "-v"]
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc] + flags + [os.path.join(CSRC, s) for s in SOURCES] + ["-o", tmp]
     if verbose:
         print(" ".join(cmd))
@@ -65,8 +71,8 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False, ptxas
         raise RuntimeError("nvcc failed:\n" + r.stdout + r.stderr)
     if ptxas_info or verbose:
         sys.stderr.write(r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None):

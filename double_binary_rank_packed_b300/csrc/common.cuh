@@ -32,6 +32,19 @@ __device__ __forceinline__ void record_status(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// Bounds checks of the debug build (-DDBF_DEBUG=1): in_range() records
+// DBF_ERR_BOUNDS in the status word when an index the kernels compute falls
+// outside the buffer it addresses, and the caller skips that access.  In the
+// release build it is the constant true and the checks compile away.
+#ifdef DBF_DEBUG
+__device__ __forceinline__ bool in_range(bool ok, int *status) {
+    if (!ok) record_status(status, DBF_ERR_BOUNDS);
+    return ok;
+}
+#else
+__device__ __forceinline__ bool in_range(bool, int *) { return true; }
+#endif
+
 // Default limit of every bounded wait: 1 s of wall-clock time.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 

@@ -489,6 +489,7 @@ const char *dbf_status_string(int code) {
         case DBF_ERR_TIMEOUT: return "device wait timed out";
         case DBF_ERR_DEVICE_ARG: return "device-side argument out of range";
         case DBF_ERR_NUMERIC: return "non-positive pivot in the factorization's Cholesky step";
+        case DBF_ERR_BOUNDS: return "index out of range in a kernel (debug build): the access was skipped";
         default: return "unknown status";
     }
 }

@@ -488,12 +488,14 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
                 const float d0 = d[2 * hh], d1 = d[2 * hh + 1];
                 const bool row_ok = nl < nrows2;
                 __nv_bfloat16 *yrow = a.y + size_t(t0 + tc0) * N + row_base + nl;
+                // (debug build) every token row written is a row of y
+                auto y_ok = [&](int t) { return in_range(t0 + tc0 + t < a.T && row_base + nl < N, a.status); };
                 if (ell == 1) {
                     const float al = row_ok ? __half2float(alp_s[nl]) : 0.f;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int t = 8 * ct + 2 * c + e;
-                        if (row_ok && t < ntok) {
+                        if (row_ok && t < ntok && y_ok(t)) {
                             float o = al * (e ? d1 : d0);
                             if (acc_mode) o += __bfloat162float(yst[t * RW + nl]);
                             yrow[size_t(t) * N] = __float2bfloat16_rn(o);
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
                     }
                 } else if (ell == 2) {
                     const int t = 4 * ct + c;
-                    if (row_ok && t < ntok) {
+                    if (row_ok && t < ntok && y_ok(t)) {
                         float o = __half2float(alp_s[nl]) * d0 + __half2float(alp_s[RW + nl]) * d1;
                         if (acc_mode) o += __bfloat162float(yst[t * RW + nl]);
                         yrow[size_t(t) * N] = __float2bfloat16_rn(o);
@@ -512,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
                                      : 0.f;
                     o += __shfl_xor_sync(0xffffffffu, o, 1);
                     const int t = 2 * ct + (c >> 1);
-                    if ((c & 1) == 0 && row_ok && t < ntok) {
+                    if ((c & 1) == 0 && row_ok && t < ntok && y_ok(t)) {
                         if (acc_mode) o += __bfloat162float(yst[t * RW + nl]);
                         yrow[size_t(t) * N] = __float2bfloat16_rn(o);
                     }
@@ -842,6 +844,8 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
                 const int i = col % ell;
                 const float v0 = __half2float(sc_s[i * RWS + rown0 + rl]) * u0;
                 const float v1 = __half2float(sc_s[i * RWS + rown0 + rl + 4]) * u1;
+                if (!in_range(vrow0 + col < size_t(a.T) * ell && (r & ~7) + 2 * (r & 3) + 1 < a.ldv, a.status))
+                    continue;
                 *reinterpret_cast<__half2 *>(a.V + (vrow0 + col) * a.ldv + (r & ~7) + 2 * (r & 3)) =
                     __floats2half2_rn(v0, v1);
             }
@@ -866,6 +870,7 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
                     s0 += __bfloat162float(yst[t * RWS + rown0 + rl]);
                     if (two) s1 += __bfloat162float(yst[t * RWS + rown0 + rl + 1]);
                 }
+                if (!in_range(t0 + tc0 + t < a.T && n + (two ? 1 : 0) < a.ldy, a.status)) continue;
                 __nv_bfloat16 *yp = a.y + size_t(t0 + tc0 + t) * a.ldy + n;
                 if (pairs_ok && two) {
                     *reinterpret_cast<__nv_bfloat162 *>(yp) = __floats2bfloat162_rn(s0, s1);

@@ -174,8 +174,9 @@ __global__ void __launch_bounds__(32 * WARPS, WARPS == 8 ? 2 : 1) dec_rs_kernel(
         for (int rbl = 0; rbl < RBH; ++rbl) {
             const int rb = rh * RBH + rbl;
             const int r0 = 16 * rb + g;
-            const uint32_t lo = (wok && r0 < R) ? __ldg(B2 + size_t(r0) * ldw2 + w0 + wl) : 0u;
-            const uint32_t hi = (wok && r0 + 8 < R) ? __ldg(B2 + size_t(r0 + 8) * ldw2 + w0 + wl) : 0u;
+            const bool wrd = wok && in_range(w0 + wl < ldw2, a.status);
+            const uint32_t lo = (wrd && r0 < R) ? __ldg(B2 + size_t(r0) * ldw2 + w0 + wl) : 0u;
+            const uint32_t hi = (wrd && r0 + 8 < R) ? __ldg(B2 + size_t(r0 + 8) * ldw2 + w0 + wl) : 0u;
             uint32_t pa[4], pv[4];
             sign_pairs8(lo, c, pa);
             sign_pairs8(hi, c, pv);
@@ -211,8 +212,9 @@ __global__ void __launch_bounds__(32 * WARPS, WARPS == 8 ? 2 : 1) dec_rs_kernel(
         const int n0 = row_base + 16 * (it % RB2) + g;
 #pragma unroll
         for (int w = 0; w < KW2; ++w) {
-            const uint32_t lo = (n0 < N) ? __ldg(B1 + size_t(n0) * ldw1 + w) : 0u;
-            const uint32_t hi = (n0 + 8 < N) ? __ldg(B1 + size_t(n0 + 8) * ldw1 + w) : 0u;
+            const bool wrd = in_range(w < ldw1, a.status);
+            const uint32_t lo = (wrd && n0 < N) ? __ldg(B1 + size_t(n0) * ldw1 + w) : 0u;
+            const uint32_t hi = (wrd && n0 + 8 < N) ? __ldg(B1 + size_t(n0 + 8) * ldw1 + w) : 0u;
             uint32_t pa[4], pv[4];
             sign_pairs8(lo, c, pa);
             sign_pairs8(hi, c, pv);
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(32 * WARPS, WARPS == 8 ? 2 : 1) dec_rs_kernel(
 #pragma unroll
             for (int ct = 0; ct < CT; ++ct) {
                 const int col = 8 * ct + g;
-                if (wb + w < we && col < ncol)
+                if (wb + w < we && col < ncol && in_range(t0 + tc0 + ctok[ct] < a.T, a.status))
                     xr[w][ct] = load_x8(a.x + size_t(t0 + tc0 + ctok[ct]) * M, 32 * (w0 + wb + w) + 8 * c, M, xvec);
                 else
                     xr[w][ct] = make_uint4(0u, 0u, 0u, 0u);
@@ -320,6 +322,7 @@ __global__ void __launch_bounds__(32 * WARPS, WARPS == 8 ? 2 : 1) dec_rs_kernel(
                 add4(u, *reinterpret_cast<const float4 *>(part + (wq * R2 + r) * CPAD + 4 * q4));
             const int pos = perm8_pos(r);
             const int owner = pos / ROWN, lp = pos - owner * ROWN;
+            if (!in_range(owner < C && rank * ROWN + lp < R2, a.status)) continue;
             st_async_v4(mapa_shared(smem_u32(rs + (rank * ROWN + lp) * CPAD + 4 * q4), static_cast<uint32_t>(owner)),
                         u, mapa_shared(smem_u32(bar_rs), static_cast<uint32_t>(owner)));
         }
@@ -343,6 +346,7 @@ __global__ void __launch_bounds__(32 * WARPS, WARPS == 8 ? 2 : 1) dec_rs_kernel(
                 const __half2 h = __floats2half2_rn(b0 * u0, b1 * u1);
                 const uint32_t word = *reinterpret_cast<const uint32_t *>(&h);
                 const uint32_t off = smem_u32(vs + ocol * LDV + p0);
+                if (!in_range(p0 + 1 < R2 && ocol < CPAD, a.status)) continue;
                 for (int dq = dg; dq < C; dq += DG)
                     st_async_b32(mapa_shared(off, static_cast<uint32_t>(dq)), word,
                                  mapa_shared(bar_off, static_cast<uint32_t>(dq)));
@@ -371,12 +375,14 @@ __global__ void __launch_bounds__(32 * WARPS, WARPS == 8 ? 2 : 1) dec_rs_kernel(
                 const int n = row_base + nl;
                 const float d0 = d[2 * hh], d1 = d[2 * hh + 1];
                 __nv_bfloat16 *ycol = a.y + size_t(t0 + tc0) * N + n;
+                // (debug build) every token row written is a row of y
+                auto y_ok = [&](int t) { return in_range(t0 + tc0 + t < a.T && n < N, a.status); };
                 if (ell == 1) {
                     const float al = row_ok ? __half2float(alp_s[nl]) : 0.f;
 #pragma unroll
                     for (int e2 = 0; e2 < 2; ++e2) {
                         const int t = 8 * ct2 + 2 * c + e2;
-                        if (row_ok && t < ntok) {
+                        if (row_ok && t < ntok && y_ok(t)) {
                             float o = al * (e2 ? d1 : d0);
                             if (a.accumulate) o += __bfloat162float(ycol[size_t(t) * N]);
                             ycol[size_t(t) * N] = __float2bfloat16_rn(o);
@@ -384,7 +390,7 @@ __global__ void __launch_bounds__(32 * WARPS, WARPS == 8 ? 2 : 1) dec_rs_kernel(
                     }
                 } else if (ell == 2) {
                     const int t = 4 * ct2 + c;
-                    if (row_ok && t < ntok) {
+                    if (row_ok && t < ntok && y_ok(t)) {
                         float o = __half2float(alp_s[nl]) * d0 + __half2float(alp_s[RW + nl]) * d1;
                         if (a.accumulate) o += __bfloat162float(ycol[size_t(t) * N]);
                         ycol[size_t(t) * N] = __float2bfloat16_rn(o);
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(32 * WARPS, WARPS == 8 ? 2 : 1) dec_rs_kernel(
                                      : 0.f;
                     o += __shfl_xor_sync(0xffffffffu, o, 1);
                     const int t = 2 * ct2 + (c >> 1);
-                    if ((c & 1) == 0 && row_ok && t < ntok) {
+                    if ((c & 1) == 0 && row_ok && t < ntok && y_ok(t)) {
                         if (a.accumulate) o += __bfloat162float(ycol[size_t(t) * N]);
                         ycol[size_t(t) * N] = __float2bfloat16_rn(o);
                     }

@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
                         const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
                         const int c = col0 + cb + j + (lane < 16 ? 0 : 1);
                         const __half2 h = (lane < 16) ? __floats2half2_rn(v0, recv) : __floats2half2_rn(recv, v1);
-                        if (store_row && c < a.C)
+                        if (store_row && c < a.C && in_range(pos + 1 < a.ldv, a.status))
                             *reinterpret_cast<__half2 *>(a.V + static_cast<size_t>(c) * a.ldv + pos) = h;
                         if (a.h_out) {
                             // the unscaled product, same layout
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
                             const int n = even ? row : row - 1;
                             float lo = even ? out[tt] : recv;
                             float hi = even ? recv : out[tt + 1];
-                            if (t < T && n < a.rows_store) {
+                            if (t < T && n < a.rows_store && in_range(n + 1 < a.ldy, a.status)) {
                                 __nv_bfloat162 *yp =
                                     reinterpret_cast<__nv_bfloat162 *>(a.y + static_cast<size_t>(t) * a.ldy + n);
                                 if (a.accumulate) {
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(const __grid_con
 #pragma unroll
                         for (int tt = 0; tt < 8; ++tt) {
                             const int t = tb + tt;
-                            if (t < T && row < a.rows_store) {
+                            if (t < T && row < a.rows_store && in_range(row < a.ldy, a.status)) {
                                 __nv_bfloat16 *yp = a.y + static_cast<size_t>(t) * a.ldy + row;
                                 float s = out[tt];
                                 if (a.accumulate) s += __bfloat162float(*yp);

@@ -33,6 +33,7 @@ DBF_ERR_CUDA = -5
 DBF_ERR_TIMEOUT = -6
 DBF_ERR_DEVICE_ARG = -7
 DBF_ERR_NUMERIC = -8
+DBF_ERR_BOUNDS = -9
 
 PATH_AUTO = 0
 PATH_DECODE = 1

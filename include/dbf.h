@@ -52,7 +52,10 @@ enum {
     DBF_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed        */
     DBF_ERR_TIMEOUT = -6,      /* device: a bounded wait ran out              */
     DBF_ERR_DEVICE_ARG = -7,   /* device: segment table out of range          */
-    DBF_ERR_NUMERIC = -8       /* device: a Cholesky pivot was not positive   */
+    DBF_ERR_NUMERIC = -8,      /* device: a Cholesky pivot was not positive   */
+    DBF_ERR_BOUNDS = -9        /* device, debug build only: an index checked
+                                  by the kernels was out of range; the access
+                                  was skipped                                  */
 };
 
 /* Kernel path selection for dbf_matmul_path (dbf_matmul uses DBF_PATH_AUTO). */

@@ -45,7 +45,7 @@ def test_struct_layout_matches_header(lib):
 
 
 def test_status_strings(lib):
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         assert lib.status_string(code) != "unknown status"
     assert lib.status_string(5) == "unknown status"
 
