@@ -608,8 +608,8 @@ __host__ __device__ inline StageSmem stage_smem(int CPAD, int RBW, int KS, int W
     if (!stage1 && acc) o += align16(size_t(CPAD) * RWS * 2);
     L.red = o;
     o += align16(size_t(kWarps) * RWS * CPAD * 4);
-    L.slots = o;  // KS > 1: this CTA's partial [RWS][CPAD], then the sums of its own rows [RWS/KS][CPAD]
-    if (KS > 1) o += align16(size_t(RWS) * CPAD * 4) + align16(size_t(RWS / KS) * CPAD * 4);
+    L.slots = o;  // KS > 1: [2 buffers][KS][RWS/KS][CPAD] partials of the owned rows, then 2 mbarriers
+    if (KS > 1) o += align16(size_t(2) * RWS * CPAD * 4) + 16;
     L.total = o;
     return L;
 }
@@ -691,6 +691,20 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
         }
     }
     cp_async_commit();
+    // KS > 1: the partial of every owned row arrives from each CTA of the cluster with st.async;
+    // one mbarrier per buffer counts the bytes of one chunk
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(smem + L.slots + align16(size_t(2) * RWS * CPAD * 4));
+    const uint32_t chunk_bytes = uint32_t(RWS) * CPAD * 4;
+    if (KS > 1) {
+        if (tid == 0) {
+            mbar_init(&xbar[0], 1);
+            mbar_init(&xbar[1], 1);
+            mbar_arrive_expect_tx(&xbar[0], chunk_bytes);
+            mbar_arrive_expect_tx(&xbar[1], chunk_bytes);
+            fence_mbar_init();
+        }
+        cluster_arrive_relaxed();  // matched by the wait before the first send
+    }
     pdl_trigger();
     if constexpr (!SEG) pdl_wait();
 
@@ -708,12 +722,8 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
     const int nchunks = (Tseg + tpc - 1) / tpc;
     const bool xvec = ((a.ldx & 7) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0);
     const uint32_t red_addr = smem_u32(red);
-    float *mine = slots;                                               // KS > 1: this CTA's partial
-    float *sums = slots + (align16(size_t(RWS) * CPAD * 4) / 4);       // KS > 1: sums of the owned rows
-    const uint32_t mine_addr = smem_u32(mine);
     const int c4 = tid % C4;
-    const int nsl = (KS > 1) ? 1 : kWarps;       // partial slices summed in the epilogue
-    const float *part = (KS > 1) ? sums : red;   // [nsl][rows][CPAD]
+    const int nsl = (KS > 1) ? KS : kWarps;      // partial slices summed in the epilogue, in order
     const int prows = (KS > 1) ? ROWN : RWS;     // rows per slice
     const int rown0 = (KS > 1) ? rank * ROWN : 0;
     const bool pairs_ok = ((a.ldy & 1) == 0);
@@ -722,7 +732,16 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
         const int tc0 = chunk * tpc;
         const int ntok = min(tpc, Tseg - tc0);
         const int ncol = ntok * ell;
-        if (chunk > 0 && KS > 1) cluster_wait_acquire();  // peers finished reading the previous chunk's partial
+        const int buf = chunk & 1;
+        const uint32_t ph = (chunk >> 1) & 1;
+        // KS > 1: the owned rows' partials of this chunk, [KS][ROWN][CPAD]; else the warp partials
+        const float *part = (KS > 1) ? slots + size_t(buf) * RWS * CPAD : red;
+        if (chunk > 0 && KS > 1) {
+            // the previous chunk's epilogue is done with `red` and its buffer; a peer writes into this
+            // chunk's buffer only after it received this CTA's partial of the chunk before
+            __syncthreads();
+            if (chunk >= 2 && tid == 0) mbar_arrive_expect_tx(&xbar[buf], chunk_bytes);
+        }
 
         // ---- 2. the first batch of activations straight into registers
         if (STAGE == 2 && a.accumulate)
@@ -796,33 +815,22 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
         }
         __syncthreads();
 
-        // ---- 4. cluster: sum the warp partials into this CTA's partial; after the
-        //         barrier each CTA sums its own rows over the partials of all
-        //         CTAs of the cluster (loads from distributed shared memory)
+        // ---- 4. cluster: sum the warp partials (in warp order) and send each row to the CTA
+        //         of the cluster that finishes it (st.async, counted on its mbarrier)
         if (KS > 1) {
+            if (chunk == 0) cluster_wait();  // every CTA of the cluster has initialised its barriers
             for (int e = tid; e < RWS * C4; e += kThreads) {
                 const int r = e / C4;
                 float4 u = *reinterpret_cast<const float4 *>(red + r * CPAD + 4 * c4);
                 for (int q = 1; q < kWarps; ++q)
                     add4(u, *reinterpret_cast<const float4 *>(red + (q * RWS + r) * CPAD + 4 * c4));
-                *reinterpret_cast<float4 *>(mine + r * CPAD + 4 * c4) = u;
+                const int owner = r / ROWN, rl = r - owner * ROWN;
+                if (!in_range(owner < KS, a.status)) continue;
+                const float *dst = slots + size_t(buf) * RWS * CPAD + (size_t(rank) * ROWN + rl) * CPAD + 4 * c4;
+                st_async_v4(mapa_shared(smem_u32(dst), static_cast<uint32_t>(owner)), u,
+                            mapa_shared(smem_u32(&xbar[buf]), static_cast<uint32_t>(owner)));
             }
-            cluster_sync_all();
-            for (int e = tid; e < ROWN * C4; e += kThreads) {
-                const int rl = e / C4;
-                const uint32_t off = mine_addr + 4u * static_cast<uint32_t>((rown0 + rl) * CPAD + 4 * c4);
-                float4 part4[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (q < KS) part4[q] = ld_dsmem_f32x4(mapa_shared(off, static_cast<uint32_t>(q)));
-                float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (q < KS) add4(u, part4[q]);
-                *reinterpret_cast<float4 *>(sums + rl * CPAD + 4 * c4) = u;
-            }
-            cluster_arrive_release();  // this CTA is done reading its peers' partials
-            __syncthreads();
+            if (!mbar_wait_bounded(&xbar[buf], ph, nullptr)) record_status(a.status, DBF_ERR_TIMEOUT);
         }
 
         // ---- 5. epilogue of this CTA's rows [rown0, rown0 + prows)
@@ -882,7 +890,8 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
         }
         __syncthreads();  // red / slots / yst are reused by the next chunk
     }
-    if (KS > 1) cluster_wait_acquire();  // peers may read this CTA's partial until they arrive
+    // Every byte a peer sends to this CTA has arrived once its waits above returned, so no
+    // peer writes into this CTA's shared memory after it exits.
 }
 
 template <int CT, int RBW, int STAGE, bool SEG>
