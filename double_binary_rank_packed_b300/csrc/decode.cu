@@ -777,34 +777,67 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
             float acc[RBW][CT][4];
 #pragma unroll
             for (int rb = 0; rb < RBW; ++rb) zero_acc<CT>(acc[rb]);
-            for (int wbat = wb; wbat < we; wbat += NWB) {
-                if (wbat != wb) load_batch(wbat);
+            if (we - wb == NWB) {
+                // exactly one batch of words: straight-line code, so the scheduler sees every
+                // shared-memory load, unpack and MMA of the warp at once (measured on the 1.5-bit
+                // layer: the stage-1 contraction 1.54 -> 1.22 us per CTA)
+                uint32_t bxs[NWB][CT][4];
 #pragma unroll
-                for (int w = 0; w < NWB; ++w) {
-                    const int wl = wbat + w;
-                    if (wl >= we) break;
-                    uint32_t bx[CT][4];
+                for (int w = 0; w < NWB; ++w)
 #pragma unroll
                     for (int ct = 0; ct < CT; ++ct) {
                         if constexpr (STAGE == 1) {
                             const uint4 gv =
-                                *reinterpret_cast<const uint4 *>(gam_s + cterm[ct] * 32 * Wc + 32 * wl + 8 * c);
-                            x_pairs(xr[w][ct], gv, bx[ct]);
+                                *reinterpret_cast<const uint4 *>(gam_s + cterm[ct] * 32 * Wc + 32 * (wb + w) + 8 * c);
+                            x_pairs(xr[w][ct], gv, bxs[w][ct]);
                         } else {
-                            bx[ct][0] = xr[w][ct].x;
-                            bx[ct][1] = xr[w][ct].y;
-                            bx[ct][2] = xr[w][ct].z;
-                            bx[ct][3] = xr[w][ct].w;
+                            bxs[w][ct][0] = xr[w][ct].x;
+                            bxs[w][ct][1] = xr[w][ct].y;
+                            bxs[w][ct][2] = xr[w][ct].z;
+                            bxs[w][ct][3] = xr[w][ct].w;
                         }
                     }
+#pragma unroll
+                for (int w = 0; w < NWB; ++w)
 #pragma unroll
                     for (int rb = 0; rb < RBW; ++rb) {
                         const int r0 = 16 * rb + g;
                         uint32_t pa[4], pv[4];
-                        sign_pairs8(bits_s[r0 * ldws + wl], c, pa);
-                        sign_pairs8(bits_s[(r0 + 8) * ldws + wl], c, pv);
+                        sign_pairs8(bits_s[r0 * ldws + wb + w], c, pa);
+                        sign_pairs8(bits_s[(r0 + 8) * ldws + wb + w], c, pv);
 #pragma unroll
-                        for (int ct = 0; ct < CT; ++ct) mma_word8(acc[rb][ct], pa, pv, bx[ct]);
+                        for (int ct = 0; ct < CT; ++ct) mma_word8(acc[rb][ct], pa, pv, bxs[w][ct]);
+                    }
+            } else {
+                for (int wbat = wb; wbat < we; wbat += NWB) {
+                    if (wbat != wb) load_batch(wbat);
+#pragma unroll
+                    for (int w = 0; w < NWB; ++w) {
+                        const int wl = wbat + w;
+                        if (wl >= we) break;
+                        uint32_t bx[CT][4];
+#pragma unroll
+                        for (int ct = 0; ct < CT; ++ct) {
+                            if constexpr (STAGE == 1) {
+                                const uint4 gv =
+                                    *reinterpret_cast<const uint4 *>(gam_s + cterm[ct] * 32 * Wc + 32 * wl + 8 * c);
+                                x_pairs(xr[w][ct], gv, bx[ct]);
+                            } else {
+                                bx[ct][0] = xr[w][ct].x;
+                                bx[ct][1] = xr[w][ct].y;
+                                bx[ct][2] = xr[w][ct].z;
+                                bx[ct][3] = xr[w][ct].w;
+                            }
+                        }
+#pragma unroll
+                        for (int rb = 0; rb < RBW; ++rb) {
+                            const int r0 = 16 * rb + g;
+                            uint32_t pa[4], pv[4];
+                            sign_pairs8(bits_s[r0 * ldws + wl], c, pa);
+                            sign_pairs8(bits_s[(r0 + 8) * ldws + wl], c, pv);
+#pragma unroll
+                            for (int ct = 0; ct < CT; ++ct) mma_word8(acc[rb][ct], pa, pv, bx[ct]);
+                        }
                     }
                 }
             }
