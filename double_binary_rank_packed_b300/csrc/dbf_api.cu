@@ -957,7 +957,18 @@ int dbf_matmul_segmented(const dbf_factors *d_adapters, int32_t n_adapters, int3
         fa.seg_ad = d_seg_adapter;
         fa.adapters = d_adapters;
         fa.n_adapters = n_adapters;
-        cudaError_t e = launch_decode_fused(true, p, fa, S, s, true);
+        // up to kChunkMapMaxS segments: one cluster per chunk of the plan's tokens, so that a
+        // segment longer than one chunk spreads over several clusters instead of running its
+        // chunks one after another.  Segment s gives max(1, ceil(len_s / tpc)) chunks, at most
+        // S + (T - 1) / tpc in all; the slots past the actual list exit at once.
+        int grid_y = S;
+        const int64_t tpc = 8 * int64_t(p.CT) / ell;
+        const int64_t slots = int64_t(S) + (T - 1) / tpc;
+        if (S <= kChunkMapMaxS && slots <= 65535) {
+            fa.chunk_map_S = S;
+            grid_y = static_cast<int>(slots);
+        }
+        cudaError_t e = launch_decode_fused(true, p, fa, grid_y, s, true);
         return e == cudaSuccess ? DBF_OK : cuda_fail(e, "segmented fused decode");
     }
     DecodeCall c = {};

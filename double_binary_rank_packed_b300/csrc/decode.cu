@@ -12,27 +12,32 @@
 //     previous kernel under programmatic dependent launch;
 //   * after the wait a CTA issues all its activation loads at once, and every
 //     later phase is spread over all threads (one or two iterations each);
-//   * partial sums leave the tensor-core fragments straight into the shared
-//     memory of the CTA that needs them (distributed shared memory inside a
-//     thread-block cluster), followed by one cluster barrier.
+//   * partial sums go from the CTA that made them into the shared memory of
+//     the CTA that needs them (st.async inside a thread-block cluster), and
+//     their arrival is counted on that CTA's mbarrier: no cluster barrier on
+//     the exchange path (the fused kernel's reduce-scatter mode for 32 or more
+//     columns keeps its two).
 //
 // The sign contraction runs on mma.sync m16n8k16 (fp16 in, fp32 accumulate):
 // packed sign words are unpacked in registers straight into the A fragment
 // (one shift + one LOP3 per fp16 pair, see sign_pair); the activation columns
-// (token t, term i -> column t*ell + i) are the B operand, read with ldmatrix
-// from shared memory in the permuted K order sign_pair expects.
+// (token t, term i -> column t*ell + i) are the B operand, loaded from global
+// memory straight into registers in the permuted K order sign_pair expects
+// (see decode_frag.cuh).
 //
 // Two kernel shapes:
-//   dec_fused_kernel  (R <= 256, the adapter case): one launch per call.  The
-//       CTAs of a cluster split stage 1 over M; every CTA pushes its partial u
-//       into every CTA of the cluster, each sums them in rank order, forms the
-//       fp16 v = beta*u itself and runs stage 2 for its own slice of the N
-//       output rows.  Every cluster recomputes stage 1 (R*M bits, small next
-//       to the call when R is small); no intermediate goes through HBM.
+//   dec_fused_kernel  (R <= 256; the adapters the reduce-scatter kernel of
+//       decode_rs.cu does not take, and routed batches): one launch per call.
+//       The CTAs of a cluster split stage 1 over M; every CTA pushes its
+//       partial u into every CTA of the cluster, each sums them in rank order,
+//       forms the fp16 v = beta*u itself and runs stage 2 for its own slice of
+//       the N output rows.  Every cluster recomputes stage 1 (R*M bits, small
+//       next to the call when R is small); no intermediate goes through HBM.
+//       A routed batch gives every chunk of every segment its own cluster.
 //   dec_stage_kernel  (any R): one launch per stage.  Stage 1 writes V (fp16)
 //       to the workspace, stage 2 reads it.  A CTA owns 16*RB weight rows and a
 //       K slice; the KS CTAs of a cluster split K and push their partials to
-//       the CTA that owns each 32-row group.
+//       the CTA that finishes each row.
 #include <algorithm>
 #include <cmath>
 
@@ -58,11 +63,16 @@ __host__ __device__ inline int ldws_for(int W) {
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
+// The prologue helpers below are kept out of line: each call site inlined
+// (an integer division and a loop apiece) made the decode kernels' code larger
+// than the SM's instruction cache, and their warps then stalled on
+// instruction fetch.
+
 // Copy nrows rows of row_bytes each from global to shared memory with
 // cp.async; the chunk size (16, 4 or 2 bytes) is the largest that every
 // address and stride allows.  2-byte chunks use plain loads and stores.
-__device__ __forceinline__ void copy_rows_async(void *dst, int dst_stride, const void *src, size_t src_stride,
-                                                int nrows, int row_bytes, int tid, int nthr) {
+__device__ __noinline__ void copy_rows_async(void *dst, int dst_stride, const void *src, size_t src_stride,
+                                             int nrows, int row_bytes, int tid, int nthr) {
     if (nrows <= 0 || row_bytes <= 0) return;
     const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
     const uintptr_t all = d | s | static_cast<uintptr_t>(dst_stride) | static_cast<uintptr_t>(src_stride) |
@@ -94,8 +104,8 @@ __device__ __forceinline__ void copy_rows_async(void *dst, int dst_stride, const
 // As copy_rows_async, for data an earlier kernel may have written (x, V, the
 // old y): 16-byte cp.async.cg (through L2 only) when aligned, else plain
 // coherent loads and stores.
-__device__ __forceinline__ void copy_rows_dep(void *dst, int dst_stride, const void *src, size_t src_stride,
-                                              int nrows, int row_bytes, int tid, int nthr) {
+__device__ __noinline__ void copy_rows_dep(void *dst, int dst_stride, const void *src, size_t src_stride,
+                                           int nrows, int row_bytes, int tid, int nthr) {
     if (nrows <= 0 || row_bytes <= 0) return;
     const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
     const uintptr_t all = d | s | static_cast<uintptr_t>(dst_stride) | static_cast<uintptr_t>(src_stride) |
@@ -113,11 +123,21 @@ __device__ __forceinline__ void copy_rows_dep(void *dst, int dst_stride, const v
 }
 
 // Zero nrows x row_bytes (row_bytes a multiple of 4) of shared memory.
-__device__ __forceinline__ void zero_rows(void *dst, int dst_stride, int nrows, int row_bytes, int tid, int nthr) {
+__device__ __noinline__ void zero_rows(void *dst, int dst_stride, int nrows, int row_bytes, int tid, int nthr) {
     const int q = row_bytes >> 2;
     for (int e = tid; e < nrows * q; e += nthr) {
         const int r = e / q, c = e - r * q;
         *reinterpret_cast<uint32_t *>(static_cast<char *>(dst) + r * dst_stride + 4 * c) = 0u;
+    }
+}
+
+// Zero the tail [from, len) of each of nrows fp16 rows of length len.
+__device__ __noinline__ void zero_half_tails(__half *base, int nrows, int len, int from, int tid, int nthr) {
+    const int w = len - from;
+    if (w <= 0) return;
+    for (int e = tid; e < nrows * w; e += nthr) {
+        const int i = e / w;
+        base[i * len + from + (e - i * w)] = __float2half_rn(0.f);
     }
 }
 
@@ -160,7 +180,7 @@ __device__ __forceinline__ void epilogue_tile(const float *tile, int ldt, const 
 // ============================================================ fused kernel
 
 struct FusedSmem {
-    size_t gam, b2, beta, b1, alp, red, slots, vs, yst, tile, total;
+    size_t gam, b2, beta, b1, alp, red, slots, vs, yst, tile, bar, total;
 };
 
 __host__ __device__ inline int fused_g1(int R, int RBW) { return ((R + 15) / 16 + RBW - 1) / RBW; }
@@ -203,8 +223,152 @@ __host__ __device__ inline FusedSmem fused_smem(int CPAD, int RBW, int Wc, int R
     if (acc) o += align16(size_t(CPAD) * RW * 2);
     L.tile = o;
     if (ell == 3) o += size_t(RW) * (CPAD + 4) * 4;
+    L.bar = align16(o);  // all-to-all exchange: the mbarrier counting the bytes of every CTA's partial
+    o = L.bar + 16;
     L.total = o;
     return L;
+}
+
+// Chunk list of a routed batch: segment s (tokens [off[s], off[s+1])) is cut
+// into ceil(len / tpc) chunks of tpc tokens, segments in order.  Finds chunk
+// q: its segment s, the segment's first token o0, the chunk's first token jt
+// inside the segment and its token count jn, and the segment's adapter ad,
+// all read in one pass over the table.  Returns false (the same in every
+// thread) when q is past the end of the list.  An empty segment and an
+// invalid entry (negative length, offsets outside [0, T]; reported with
+// o0 = -1) count as one chunk, so that a cluster checks every entry, as in
+// the one-segment-per-cluster mode.  Uses 8 ints of shared memory before any
+// other use of it; all threads of the CTA take part.
+constexpr int kAdTableSmemMax = 8192;  // adapter tables up to this size go to shared memory
+static_assert(sizeof(dbf_factors) % 16 == 0, "the adapter table is copied in 16-byte pieces");
+
+__device__ __noinline__ bool fused_find_chunk(const int32_t *off, const int32_t *seg_ad, int S, int T, int tpc, int q,
+                                              int &s, int &o0, int &jt, int &jn, int &ad, int *sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kPer = (kChunkMapMaxS + kThreads - 1) / kThreads;  // segments per thread
+    int lo[kPer], hi[kPer], sa[kPer], cnt[kPer];
+    int mine = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = tid * kPer + k;
+        lo[k] = i < S ? off[i] : 0;
+        hi[k] = i < S ? off[i + 1] : 0;
+        sa[k] = i < S ? seg_ad[i] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = tid * kPer + k;
+        const bool ok = !(lo[k] < 0 || hi[k] < lo[k] || hi[k] > T);
+        cnt[k] = i >= S ? 0 : (ok ? max(1, (hi[k] - lo[k] + tpc - 1) / tpc) : 1);
+        mine += cnt[k];
+    }
+    // exclusive prefix of the per-thread totals across the CTA (thread order = segment order)
+    int incl = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) sm[warp] = incl;
+    __syncthreads();
+    int before = incl - mine;
+    for (int w = 0; w < warp; ++w) before += sm[w];
+    int total = 0;
+    for (int w = 0; w < kWarps; ++w) total += sm[w];
+    __syncthreads();  // sm is reused below
+    if (q >= total) return false;
+    if (q >= before && q < before + mine) {
+        int acc = before;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            if (q >= acc && q < acc + cnt[k]) {
+                const int i = tid * kPer + k;
+                const int j = q - acc;
+                const bool ok = !(lo[k] < 0 || hi[k] < lo[k] || hi[k] > T);
+                sm[0] = i;
+                sm[1] = ok ? lo[k] : -1;
+                sm[2] = ok ? j * tpc : 0;
+                sm[3] = ok ? min(tpc, hi[k] - lo[k] - j * tpc) : 0;
+                sm[4] = sa[k];
+            }
+            acc += cnt[k];
+        }
+    }
+    __syncthreads();
+    s = sm[0];
+    o0 = sm[1];
+    jt = sm[2];
+    jn = sm[3];
+    ad = sm[4];
+    __syncthreads();  // the caller reuses sm
+    return true;
+}
+
+// What the stage-2 epilogue of the fused kernel needs besides the item.
+struct FusedEpi {
+    __nv_bfloat16 *y;  // row (t0 + tc0) of y, column row_base: y of the chunk's first token
+    const __half *alp_s;
+    const __nv_bfloat16 *yst;
+    int *status;
+    uint32_t tile_addr;
+    int N, RW, ell, nrows2, ntok, ldt, acc;
+    int tok_left, rows_left;  // (debug build) token rows of y from the chunk's first, rows from row_base
+};
+
+// One stage-2 item (rows 16*rb2 .. +15 of the CTA's slice, column tile ct;
+// accumulator fragment q0..q3) -> y[t][n] = bf16(sum_i alpha_i[n] q (+ y)),
+// or into the fp32 tile for ell = 3.  Inlined: a routed batch runs four
+// items side by side, and the epilogues of the four overlap only inline
+// (out of line, the routed batch measured 17.4 -> 22.5 us).
+__device__ __forceinline__ void fused_epilogue_item(const FusedEpi &e, float q0, float q1, float q2, float q3, int rb2,
+                                                 int ct) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const int n0 = 16 * rb2 + g;
+    if (e.ell == 3) {
+        float dd[1][4] = {{q0, q1, q2, q3}};
+        put_frag<1>(e.tile_addr + 4u * static_cast<uint32_t>(16 * rb2 * e.ldt + 8 * ct), e.ldt, dd, lane, false, 0);
+        return;
+    }
+    // rows n0 (q0, q1) and n0 + 8 (q2, q3); columns 8ct + 2c, 8ct + 2c + 1
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int nl = n0 + 8 * hh;
+        const float d0 = hh ? q2 : q0, d1 = hh ? q3 : q1;
+        const bool row_ok = nl < e.nrows2;
+        __nv_bfloat16 *yrow = e.y + nl;
+        // (debug build) every token row written is a row of y
+        auto y_ok = [&](int t) { return in_range(t < e.tok_left && nl < e.rows_left, e.status); };
+        if (e.ell == 1) {
+            const float al = row_ok ? __half2float(e.alp_s[nl]) : 0.f;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int t = 8 * ct + 2 * c + k;
+                if (row_ok && t < e.ntok && y_ok(t)) {
+                    float o = al * (k ? d1 : d0);
+                    if (e.acc) o += __bfloat162float(e.yst[t * e.RW + nl]);
+                    yrow[size_t(t) * e.N] = __float2bfloat16_rn(o);
+                }
+            }
+        } else if (e.ell == 2) {
+            const int t = 4 * ct + c;
+            if (row_ok && t < e.ntok && y_ok(t)) {
+                float o = __half2float(e.alp_s[nl]) * d0 + __half2float(e.alp_s[e.RW + nl]) * d1;
+                if (e.acc) o += __bfloat162float(e.yst[t * e.RW + nl]);
+                yrow[size_t(t) * e.N] = __float2bfloat16_rn(o);
+            }
+        } else {  // ell == 4: terms 0,1 in lane c even, 2,3 in lane c odd
+            const int i0 = 2 * (c & 1);
+            float o = row_ok ? __half2float(e.alp_s[i0 * e.RW + nl]) * d0 +
+                                   __half2float(e.alp_s[(i0 + 1) * e.RW + nl]) * d1
+                             : 0.f;
+            o += __shfl_xor_sync(0xffffffffu, o, 1);
+            const int t = 2 * ct + (c >> 1);
+            if ((c & 1) == 0 && row_ok && t < e.ntok && y_ok(t)) {
+                if (e.acc) o += __bfloat162float(e.yst[t * e.RW + nl]);
+                yrow[size_t(t) * e.N] = __float2bfloat16_rn(o);
+            }
+        }
+    }
 }
 
 template <int CT, int RBW, bool SEG>
@@ -223,18 +387,70 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
     const uint32_t *B1 = a.B1, *B2 = a.B2;
     int ldw1 = a.ldw1, ldw2 = a.ldw2;
     const __half *alpha = a.alpha, *beta = a.beta, *gamma = a.gamma;
+    const int G1 = fused_g1(R, RBW);
+    const int R1 = 16 * RBW * G1, R2 = (R + 31) & ~31;
+    const int Kw1 = (M + 31) >> 5, Kw2 = R2 >> 5;
+    const int KP = fused_kp(G1);
+    const int Wc = a.Wc, RW = a.RW;
+    const bool acc_mode = a.accumulate != 0;
+    const FusedSmem L = fused_smem(CPAD, RBW, Wc, R, RW, ell, C, acc_mode);
+    const int w0 = rank * Wc;
+    const int Wslice = max(0, min(Wc, Kw1 - w0));
+
     int t0 = 0, Tseg = a.T;
     if constexpr (SEG) {
-        pdl_wait();  // the routing table may come from the previous kernel
-        const int s = blockIdx.y;
-        const int o0 = a.seg_off[s], o1 = a.seg_off[s + 1], ad = a.seg_ad[s];
-        if (o0 < 0 || o1 < o0 || o1 > a.T || ad < 0 || ad >= a.n_adapters) {
-            if (tid == 0 && blockIdx.x == 0) record_status(a.status, DBF_ERR_DEVICE_ARG);
-            return;  // uniform over the cluster: every CTA of it reads the same entry
+        // The adapter table is factor memory (no earlier kernel writes it): in chunk-list
+        // mode a small table goes to shared memory (the stage-1 reduction area, unused
+        // until stage 1) while the previous kernel finishes, which takes a dependent
+        // memory round trip off the path behind the wait.
+        const size_t table_bytes = size_t(a.n_adapters) * sizeof(dbf_factors);
+        const bool table_s = a.chunk_map_S > 0 && table_bytes <= kAdTableSmemMax &&
+                             table_bytes <= size_t(KP) * R1 * CPAD * 4 &&
+                             (reinterpret_cast<uintptr_t>(a.adapters) & 15) == 0;
+        const dbf_factors *tab = reinterpret_cast<const dbf_factors *>(smem + L.red);
+        if (table_s) {
+            for (int e = tid; e < static_cast<int>(table_bytes / 16); e += kThreads)
+                cp_async_16(smem + L.red + 16 * e, reinterpret_cast<const char *>(a.adapters) + 16 * e);
+            cp_async_commit();
         }
-        t0 = o0;
-        Tseg = o1 - o0;
-        const dbf_factors f = a.adapters[ad];
+        pdl_wait();  // the routing table may come from the previous kernel
+        int s = blockIdx.y, o0, ad;
+        if (a.chunk_map_S > 0) {
+            // every segment in order contributes ceil(len / tpc) chunks; find chunk
+            // blockIdx.y (uniform over the cluster: all its CTAs scan the same table)
+            const int tpc = CPAD / ell;
+            int jt, jn;
+            if (table_s) cp_async_wait_all();  // made visible by the barriers of the scan
+            if (!fused_find_chunk(a.seg_off, a.seg_ad, a.chunk_map_S, a.T, tpc, static_cast<int>(blockIdx.y), s, o0,
+                                  jt, jn, ad, reinterpret_cast<int *>(smem)))
+                return;  // a slot past the end of the chunk list
+            if (o0 < 0 || jn < 0 || ad < 0 || ad >= a.n_adapters) {
+                // reported once per segment: by the cluster of its first chunk
+                if (tid == 0 && blockIdx.x == 0 && jt == 0) record_status(a.status, DBF_ERR_DEVICE_ARG);
+                return;  // uniform over the cluster: every CTA of it reads the same entry
+            }
+            t0 = o0 + jt;
+            Tseg = jn;
+            // this CTA's activation slice into L2 while the factors are looked up and fetched
+            if (Tseg > 0) {
+                const int lines = (Wslice * 64 + 127) / 128;
+                for (int e = tid; e < Tseg * lines; e += kThreads) {
+                    const int t = e / lines, l = e - t * lines;
+                    prefetch_l2(a.x + size_t(t0 + t) * M + 32 * w0 + 64 * l);
+                }
+            }
+        } else {
+            o0 = a.seg_off[s];
+            const int o1 = a.seg_off[s + 1];
+            ad = a.seg_ad[s];
+            if (o0 < 0 || o1 < o0 || o1 > a.T || ad < 0 || ad >= a.n_adapters) {
+                if (tid == 0 && blockIdx.x == 0) record_status(a.status, DBF_ERR_DEVICE_ARG);
+                return;  // uniform over the cluster: every CTA of it reads the same entry
+            }
+            t0 = o0;
+            Tseg = o1 - o0;
+        }
+        const dbf_factors f = table_s ? tab[ad] : a.adapters[ad];
         B1 = f.B1;
         B2 = f.B2;
         ldw1 = f.ldw1;
@@ -243,15 +459,9 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
         beta = reinterpret_cast<const __half *>(f.beta);
         gamma = reinterpret_cast<const __half *>(f.gamma);
         if (Tseg == 0) return;
+        if (table_s) __syncthreads();  // every thread holds its copy of the entry before the area is reused
     }
 
-    const int G1 = fused_g1(R, RBW);
-    const int R1 = 16 * RBW * G1, R2 = (R + 31) & ~31;
-    const int Kw1 = (M + 31) >> 5, Kw2 = R2 >> 5;
-    const int KP = fused_kp(G1);
-    const int Wc = a.Wc, RW = a.RW;
-    const bool acc_mode = a.accumulate != 0;
-    const FusedSmem L = fused_smem(CPAD, RBW, Wc, R, RW, ell, C, acc_mode);
     __half *gam_s = reinterpret_cast<__half *>(smem + L.gam);
     uint32_t *b2_s = reinterpret_cast<uint32_t *>(smem + L.b2);
     __half *beta_s = reinterpret_cast<__half *>(smem + L.beta);
@@ -265,8 +475,6 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
 
     const int ldb2 = ldws_for(Wc), ldb1 = ldws_for(Kw2);
     const int ldv = R2 + 8, ldt = CPAD + 4;
-    const int w0 = rank * Wc;
-    const int Wslice = max(0, min(Wc, Kw1 - w0));
     const int kvalid = max(0, min(32 * Wslice, M - 32 * w0));
     const int row_base = blockIdx.x * RW;  // first stage-2 output row of this CTA
     const int nrows2 = max(0, min(RW, N - row_base));
@@ -275,19 +483,23 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
     copy_rows_async(b2_s, ldb2 * 4, B2 + w0, size_t(ldw2) * 4, R, Wslice * 4, tid, kThreads);
     zero_rows(b2_s + R * ldb2, ldb2 * 4, R1 - R, Wslice * 4, tid, kThreads);
     if (kvalid > 0) copy_rows_async(gam_s, 64 * Wc, gamma + 32 * w0, size_t(M) * 2, ell, kvalid * 2, tid, kThreads);
-    for (int e = tid; e < ell * (32 * Wc - kvalid); e += kThreads) {
-        const int i = e / (32 * Wc - kvalid);
-        gam_s[i * 32 * Wc + kvalid + (e - i * (32 * Wc - kvalid))] = __float2half_rn(0.f);
-    }
+    zero_half_tails(gam_s, ell, 32 * Wc, kvalid, tid, kThreads);
     copy_rows_async(beta_s, R2 * 2, beta, size_t(R) * 2, ell, R * 2, tid, kThreads);
-    for (int e = tid; e < ell * (R2 - R); e += kThreads) {
-        const int i = e / (R2 - R);
-        beta_s[i * R2 + R + (e - i * (R2 - R))] = __float2half_rn(0.f);
-    }
+    zero_half_tails(beta_s, ell, R2, R, tid, kThreads);
     copy_rows_async(b1_s, ldb1 * 4, B1 + size_t(row_base) * ldw1, size_t(ldw1) * 4, nrows2, Kw2 * 4, tid, kThreads);
     zero_rows(b1_s + nrows2 * ldb1, ldb1 * 4, RW - nrows2, Kw2 * 4, tid, kThreads);
     copy_rows_async(alp_s, RW * 2, alpha + row_base, size_t(N) * 2, ell, nrows2 * 2, tid, kThreads);
     cp_async_commit();
+    // all-to-all exchange: every CTA of the cluster (this one included) sends its partial u
+    // of a chunk with st.async, counted on this CTA's mbarrier (one phase per chunk)
+    const bool scatter = CPAD >= 32 && fused_scatter(C, R, CPAD);  // (compiled for 32+ columns only)
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(smem + L.bar);
+    const uint32_t a2a_bytes = uint32_t(C) * R1 * CPAD * 4;
+    if (C > 1 && !scatter && tid == 0) {
+        mbar_init(xbar, 1);
+        mbar_arrive_expect_tx(xbar, a2a_bytes);
+        fence_mbar_init();
+    }
     if (C > 1) cluster_arrive_relaxed();  // matched by the wait before the first push
     pdl_trigger();
     if constexpr (!SEG) pdl_wait();
@@ -318,14 +530,18 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
     const uint32_t red_addr = smem_u32(red), slots_addr = smem_u32(slots), tile_addr = smem_u32(tile);
     const uint32_t vs_addr = smem_u32(vs);
     const int RB2 = RW / 16;
-    const bool scatter = fused_scatter(C, R, CPAD);
     const int RO = R2 / C;  // rows of v each CTA of the cluster finishes (scatter mode)
 
     for (int chunk = 0; chunk < nchunks; ++chunk) {
         const int tc0 = chunk * tpc;
         const int ntok = min(tpc, Tseg - tc0);
         const int ncol = ntok * ell;
-        if (chunk > 0 && C > 1) cluster_sync_all();  // peers finished reading the previous chunk's slots
+        const int ctu = (ncol + 7) >> 3;  // column tiles that hold a column of this chunk
+        if (chunk > 0 && C > 1) {
+            // re-armed before the barrier: no peer sends this chunk's partial until it has passed it
+            if (!scatter && tid == 0) mbar_arrive_expect_tx(xbar, a2a_bytes);
+            cluster_sync_all();  // peers finished reading the previous chunk's slots
+        }
         const __nv_bfloat16 *xc = a.x + size_t(t0 + tc0) * M;
 
         // ---- 2. old y by cp.async; the first batch of x straight into registers
@@ -365,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
                     uint32_t bx[CT][4];
 #pragma unroll
                     for (int ct = 0; ct < CT; ++ct) {
+                        if (ct >= ctu) break;
                         const uint4 gv = *reinterpret_cast<const uint4 *>(gam_s + cterm[ct] * 32 * Wc + 32 * wl + 8 * c);
                         x_pairs(xr[w][ct], gv, bx[ct]);
                     }
@@ -375,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
                         sign_pairs8(b2_s[r0 * ldb2 + wl], c, pa);
                         sign_pairs8(b2_s[(r0 + 8) * ldb2 + wl], c, pv);
 #pragma unroll
-                        for (int ct = 0; ct < CT; ++ct) mma_word8(acc[rb][ct], pa, pv, bx[ct]);
+                        for (int ct = 0; ct < CT; ++ct)
+                            if (ct < ctu) mma_word8(acc[rb][ct], pa, pv, bx[ct]);
                     }
                 }
             }
@@ -440,18 +658,19 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
                 const uint32_t off = slots_addr + 4u * static_cast<uint32_t>((rank * R1 + r) * CPAD + 4 * c4);
                 if (C > 1) {
                     for (int q = 0; q < C; ++q)
-                        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                         mapa_shared(off, static_cast<uint32_t>(q))),
-                                     "f"(u.x), "f"(u.y), "f"(u.z), "f"(u.w)
-                                     : "memory");
+                        st_async_v4(mapa_shared(off, static_cast<uint32_t>(q)), u,
+                                    mapa_shared(smem_u32(xbar), static_cast<uint32_t>(q)));
                 } else {
                     *reinterpret_cast<float4 *>(slots + r * CPAD + 4 * c4) = u;
                 }
             }
-            if (C > 1)
-                cluster_sync_all();  // every slot of every CTA is filled
-            else
+            if (C > 1) {
+                // every slot of this CTA is filled once the chunk's bytes have all arrived
+                if (!mbar_wait_bounded(xbar, static_cast<uint32_t>(chunk & 1), nullptr))
+                    record_status(a.status, DBF_ERR_TIMEOUT);
+            } else {
                 __syncthreads();
+            }
 
             // ---- 5. u = sum of the slots in rank order, v = beta * u (fp16, perm8 order)
             for (int e = tid; e < R2 * C4; e += kThreads) {
@@ -474,58 +693,30 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
         //         rows); there a warp runs kIB of them side by side, so their
         //         independent chains of loads, MMAs and epilogue overlap.
         constexpr int kIB = 4;
+        FusedEpi epi;
+        epi.y = a.y + size_t(t0 + tc0) * N + row_base;
+        epi.alp_s = alp_s;
+        epi.yst = yst;
+        epi.status = a.status;
+        epi.tile_addr = tile_addr;
+        epi.N = N;
+        epi.RW = RW;
+        epi.ell = ell;
+        epi.nrows2 = nrows2;
+        epi.ntok = ntok;
+        epi.ldt = ldt;
+        epi.acc = acc_mode;
+        epi.tok_left = a.T - (t0 + tc0);
+        epi.rows_left = N - row_base;
         auto epilogue_item = [&](const float (&d)[4], int rb2, int ct) {
-            const int n0 = 16 * rb2 + g;
-            if (ell == 3) {
-                float dd[1][4] = {{d[0], d[1], d[2], d[3]}};
-                put_frag<1>(tile_addr + 4u * static_cast<uint32_t>(16 * rb2 * ldt + 8 * ct), ldt, dd, lane, false, 0);
-                return;
-            }
-            // rows n0 (d[0], d[1]) and n0 + 8 (d[2], d[3]); columns 8ct + 2c, 8ct + 2c + 1
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int nl = n0 + 8 * hh;
-                const float d0 = d[2 * hh], d1 = d[2 * hh + 1];
-                const bool row_ok = nl < nrows2;
-                __nv_bfloat16 *yrow = a.y + size_t(t0 + tc0) * N + row_base + nl;
-                // (debug build) every token row written is a row of y
-                auto y_ok = [&](int t) { return in_range(t0 + tc0 + t < a.T && row_base + nl < N, a.status); };
-                if (ell == 1) {
-                    const float al = row_ok ? __half2float(alp_s[nl]) : 0.f;
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = 8 * ct + 2 * c + e;
-                        if (row_ok && t < ntok && y_ok(t)) {
-                            float o = al * (e ? d1 : d0);
-                            if (acc_mode) o += __bfloat162float(yst[t * RW + nl]);
-                            yrow[size_t(t) * N] = __float2bfloat16_rn(o);
-                        }
-                    }
-                } else if (ell == 2) {
-                    const int t = 4 * ct + c;
-                    if (row_ok && t < ntok && y_ok(t)) {
-                        float o = __half2float(alp_s[nl]) * d0 + __half2float(alp_s[RW + nl]) * d1;
-                        if (acc_mode) o += __bfloat162float(yst[t * RW + nl]);
-                        yrow[size_t(t) * N] = __float2bfloat16_rn(o);
-                    }
-                } else {  // ell == 4: terms 0,1 in lane c even, 2,3 in lane c odd
-                    const int i0 = 2 * (c & 1);
-                    float o = row_ok ? __half2float(alp_s[i0 * RW + nl]) * d0 + __half2float(alp_s[(i0 + 1) * RW + nl]) * d1
-                                     : 0.f;
-                    o += __shfl_xor_sync(0xffffffffu, o, 1);
-                    const int t = 2 * ct + (c >> 1);
-                    if ((c & 1) == 0 && row_ok && t < ntok && y_ok(t)) {
-                        if (acc_mode) o += __bfloat162float(yst[t * RW + nl]);
-                        yrow[size_t(t) * N] = __float2bfloat16_rn(o);
-                    }
-                }
-            }
+            fused_epilogue_item(epi, d[0], d[1], d[2], d[3], rb2, ct);
         };
-        // few items per warp (the single-adapter shapes): one at a time, as a batch
-        // only adds work there
-        const bool batched = SEG && RB2 * CT >= 8 * kWarps;
-        if (!batched) {
-            for (int it = warp; it < RB2 * CT; it += kWarps) {
+        // items of the column tiles that hold columns (a routed segment is often
+        // shorter than the chunk); a single adapter gives a warp few items: one
+        // at a time there, as a batch only adds work
+        const int items = RB2 * ctu;
+        if constexpr (!SEG) {
+            for (int it = warp; it < items; it += kWarps) {
                 const int rb2 = it % RB2, ct = it / RB2;
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
                 const int n0 = 16 * rb2 + g;
@@ -541,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
             }
         }
         if constexpr (SEG) {
-        for (int it0 = warp; batched && it0 < RB2 * CT; it0 += kWarps * kIB) {
+        for (int it0 = warp; it0 < items; it0 += kWarps * kIB) {
             float d[kIB][4];
             int rbv[kIB], ctv[kIB];
 #pragma unroll
@@ -555,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
             for (int w = 0; w < Kw2; ++w) {
 #pragma unroll
                 for (int b = 0; b < kIB; ++b) {
-                    if (it0 + b * kWarps >= RB2 * CT) break;
+                    if (it0 + b * kWarps >= items) break;
                     const int n0 = 16 * rbv[b] + g;
                     const uint4 bv = *reinterpret_cast<const uint4 *>(vs + (8 * ctv[b] + g) * ldv + 32 * w + 8 * c);
                     const uint32_t bb[4] = {bv.x, bv.y, bv.z, bv.w};
@@ -567,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_fused_kernel(const FusedArgs 
             }
 #pragma unroll
             for (int b = 0; b < kIB; ++b) {
-                if (it0 + b * kWarps >= RB2 * CT) break;
+                if (it0 + b * kWarps >= items) break;
                 epilogue_item(d[b], rbv[b], ctv[b]);
             }
         }
@@ -678,17 +869,11 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
                     kThreads);
     zero_rows(bits_s + nr * ldws, ldws * 4, RWS - nr, Wslice * 4, tid, kThreads);
     copy_rows_async(sc_s, RWS * 2, scale_out + row0, size_t(a.rows) * 2, ell, nr * 2, tid, kThreads);
-    for (int e = tid; e < ell * (RWS - nr); e += kThreads) {
-        const int i = e / (RWS - nr);
-        sc_s[i * RWS + nr + (e - i * (RWS - nr))] = __float2half_rn(0.f);
-    }
+    zero_half_tails(sc_s, ell, RWS, nr, tid, kThreads);
     if (STAGE == 1) {
         if (kvalid > 0)
             copy_rows_async(gam_s, 64 * Wc, scale_in + 32 * w0, size_t(a.K) * 2, ell, kvalid * 2, tid, kThreads);
-        for (int e = tid; e < ell * (32 * Wc - kvalid); e += kThreads) {
-            const int i = e / (32 * Wc - kvalid);
-            gam_s[i * 32 * Wc + kvalid + (e - i * (32 * Wc - kvalid))] = __float2half_rn(0.f);
-        }
+        zero_half_tails(gam_s, ell, 32 * Wc, kvalid, tid, kThreads);
     }
     cp_async_commit();
     // KS > 1: the partial of every owned row arrives from each CTA of the cluster with st.async;

@@ -19,16 +19,22 @@ __device__ __forceinline__ void mma_word8(float (&acc)[4], const uint32_t (&pa)[
     mma_16816(acc, pa[2], pv[2], pa[3], pv[3], b[2], b[3]);
 }
 
-// 8 bf16 of x (k0 .. k0+7 of one row, zero at k >= kmax) with plain
-// coherent loads: x is written by an earlier kernel.
-__device__ __forceinline__ uint4 load_x8(const __nv_bfloat16 *row, int k0, int kmax, bool vec) {
-    if (vec && k0 + 8 <= kmax) return *reinterpret_cast<const uint4 *>(row + k0);
+// The ragged or unaligned case of load_x8, kept out of line: it is rare, and
+// inlined at every unrolled call site it would multiply the kernels' code.
+static __device__ __noinline__ uint4 load_x8_slow(const __nv_bfloat16 *row, int k0, int kmax) {
     const uint16_t *r16 = reinterpret_cast<const uint16_t *>(row);
     uint16_t v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = (k0 + j < kmax) ? r16[k0 + j] : uint16_t(0);
     return make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16), v[4] | (uint32_t(v[5]) << 16),
                       v[6] | (uint32_t(v[7]) << 16));
+}
+
+// 8 bf16 of x (k0 .. k0+7 of one row, zero at k >= kmax) with plain
+// coherent loads: x is written by an earlier kernel.
+__device__ __forceinline__ uint4 load_x8(const __nv_bfloat16 *row, int k0, int kmax, bool vec) {
+    if (vec && k0 + 8 <= kmax) return *reinterpret_cast<const uint4 *>(row + k0);
+    return load_x8_slow(row, k0, kmax);
 }
 
 // The lane's four B pairs of one word from 8 bf16 x (physical k 8c..8c+7)

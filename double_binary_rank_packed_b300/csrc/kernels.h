@@ -87,7 +87,16 @@ struct FusedArgs {
     const dbf_factors *adapters;
     int n_adapters;
     int *status;
+    // routed batches: 0 = blockIdx.y is a segment and the CTA runs all of its
+    // chunks; > 0 = the number of segments S (at most kChunkMapMaxS), and
+    // blockIdx.y is one chunk of the batch's chunk list (every segment in
+    // order, cut into chunks of the plan's tokens; slots past the list exit)
+    int chunk_map_S;
 };
+
+// Routed batches of at most this many segments give every chunk its own
+// cluster; each CTA finds its chunk with a scan of the segment table.
+constexpr int kChunkMapMaxS = 1024;
 
 struct FusedPlan {
     int CT, RBW, C, RW, Wc, grid_x;  // CT = 0: no plan; RBW: stage-1 16-row blocks per warp

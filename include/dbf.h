@@ -31,6 +31,15 @@
  *     invalid segment table) are recorded in a device status word that
  *     dbf_check_status() reads and clears.
  *   - T = 0 (no tokens) is a no-op that returns DBF_OK.
+ *   - The matmul kernels use programmatic dependent launch: they start while
+ *     the kernel before them on the stream finishes, and they read factor
+ *     memory (packed signs, scales, and the d_adapters table of
+ *     dbf_matmul_segmented) before waiting for it; they wait before reading
+ *     x, y and the segment tables.  Only kernels that allow this overlap let
+ *     it happen (a kernel that does not is complete before the next one
+ *     starts): this library's matmul kernels, which never write factor
+ *     memory.  So factor memory may come from any earlier copy or kernel,
+ *     except a kernel of the caller's that itself allows the overlap.
  */
 #ifndef DBF_H
 #define DBF_H
@@ -282,7 +291,11 @@ int dbf_matmul_hostio(const dbf_factors *f, const uint16_t *x_host, int64_t T,
  *   d_seg_adapter device int32 [S], each in [0, n_adapters)
  * Rows of y outside every segment are not written.  The table is read on the
  * device (no host synchronisation); an out-of-range entry skips that segment
- * and records DBF_ERR_DEVICE_ARG for dbf_check_status.
+ * and records DBF_ERR_DEVICE_ARG for dbf_check_status.  With S <= 1024 every
+ * chunk of a segment (as many tokens as the launch's column tile holds) gets
+ * its own thread-block cluster, found by a scan of the offsets on the device;
+ * larger S give a cluster per segment, which runs the segment's chunks in
+ * turn.  The results are the same bits either way.
  */
 size_t dbf_segmented_workspace_bytes(int32_t N, int32_t M, int32_t R, int32_t ell,
                                      int64_t T, int32_t S);

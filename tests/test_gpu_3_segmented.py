@@ -82,3 +82,59 @@ def test_bad_segment_entry_is_reported_and_skipped(cuda_lib):
     y, _ = O.matmul_segmented(xb, adapters, [0, 4], [0])
     U.assert_close(got[:4], y[:4], "valid segment")
     assert (got[4:] == 0).all()
+
+
+def test_chunk_clusters_match_segment_clusters(cuda_lib):
+    # The same routing twice: compact (S <= 1024: a cluster per chunk, found by a scan
+    # on the device) and padded with empty segments past 1024 (a cluster per segment,
+    # chunks in turn).  The two are planned for different segment lengths (their tile
+    # plans, and so their summation orders, may differ): each is held to the oracle.
+    N, M, R, ell = 160, 224, 48, 2
+    adapters = [G.make_factors(N, M, R, ell, 990 + a) for a in range(3)]
+    T = 70
+    xb = G.make_x(T, M, 991)
+    off = [0, 1, 37, 38, 45, 70]      # segments of 1, 36, 1, 7 and 25 tokens
+    ad = [2, 0, 1, 2, 0]
+    compact, st = run_segmented(cuda_lib, adapters, N, M, R, ell, xb, off, ad)
+    assert st == 0
+    pad_off, pad_ad = [0], []
+    for s in range(len(ad)):
+        for _ in range(230):          # 230 empty segments before each real one
+            pad_off.append(off[s])
+            pad_ad.append(1)
+        pad_off.append(off[s + 1])
+        pad_ad.append(ad[s])
+    assert len(pad_ad) > 1024
+    padded, st = run_segmented(cuda_lib, adapters, N, M, R, ell, xb, pad_off, pad_ad)
+    assert st == 0
+    y, _ = O.matmul_segmented(xb, adapters, off, ad)
+    U.assert_close(compact, y, "chunk clusters")
+    U.assert_close(padded, y, "segment clusters")
+
+
+def test_bad_entry_of_an_empty_segment_is_reported(cuda_lib):
+    N, M, R, ell = 64, 96, 32, 1
+    adapters = [G.make_factors(N, M, R, ell, 975)]
+    T = 8
+    xb = G.make_x(T, M, 976)
+    off = [0, 4, 4, 8]
+    ad = [0, 9, 0]     # the empty middle segment names a missing adapter
+    got, st = run_segmented(cuda_lib, adapters, N, M, R, ell, xb, off, ad)
+    assert st == cuda_lib.DBF_ERR_DEVICE_ARG
+    y, _ = O.matmul_segmented(xb, adapters, [0, 4, 8], [0, 0])
+    U.assert_close(got, y, "segments around the bad entry")
+
+
+def test_large_adapter_table(cuda_lib):
+    # 160 adapters (a table larger than the shared-memory copy takes), four of them used
+    N, M, R, ell = 96, 128, 32, 1
+    base = [G.make_factors(N, M, R, ell, 1000 + a) for a in range(4)]
+    adapters = [base[a % 4] for a in range(160)]
+    T = 20
+    xb = G.make_x(T, M, 1001)
+    off = [0, 3, 11, 12, 20]
+    ad = [159, 2, 80, 41]
+    got, st = run_segmented(cuda_lib, adapters, N, M, R, ell, xb, off, ad)
+    assert st == 0
+    y, _ = O.matmul_segmented(xb, adapters, off, ad)
+    U.assert_close(got, y, "large adapter table")
