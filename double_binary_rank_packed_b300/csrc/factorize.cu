@@ -90,11 +90,14 @@ __global__ void __launch_bounds__(256, 2) fz_gemm_nt_kernel(int m, int n, int kk
             fz_cp_async_4(bs + r, vb ? B + int64_t(gb) * ldb + gt : B, vb);
         }
     };
-    float acc[8][8];
+    // accumulators in column pairs: one paired fp32 FMA (__ffma2_rn: two fused multiply-adds,
+    // each rounded to nearest as fmaf is) updates two outputs, which halves the FMA
+    // instructions of a kernel whose issue slots, not its FMA pipe, were the limit
+    float2 acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int q = 0; q < 4; ++q) acc[i][q] = make_float2(0.f, 0.f);
 
     const int nsteps = (kk + kGemmBK - 1) / kGemmBK;
     issue(0, 0);
@@ -115,11 +118,14 @@ __global__ void __launch_bounds__(256, 2) fz_gemm_nt_kernel(int m, int n, int kk
             const float4 b0 = *reinterpret_cast<const float4 *>(bs + t * kGemmPitch + tx * 4);
             const float4 b1 = *reinterpret_cast<const float4 *>(bs + t * kGemmPitch + 64 + tx * 4);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                                  make_float2(b1.z, b1.w)};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
+                const float2 ai = make_float2(av[i], av[i]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int q = 0; q < 4; ++q) acc[i][q] = __ffma2_rn(ai, bp[q], acc[i][q]);
+            }
         }
     }
     fz_cp_async_wait<0>();
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(256, 2) fz_gemm_nt_kernel(int m, int n, int kk
             const int gc = col0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
             if (gc >= n) continue;
             float *c = C + int64_t(gr) * ldc + gc;
-            const float v = alpha * acc[i][j];
+            const float v = alpha * ((j & 1) ? acc[i][j >> 1].y : acc[i][j >> 1].x);
             *c = (beta != 0.f) ? fmaf(beta, *c, v) : v;
         }
     }
