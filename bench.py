@@ -444,7 +444,9 @@ class FactorizeWorkload:
         self.bound = "alu"
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         self.alu_peak_tflops = sms * FP32_LANES_PER_SM * 2 * MAX_SM_MHZ * 1e6 / 1e12
-        self.alu_peak_source = f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x {MAX_SM_MHZ} MHz"
+        self.alu_peak_source = (f"derived: {sms} SMs x {FP32_LANES_PER_SM} fp32 lanes x 2 x {MAX_SM_MHZ} MHz "
+                                "(the fp32 engine; the round's P-update GEMMs run on the tf32 tensor cores, three "
+                                "products per term)")
 
     def capture(self):
         self.dbf.factorize(self.W, *self.f, outer=1, workspace=self.ws, **FACT_SCHED)

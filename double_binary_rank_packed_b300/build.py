@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libdbf.so")
 # the debug build (bounds checks in the kernels, see in_range in csrc/common.cuh)
 LIB_DEBUG = os.path.join(HERE, "libdbf_debug.so")
-SOURCES = ["dbf_api.cu", "decode.cu", "decode_rs.cu", "prefill.cu", "misc.cu", "noalloc.cu", "factorize.cu"]
+SOURCES = ["dbf_api.cu", "decode.cu", "decode_rs.cu", "prefill.cu", "misc.cu", "noalloc.cu", "factorize.cu", "factorize_tc.cu"]
 HEADERS = ["common.cuh", "decode_frag.cuh", "kernels.h", "factorize.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

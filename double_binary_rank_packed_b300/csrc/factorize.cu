@@ -396,26 +396,34 @@ __global__ void fz_fill_kernel(float *v, int k, float value) {
 //   else:  UY = Y - z,    RHS = Cw + rho (z - UY)
 // Grid: x over column blocks of 256, y over rows.
 __global__ void __launch_bounds__(256) fz_dual_rhs_kernel(const float *__restrict__ Cw, float *UY,
-                                                          float *__restrict__ RHS, const int8_t *__restrict__ S0,
-                                                          const float *__restrict__ r, const float *__restrict__ c,
-                                                          const float *__restrict__ rho_p, int k, int init) {
+                                                          float *__restrict__ RHS3, int64_t ld3,
+                                                          const int8_t *__restrict__ S0, const float *__restrict__ r,
+                                                          const float *__restrict__ c, const float *__restrict__ rho_p,
+                                                          int k, int init) {
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= k) return;
     const int i = blockIdx.y;
     const int64_t e = int64_t(i) * k + j;
     const float rho = *rho_p;
     const float rc = r[i] * c[j];
+    float v;
     if (init) {
         const float z = float(S0[e]) * rc;
         UY[e] = 0.f;
-        RHS[e] = fmaf(rho, z, Cw[e]);
+        v = fmaf(rho, z, Cw[e]);
     } else {
         const float y = UY[e];
         const float z = y >= 0.f ? rc : -rc;
         const float un = y - z;
         UY[e] = un;
-        RHS[e] = fmaf(rho, z - un, Cw[e]);
+        v = fmaf(rho, z - un, Cw[e]);
     }
+    // the right-hand side in the split form of the tensor-core P-update: [hi | hi | lo]
+    const float hi = tf32_rna(v), lo = tf32_rna(v - hi);
+    float *o = RHS3 + int64_t(i) * ld3;
+    o[j] = hi;
+    o[k + j] = hi;
+    o[2 * k + j] = lo;
 }
 
 // Importance weighting: W'[i][j] = d_out[i] * W[i][j] * d_in[j].  Grid: x over
@@ -455,7 +463,7 @@ cudaError_t gemm_nt(int m, int n, int kk, float alpha, const float *A, int64_t l
 
 // Scratch of one factorization, carved from the caller's workspace.
 struct FzScratch {
-    float *Wt, *F, *G, *LinvT, *Ginv, *Cw, *UY, *RHS, *u, *part, *rho;
+    float *Wt, *F, *G, *LinvT, *Ginv, *Cw, *UY, *RHS3, *Ginv3, *u, *part, *rho;
     int8_t *Bt;
 };
 
@@ -476,7 +484,9 @@ size_t carve(void *base, int64_t N, int64_t M, int64_t k, FzScratch *s) {
     t.Ginv = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * k));
     t.Cw = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * k));
     t.UY = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * k));
-    t.RHS = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * k));
+    // the P-update's operands in the split form of the tensor-core GEMM
+    t.RHS3 = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * tc_split_ld(int(k))));
+    t.Ginv3 = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * tc_split_ld(int(k))));
     t.u = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax)));
     t.part = reinterpret_cast<float *>(take(sizeof(float) * size_t(kMaxColChunks) * k));
     t.rho = reinterpret_cast<float *>(take(sizeof(float) * 4));
@@ -492,9 +502,9 @@ int step_launches(int k, int inner, int power_iters) {
     if (inner <= 0) return 0;
     const int chol = 3 * chol_steps(k) - 2;  // the last block has no panel and no trailing update
     const int svid = (power_iters > 0 ? 3 * power_iters : 1) + 1;
-    // F, F F^T, ridge; Cholesky; L^-T rows, inverse and its mirror, T F^T, first dual pass;
-    // per iteration the P-update GEMM, the SVID passes and (but the last) a dual pass
-    return 3 + chol + 5 + inner * (1 + svid) + (inner - 1);
+    // F, F F^T, ridge; Cholesky; L^-T rows, inverse, its mirror and its split form, T F^T, first
+    // dual pass; per iteration the P-update GEMM, the SVID passes and (but the last) a dual pass
+    return 3 + chol + 6 + inner * (1 + svid) + (inner - 1);
 }
 
 // SVID of Y [n x k]: c (= v) by power iteration, then r = |Y| c; S_out optional.
@@ -548,16 +558,19 @@ cudaError_t admm_step(const float *T, int n, int p, int k, const float *r2, cons
     if ((e = gemm_nt(k, k, k, 1.f, w.LinvT, k, w.LinvT, k, 0.f, w.Ginv, k, s, 1)) != cudaSuccess) return e;
     fz_mirror_lower_kernel<<<dim3(cdiv(k, 32), cdiv(k, 32)), dim3(32, 8), 0, s>>>(w.Ginv, k);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = tc_split3(w.Ginv, k, k, k, w.Ginv3, 1, s)) != cudaSuccess) return e;
+    const int64_t ld3 = tc_split_ld(k);
     if ((e = gemm_nt(n, k, p, 1.f, T, p, w.F, p, 0.f, w.Cw, k, s)) != cudaSuccess) return e;
     const dim3 ew(cdiv(k, 256), n);
-    fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS, S, r, c, w.rho, k, 1);
+    fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS3, ld3, S, r, c, w.rho, k, 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     for (int it = 0; it < prm.inner; ++it) {
         const bool last = it == prm.inner - 1;
-        if ((e = gemm_nt(n, k, k, 1.f, w.RHS, k, w.Ginv, k, 1.f, w.UY, k, s)) != cudaSuccess) return e;
+        // UY += RHS (F F^T + rho I)^-1 on the tensor cores (three tf32 products per term)
+        if ((e = tc_gemm_nt_split(n, k, k, 1.f, w.RHS3, w.Ginv3, 1.f, w.UY, k, status, s)) != cudaSuccess) return e;
         if ((e = svid(w.UY, n, k, prm.power_iters, w, r, c, last ? S : nullptr, s)) != cudaSuccess) return e;
         if (!last) {
-            fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS, nullptr, r, c, w.rho, k, 0);
+            fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS3, ld3, nullptr, r, c, w.rho, k, 0);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }
@@ -582,6 +595,7 @@ cudaError_t prepare_factorize(int64_t k) {
     cudaError_t e = cudaFuncSetAttribute(fz_gemm_nt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kGemmSmem));
     if (e != cudaSuccess) return e;
+    if ((e = tc_prepare()) != cudaSuccess) return e;
     const size_t smem = factorize_tri_smem(k);
     if (smem <= 48 * 1024) return cudaSuccess;
     return cudaFuncSetAttribute(fz_tri_inv_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
