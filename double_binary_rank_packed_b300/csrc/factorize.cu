@@ -17,9 +17,11 @@
 // and F = Q = diag(mR) B diag(b); the B-step is the same step on W^T with
 // F = P^T, whose result is Q^T = diag(b) B^T diag(mR).
 //
-// Everything is fp32.  The contractions (F F^T, T F^T, the inverse, the
-// P-update) run on a shared-memory-tiled SIMT GEMM: this is an optimiser
-// step that needs fp32 products, not a reduced-precision tensor-core one.
+// Everything is fp32-accurate: this is an optimiser step that needs fp32
+// products, not reduced-precision ones.  The P-update runs on the tensor
+// cores with each operand split into two tf32 parts and three products per
+// term (factorize_tc.cu), which keeps fp32 accuracy; the other contractions
+// (F F^T, T F^T, the inverse) run on a shared-memory-tiled SIMT GEMM.
 // (F F^T + rho I)^-1 is formed once per step (blocked Cholesky, triangular
 // inverse, then the lower triangle of L^-T L^-1 as an NT product, mirrored,
 // so it is exactly symmetric and the P-update can read it in the NT layout),
