@@ -18,10 +18,11 @@
 // F = P^T, whose result is Q^T = diag(b) B^T diag(mR).
 //
 // Everything is fp32-accurate: this is an optimiser step that needs fp32
-// products, not reduced-precision ones.  The P-update runs on the tensor
-// cores with each operand split into two tf32 parts and three products per
-// term (factorize_tc.cu), which keeps fp32 accuracy; the other contractions
-// (F F^T, T F^T, the inverse) run on a shared-memory-tiled SIMT GEMM.
+// products, not reduced-precision ones.  The P-update and T F^T run on the
+// tensor cores with each operand split into two tf32 parts and three
+// products per term (factorize_tc.cu), which keeps fp32 accuracy; F F^T and
+// the inverse, whose errors the condition number amplifies, run on a
+// shared-memory-tiled SIMT GEMM.
 // (F F^T + rho I)^-1 is formed once per step (blocked Cholesky, triangular
 // inverse, then the lower triangle of L^-T L^-1 as an NT product, mirrored,
 // so it is exactly symmetric and the P-update can read it in the NT layout),
@@ -398,13 +399,19 @@ __global__ void fz_fill_kernel(float *v, int k, float value) {
 //   else:  UY = Y - z,    RHS = Cw + rho (z - UY)
 // Grid: x over column blocks of 256, y over rows.
 __global__ void __launch_bounds__(256) fz_dual_rhs_kernel(const float *__restrict__ Cw, float *UY,
-                                                          float *__restrict__ RHS3, int64_t ld3,
+                                                          float *__restrict__ RHS2, int k2,
                                                           const int8_t *__restrict__ S0, const float *__restrict__ r,
                                                           const float *__restrict__ c, const float *__restrict__ rho_p,
                                                           int k, int init) {
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= k) return;
+    if (j >= k2) return;
     const int i = blockIdx.y;
+    float *o = RHS2 + int64_t(i) * 2 * k2;  // the right-hand side in split form [hi | lo]
+    if (j >= k) {
+        o[j] = 0.f;
+        o[k2 + j] = 0.f;
+        return;
+    }
     const int64_t e = int64_t(i) * k + j;
     const float rho = *rho_p;
     const float rc = r[i] * c[j];
@@ -420,12 +427,9 @@ __global__ void __launch_bounds__(256) fz_dual_rhs_kernel(const float *__restric
         UY[e] = un;
         v = fmaf(rho, z - un, Cw[e]);
     }
-    // the right-hand side in the split form of the tensor-core P-update: [hi | hi | lo]
-    const float hi = tf32_rna(v), lo = tf32_rna(v - hi);
-    float *o = RHS3 + int64_t(i) * ld3;
+    const float hi = tf32_rna(v);
     o[j] = hi;
-    o[k + j] = hi;
-    o[2 * k + j] = lo;
+    o[k2 + j] = tf32_rna(v - hi);
 }
 
 // Importance weighting: W'[i][j] = d_out[i] * W[i][j] * d_in[j].  Grid: x over
@@ -465,7 +469,10 @@ cudaError_t gemm_nt(int m, int n, int kk, float alpha, const float *A, int64_t l
 
 // Scratch of one factorization, carved from the caller's workspace.
 struct FzScratch {
-    float *Wt, *F, *G, *LinvT, *Ginv, *Cw, *UY, *RHS3, *Ginv3, *u, *part, *rho;
+    float *Wt, *F, *G, *LinvT, *Ginv, *Cw, *UY, *u, *part, *rho;
+    // split forms [hi | lo] of the tensor-core GEMMs' operands: W, W^T, F, the inverse and the
+    // right-hand side
+    float *W2, *Wt2, *F2, *Ginv2, *RHS2;
     int8_t *Bt;
 };
 
@@ -486,9 +493,12 @@ size_t carve(void *base, int64_t N, int64_t M, int64_t k, FzScratch *s) {
     t.Ginv = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * k));
     t.Cw = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * k));
     t.UY = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * k));
-    // the P-update's operands in the split form of the tensor-core GEMM
-    t.RHS3 = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * tc_split_ld(int(k))));
-    t.Ginv3 = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * tc_split_ld(int(k))));
+    const size_t k2 = 2 * size_t(tc_split_half(int(k))), n2 = 2 * size_t(tc_split_half(int(nmax)));
+    t.W2 = reinterpret_cast<float *>(take(sizeof(float) * size_t(N) * 2 * tc_split_half(int(M))));
+    t.Wt2 = reinterpret_cast<float *>(take(sizeof(float) * size_t(M) * 2 * tc_split_half(int(N))));
+    t.F2 = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * n2));
+    t.Ginv2 = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * k2));
+    t.RHS2 = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax) * k2));
     t.u = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax)));
     t.part = reinterpret_cast<float *>(take(sizeof(float) * size_t(kMaxColChunks) * k));
     t.rho = reinterpret_cast<float *>(take(sizeof(float) * 4));
@@ -504,9 +514,10 @@ int step_launches(int k, int inner, int power_iters) {
     if (inner <= 0) return 0;
     const int chol = 3 * chol_steps(k) - 2;  // the last block has no panel and no trailing update
     const int svid = (power_iters > 0 ? 3 * power_iters : 1) + 1;
-    // F, F F^T, ridge; Cholesky; L^-T rows, inverse, its mirror and its split form, T F^T, first
-    // dual pass; per iteration the P-update GEMM, the SVID passes and (but the last) a dual pass
-    return 3 + chol + 6 + inner * (1 + svid) + (inner - 1);
+    // F and its split form, F F^T, ridge; Cholesky; L^-T rows, inverse, its mirror and its split
+    // form, T F^T, first dual pass; per iteration the P-update GEMM, the SVID passes and (but the
+    // last) a dual pass
+    return 4 + chol + 6 + inner * (1 + svid) + (inner - 1);
 }
 
 // SVID of Y [n x k]: c (= v) by power iteration, then r = |Y| c; S_out optional.
@@ -531,14 +542,20 @@ cudaError_t svid(const float *Y, int n, int k, int power_iters, const FzScratch 
 
 // One alternating step: the left factor (r, S [n x k], c) of T [n x p] ~ P F
 // with F built from the other side's factor (r2 [p], S2 [p x k], c2 [k]).
-cudaError_t admm_step(const float *T, int n, int p, int k, const float *r2, const int8_t *S2, const float *c2,
+// T2 is T in the split form of the tensor-core GEMM.
+cudaError_t admm_step(const float *T2, int n, int p, int k, const float *r2, const int8_t *S2, const float *c2,
                       float *r, int8_t *S, float *c, const dbf_factorize_params &prm, const FzScratch &w,
                       int *status, cudaStream_t s) {
     if (prm.inner <= 0) return cudaSuccess;
     cudaError_t e;
     fz_build_f_kernel<<<dim3(cdiv(k, 32), cdiv(p, 32)), dim3(32, 8), 0, s>>>(r2, S2, c2, p, k, w.F);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // F F^T: the Cholesky steps read only its lower triangle (and the diagonal)
+    if ((e = tc_split2(w.F, p, k, p, w.F2, s)) != cudaSuccess) return e;
+    // F F^T: the Cholesky steps read only its lower triangle (and the diagonal).  On the SIMT
+    // GEMM, as the inverse product below: an error in F F^T reaches the inverse multiplied by its
+    // condition number (up to k / rho_rel + 1), and the three-product tensor-core sum moved
+    // enough sign decisions downstream to fail the oracle's agreement bands (98.9% of B's signs
+    // after two weighted rounds at 300 x 260, k = 130, against 99%)
     if ((e = gemm_nt(k, k, p, 1.f, w.F, p, w.F, p, 0.f, w.G, k, s, 1)) != cudaSuccess) return e;
     fz_ridge_kernel<<<1, 1024, 0, s>>>(w.G, k, prm.rho_rel, w.rho);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -560,19 +577,19 @@ cudaError_t admm_step(const float *T, int n, int p, int k, const float *r2, cons
     if ((e = gemm_nt(k, k, k, 1.f, w.LinvT, k, w.LinvT, k, 0.f, w.Ginv, k, s, 1)) != cudaSuccess) return e;
     fz_mirror_lower_kernel<<<dim3(cdiv(k, 32), cdiv(k, 32)), dim3(32, 8), 0, s>>>(w.Ginv, k);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = tc_split3(w.Ginv, k, k, k, w.Ginv3, 1, s)) != cudaSuccess) return e;
-    const int64_t ld3 = tc_split_ld(k);
-    if ((e = gemm_nt(n, k, p, 1.f, T, p, w.F, p, 0.f, w.Cw, k, s)) != cudaSuccess) return e;
-    const dim3 ew(cdiv(k, 256), n);
-    fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS3, ld3, S, r, c, w.rho, k, 1);
+    if ((e = tc_split2(w.Ginv, k, k, k, w.Ginv2, s)) != cudaSuccess) return e;
+    if ((e = tc_gemm_nt_split(n, k, p, 1.f, T2, w.F2, 0.f, w.Cw, k, status, s)) != cudaSuccess) return e;
+    const int k2 = tc_split_half(k);
+    const dim3 ew(cdiv(k2, 256), n);
+    fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS2, k2, S, r, c, w.rho, k, 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     for (int it = 0; it < prm.inner; ++it) {
         const bool last = it == prm.inner - 1;
         // UY += RHS (F F^T + rho I)^-1 on the tensor cores (three tf32 products per term)
-        if ((e = tc_gemm_nt_split(n, k, k, 1.f, w.RHS3, w.Ginv3, 1.f, w.UY, k, status, s)) != cudaSuccess) return e;
+        if ((e = tc_gemm_nt_split(n, k, k, 1.f, w.RHS2, w.Ginv2, 1.f, w.UY, k, status, s)) != cudaSuccess) return e;
         if ((e = svid(w.UY, n, k, prm.power_iters, w, r, c, last ? S : nullptr, s)) != cudaSuccess) return e;
         if (!last) {
-            fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS3, ld3, nullptr, r, c, w.rho, k, 0);
+            fz_dual_rhs_kernel<<<ew, 256, 0, s>>>(w.Cw, w.UY, w.RHS2, k2, nullptr, r, c, w.rho, k, 0);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }
@@ -587,8 +604,8 @@ int factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_
     (void)N;
     (void)M;
     if (p.outer <= 0 || p.inner <= 0) return 0;
-    // transposes of W and B in, the rounds, the transpose of B out
-    return 2 + p.outer * 2 * step_launches(int(k), p.inner, p.power_iters) + 1;
+    // transposes of W and B in, the split forms of W and W^T, the rounds, the transpose of B out
+    return 4 + p.outer * 2 * step_launches(int(k), p.inner, p.power_iters) + 1;
 }
 
 size_t factorize_tri_smem(int64_t k) { return sizeof(float) * size_t(k); }
@@ -642,11 +659,14 @@ cudaError_t launch_factorize(const float *W, int N, int M, int k, const dbf_fact
     fz_transpose_kernel<float><<<dim3(cdiv(M, 32), cdiv(N, 32)), dim3(32, 8), 0, s>>>(W, N, M, w.Wt);
     fz_transpose_kernel<int8_t><<<dim3(cdiv(M, 32), cdiv(k, 32)), dim3(32, 8), 0, s>>>(B, k, M, w.Bt);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = tc_split2(W, M, N, M, w.W2, s)) != cudaSuccess) return e;
+    if ((e = tc_split2(w.Wt, N, M, N, w.Wt2, s)) != cudaSuccess) return e;
     for (int o = 0; o < p.outer; ++o) {
         // A-step: W ~ P Q with Q^T = diag(b) B^T diag(mR) fixed.
-        if ((e = admm_step(W, N, M, k, b, w.Bt, m_right, a, A, m_left, p, w, status, s)) != cudaSuccess) return e;
+        if ((e = admm_step(w.W2, N, M, k, b, w.Bt, m_right, a, A, m_left, p, w, status, s)) != cudaSuccess)
+            return e;
         // B-step: W^T ~ Q^T P^T with P = diag(a) A diag(mL) fixed.
-        if ((e = admm_step(w.Wt, M, N, k, a, A, m_left, b, w.Bt, m_right, p, w, status, s)) != cudaSuccess)
+        if ((e = admm_step(w.Wt2, M, N, k, a, A, m_left, b, w.Bt, m_right, p, w, status, s)) != cudaSuccess)
             return e;
     }
     fz_transpose_kernel<int8_t><<<dim3(cdiv(k, 32), cdiv(M, 32)), dim3(32, 8), 0, s>>>(w.Bt, M, k, B);

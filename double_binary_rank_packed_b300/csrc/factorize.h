@@ -26,17 +26,17 @@ cudaError_t launch_factorize_weighted(const float *W, int N, int M, int k, const
                                       float *m_right, int8_t *B, float *b, void *workspace, int *status,
                                       cudaStream_t s);
 
-// Tensor-core GEMM of the P-update (factorize_tc.cu).  Operands in split
-// form: X3 rows of tc_split_ld(kk) floats holding [hi | hi | lo] (mode 0,
-// the left operand) or [hi | lo | hi] (mode 1, the right one) of X's row,
-// hi = tf32(x), lo = tf32(x - hi).  tc_gemm_nt_split computes
-// C = alpha * A B^T + beta * C from A3 [m rows] and B3 [n rows] with three
-// tf32 products per term (fp32 accuracy) on tcgen05; a timeout of one of its
-// bounded waits records DBF_ERR_TIMEOUT in *status.
+// Tensor-core GEMM of the factorization (factorize_tc.cu).  Operands in
+// split form: X2 rows of 2 * tc_split_half(kk) floats, [hi | lo] of X's row
+// (hi = tf32(x), lo = tf32(x - hi), each half zero past kk).
+// tc_gemm_nt_split computes C = alpha * A B^T + beta * C from A2 [m rows] and
+// B2 [n rows] with three tf32 products per term (fp32 accuracy) on tcgen05;
+// with `lower` set, tiles wholly above the diagonal are skipped.  A timeout of
+// one of its bounded waits records DBF_ERR_TIMEOUT in *status.
 cudaError_t tc_prepare();  // the GEMM's shared-memory attribute, before its first launch on a device
-int64_t tc_split_ld(int kk);
-cudaError_t tc_split3(const float *X, int64_t ldx, int rows, int kk, float *X3, int mode, cudaStream_t s);
-cudaError_t tc_gemm_nt_split(int m, int n, int kk, float alpha, const float *A3, const float *B3, float beta,
-                             float *C, int64_t ldc, int *status, cudaStream_t s);
+int tc_split_half(int kk);
+cudaError_t tc_split2(const float *X, int64_t ldx, int rows, int kk, float *X2, cudaStream_t s);
+cudaError_t tc_gemm_nt_split(int m, int n, int kk, float alpha, const float *A2, const float *B2, float beta,
+                             float *C, int64_t ldc, int *status, cudaStream_t s, int lower = 0);
 
 }  // namespace dbfk

@@ -1,17 +1,18 @@
 // Tensor-core GEMM of the double binary factorization (DBF page, section 2,
 // "Factorización"; the ADMM P-update Y = RHS (F F^T + rho I)^-1 of each
-// iteration): C = alpha * A B^T + beta * C with fp32 A [m x kk], B [n x kk]
+// iteration, and T F^T): C = alpha * A B^T + beta * C with fp32 A [m x kk], B [n x kk]
 // in memory, on tcgen05.mma kind::tf32 with fp32 accumulation in tensor
 // memory.
 //
 // fp32 accuracy from tf32 products: every operand x is split into
 // hi = tf32(x) and lo = tf32(x - hi), and A B^T is taken as
 // A_hi B_hi^T + A_hi B_lo^T + A_lo B_hi^T (the lo * lo term is below fp32's
-// resolution).  The three products are laid side by side along K:
-// A3 = [A_hi | A_hi | A_lo] and B3 = [B_hi | B_lo | B_hi], each row 3*kk
-// long, so one plain tf32 GEMM over K = 3*kk sums them.  The split operands
-// are written by the kernels that produce A and B (fz_split3_kernel here,
-// and the dual pass of factorize.cu for the right-hand side).
+// resolution).  A matrix in split form holds each row as [hi | lo], each
+// half kk2 = kk rounded up to 32 wide (zero past kk), so one split serves as
+// either operand; the kernel runs the three products as three passes over K
+// that read the (hi, hi), (hi, lo) and (lo, hi) halves, all accumulating
+// into one TMEM tile.  The split forms are written by fz_split2_kernel here
+// and by the dual pass of factorize.cu for the right-hand side.
 //
 // Tile 128 x 256 (one CTA per SM: a 4-stage TMA ring of 48 KB stages), K step
 // 32 fp32 (one 128-byte swizzle row); warp 0 loads the ring with TMA, warp 1
@@ -57,7 +58,7 @@ __device__ __forceinline__ void tc_mma_ss_tf32(uint32_t d_tmem, uint64_t a_desc,
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     fz_tc_gemm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap b_map, int m,
-                      int n, int k3, float alpha, float beta, float *C, int64_t ldc, int *status) {
+                      int n, int kk2, float alpha, float beta, float *C, int64_t ldc, int lower, int *status) {
     extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -72,7 +73,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = blockIdx.y * kTcBM, col0 = blockIdx.x * kTcBN;
-    const int nk = (k3 + kTcBK - 1) / kTcBK;
+    if (lower && col0 >= row0 + kTcBM) return;  // the whole tile is above the diagonal
+    const int kpass = kk2 / kTcBK;              // K steps of one product
+    const int nk = 3 * kpass;                   // (hi, hi), (hi, lo), (lo, hi)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
@@ -110,9 +113,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (elect_one()) {
                 unsigned char *st = smem + s * kTcStageBytes;
+                const int pass = ks / kpass, kin = (ks - pass * kpass) * kTcBK;
+                const int xa = (pass == 2 ? kk2 : 0) + kin, xb = (pass == 1 ? kk2 : 0) + kin;
                 mbar_arrive_expect_tx(&full[s], kTcStageBytes);
-                tma_load_2d(st, &a_map, &full[s], ks * kTcBK, row0);
-                tma_load_2d(st + kTcABytes, &b_map, &full[s], ks * kTcBK, col0);
+                tma_load_2d(st, &a_map, &full[s], xa, row0);
+                tma_load_2d(st + kTcABytes, &b_map, &full[s], xb, col0);
             }
             __syncwarp();
             ++issued;
@@ -205,19 +210,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-// B3[c] = [hi(B[c]) | lo(B[c]) | hi(B[c])] (mode 1) or A3[r] = [hi | hi | lo]
-// (mode 0), each part kk wide, rows ld3 apart.  Grid: x over column blocks
-// of 256, y over rows.
-__global__ void __launch_bounds__(256) fz_split3_kernel(const float *__restrict__ X, int64_t ldx, int kk,
-                                                        float *__restrict__ X3, int64_t ld3, int mode) {
+// X2[r] = [hi(X[r]) | lo(X[r])], each half kk2 wide, zero past kk.  Grid: x
+// over column blocks of 256 (covering kk2), y over rows.
+__global__ void __launch_bounds__(256) fz_split2_kernel(const float *__restrict__ X, int64_t ldx, int kk,
+                                                        float *__restrict__ X2, int kk2) {
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= kk) return;
-    const float x = X[int64_t(blockIdx.y) * ldx + j];
+    if (j >= kk2) return;
+    const float x = j < kk ? X[int64_t(blockIdx.y) * ldx + j] : 0.f;
     const float hi = tf32_rna(x), lo = tf32_rna(x - hi);
-    float *o = X3 + int64_t(blockIdx.y) * ld3;
+    float *o = X2 + int64_t(blockIdx.y) * 2 * kk2;
     o[j] = hi;
-    o[kk + j] = mode ? lo : hi;
-    o[2 * kk + j] = mode ? hi : lo;
+    o[kk2 + j] = lo;
 }
 
 bool encode_f32_map(CUtensorMap *map, const float *base, int rows, int cols, int64_t ld, int box_rows) {
@@ -247,23 +250,25 @@ cudaError_t tc_prepare() {
     return cudaFuncSetAttribute(fz_tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTcSmem));
 }
 
-int64_t tc_split_ld(int kk) { return (int64_t(3) * kk + 3) & ~int64_t(3); }
+int tc_split_half(int kk) { return (kk + kTcBK - 1) / kTcBK * kTcBK; }
 
-cudaError_t tc_split3(const float *X, int64_t ldx, int rows, int kk, float *X3, int mode, cudaStream_t s) {
+cudaError_t tc_split2(const float *X, int64_t ldx, int rows, int kk, float *X2, cudaStream_t s) {
     if (rows <= 0 || kk <= 0) return cudaSuccess;
-    fz_split3_kernel<<<dim3((kk + 255) / 256, rows), 256, 0, s>>>(X, ldx, kk, X3, tc_split_ld(kk), mode);
+    const int kk2 = tc_split_half(kk);
+    fz_split2_kernel<<<dim3((kk2 + 255) / 256, rows), 256, 0, s>>>(X, ldx, kk, X2, kk2);
     return cudaGetLastError();
 }
 
-cudaError_t tc_gemm_nt_split(int m, int n, int kk, float alpha, const float *A3, const float *B3, float beta, float *C,
-                             int64_t ldc, int *status, cudaStream_t s) {
+cudaError_t tc_gemm_nt_split(int m, int n, int kk, float alpha, const float *A2, const float *B2, float beta, float *C,
+                             int64_t ldc, int *status, cudaStream_t s, int lower) {
     if (m <= 0 || n <= 0) return cudaSuccess;
-    const int64_t ld3 = tc_split_ld(kk);
+    const int kk2 = tc_split_half(kk);
     CUtensorMap a_map, b_map;
-    if (!encode_f32_map(&a_map, A3, m, 3 * kk, ld3, kTcBM) || !encode_f32_map(&b_map, B3, n, 3 * kk, ld3, kTcBN))
+    if (!encode_f32_map(&a_map, A2, m, 2 * kk2, 2 * int64_t(kk2), kTcBM) ||
+        !encode_f32_map(&b_map, B2, n, 2 * kk2, 2 * int64_t(kk2), kTcBN))
         return cudaErrorInvalidValue;
     const dim3 grid((n + kTcBN - 1) / kTcBN, (m + kTcBM - 1) / kTcBM);
-    fz_tc_gemm_kernel<<<grid, kTcThreads, kTcSmem, s>>>(a_map, b_map, m, n, 3 * kk, alpha, beta, C, ldc, status);
+    fz_tc_gemm_kernel<<<grid, kTcThreads, kTcSmem, s>>>(a_map, b_map, m, n, kk2, alpha, beta, C, ldc, lower, status);
     return cudaGetLastError();
 }
 

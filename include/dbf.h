@@ -401,9 +401,9 @@ typedef struct dbf_factorize_params {
  *                   right factor, fixed in the first A-step, overwritten
  *   workspace  device, >= dbf_factorize_workspace_bytes(N, M, k), 256-byte
  *              aligned, not shared with concurrent calls
- * Computes to fp32 accuracy: the P-update products on the tensor cores from
- * operands split into two tf32 parts (three products per term), the other
- * contractions on fp32 SIMT GEMMs, a blocked Cholesky; the reductions have a
+ * Computes to fp32 accuracy: the P-update and T F^T products on the tensor
+ * cores from operands split into two tf32 parts (three products per term),
+ * F F^T and the inverse on fp32 SIMT GEMMs, a blocked Cholesky; the reductions have a
  * fixed order, so a rerun gives the same bits.  Limits: 1 <= N, M <= 65535,
  * 1 <= k <= 16384, else DBF_ERR_UNSUPPORTED; null pointers or params out of
  * range give DBF_ERR_INVALID_ARG.  Asynchronous on `stream`; a pivot that
