@@ -1102,4 +1102,34 @@ int dbf_selftest_bounded_wait(int64_t limit_us, void *stream) {
     return e == cudaSuccess ? DBF_OK : cuda_fail(e, "dbf_selftest_bounded_wait");
 }
 
+size_t dbf_selftest_split_gemm_workspace_bytes(int32_t m, int32_t n, int32_t kk) {
+    if (m < 1 || n < 1 || kk < 1 || m > 65535 || n > 65535 || kk > 65535) return 0;
+    const size_t half = static_cast<size_t>(dbfk::tc_split_half(kk));
+    const size_t a = (sizeof(float) * size_t(m) * 2 * half + 255) & ~size_t(255);
+    return a + sizeof(float) * size_t(n) * 2 * half;
+}
+
+int dbf_selftest_split_gemm(int32_t m, int32_t n, int32_t kk, float alpha, const float *A, int64_t lda,
+                            const float *B, int64_t ldb, float beta, float *C, int64_t ldc, int lower,
+                            void *workspace, size_t ws_bytes, void *stream) {
+    if (m < 1 || n < 1 || kk < 1 || !A || !B || !C || (lower != 0 && lower != 1)) return DBF_ERR_INVALID_ARG;
+    if (m > 65535 || n > 65535 || kk > 65535) return DBF_ERR_UNSUPPORTED;
+    if (lda < kk || ldb < kk || ldc < n) return DBF_ERR_INVALID_ARG;
+    const size_t need = dbf_selftest_split_gemm_workspace_bytes(m, n, kk);
+    if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return DBF_ERR_ALIGNMENT;
+    int *st = status_ptr();
+    if (!st) return cuda_fail(cudaGetLastError(), "status word");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = dbfk::tc_prepare();
+    const size_t half = static_cast<size_t>(dbfk::tc_split_half(kk));
+    float *A2 = static_cast<float *>(workspace);
+    float *B2 = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                          ((sizeof(float) * size_t(m) * 2 * half + 255) & ~size_t(255)));
+    if (e == cudaSuccess) e = dbfk::tc_split2(A, lda, m, kk, A2, s);
+    if (e == cudaSuccess) e = dbfk::tc_split2(B, ldb, n, kk, B2, s);
+    if (e == cudaSuccess) e = dbfk::tc_gemm_nt_split(m, n, kk, alpha, A2, B2, beta, C, ldc, st, s, lower);
+    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "dbf_selftest_split_gemm");
+}
+
 }  // extern "C"

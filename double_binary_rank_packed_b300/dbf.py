@@ -49,6 +49,7 @@ EXPORTED = (
     "dbf_grouped_launch_count", "dbf_matmul_hostio_batch", "dbf_hostio_batch_workspace_bytes",
     "dbf_factorize", "dbf_factorize_workspace_bytes", "dbf_factorize_launch_count",
     "dbf_factorize_weighted", "dbf_factorize_weighted_workspace_bytes", "dbf_factorize_weighted_launch_count",
+    "dbf_selftest_split_gemm", "dbf_selftest_split_gemm_workspace_bytes",
 )
 
 
@@ -101,6 +102,9 @@ def _load():
         "dbf_matmul_segmented": (ci, [vp, i32, i32, i32, i32, i32, vp, i64, vp, vp, vp, i32, ci, vp, sz, vp]),
         "dbf_check_status": (ci, [vp]),
         "dbf_selftest_bounded_wait": (ci, [i64, vp]),
+        "dbf_selftest_split_gemm_workspace_bytes": (sz, [i32, i32, i32]),
+        "dbf_selftest_split_gemm": (ci, [i32, i32, i32, ctypes.c_float, vp, i64, vp, i64, ctypes.c_float, vp, i64,
+                                         ci, vp, sz, vp]),
         "dbf_status_string": (ctypes.c_char_p, [ci]),
         "dbf_last_cuda_error": (ctypes.c_char_p, []),
         "dbf_launch_count": (ci, [fp, i64, ci]),
@@ -581,6 +585,25 @@ def check_status(stream=None) -> int:
 
 def selftest_bounded_wait(limit_us: int, stream=None) -> int:
     return int(_lib.dbf_selftest_bounded_wait(limit_us, _stream_handle(stream)))
+
+
+@_on_stream
+def selftest_split_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha: float = 1.0, beta: float = 0.0,
+                        lower: bool = False, stream=None) -> torch.Tensor:
+    """C = alpha A B^T + beta C on the factorization's split-tf32 tensor-core GEMM
+    (dbf_selftest_split_gemm); A [m, kk], B [n, kk], C [m, n], fp32 CUDA tensors, rows contiguous."""
+    for t in (A, B, C):
+        if t.dtype != torch.float32 or t.dim() != 2 or not t.is_cuda or t.stride(1) != 1:
+            raise ValueError("A, B and C must be 2-D fp32 CUDA tensors with contiguous rows")
+    m, kk = A.shape
+    n = B.shape[0]
+    if B.shape[1] != kk or tuple(C.shape) != (m, n):
+        raise ValueError("shapes must be A [m, kk], B [n, kk], C [m, n]")
+    ws = new_workspace(int(_lib.dbf_selftest_split_gemm_workspace_bytes(m, n, kk)), A.device)
+    _check(_lib.dbf_selftest_split_gemm(m, n, kk, alpha, _ptr(A), A.stride(0), _ptr(B), B.stride(0), beta, _ptr(C),
+                                        C.stride(0), int(lower), _ptr(ws), ws.numel(), _stream_handle(stream)),
+           "dbf_selftest_split_gemm")
+    return C
 
 
 # ------------------------------------------------------- no-allocation variant

@@ -333,6 +333,25 @@ int dbf_check_status(void *stream);
 int dbf_selftest_bounded_wait(int64_t limit_us, void *stream);
 
 /*
+ * dbf_selftest_split_gemm: C = alpha * A B^T + beta * C on the tensor-core
+ * GEMM that dbf_factorize uses for its P-update and T F^T (each operand split
+ * into two tf32 parts, three tf32 products per term, fp32 accumulation; DBF
+ * page, section 2, the ADMM P-update).  For tests of that kernel.
+ *   A  device fp32 [m][lda], B device fp32 [n][ldb], C device fp32 [m][ldc]
+ *      (all row-major; K = kk columns of A and B are used)
+ *   lower  1: tiles of C wholly above the diagonal (128 x 256 tiles) are
+ *          left untouched
+ *   workspace  device, >= dbf_selftest_split_gemm_workspace_bytes(m, n, kk),
+ *              256-byte aligned (the split forms of A and B)
+ * 1 <= m, n, kk <= 65535 and lda, ldb >= kk, ldc >= n, else
+ * DBF_ERR_INVALID_ARG / DBF_ERR_UNSUPPORTED.  Asynchronous on `stream`.
+ */
+size_t dbf_selftest_split_gemm_workspace_bytes(int32_t m, int32_t n, int32_t kk);
+int dbf_selftest_split_gemm(int32_t m, int32_t n, int32_t kk, float alpha, const float *A, int64_t lda,
+                            const float *B, int64_t ldb, float beta, float *C, int64_t ldc, int lower,
+                            void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * dbf_matmul_decode_noalloc: dbf_matmul_path(..., DBF_PATH_DECODE) for
  * callers that cannot allocate device memory for a call: serving loops that
  * must never take cudaMalloc's implicit device synchronisation on the token
