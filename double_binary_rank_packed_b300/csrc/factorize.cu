@@ -294,51 +294,74 @@ __global__ void __launch_bounds__(128) fz_chol_panel_kernel(float *G, int k, int
         if (c < nb) row[c] = x[c];
 }
 
-// Row r of L^-T (= column r of L^-1): solve L x = e_r by forward substitution,
-// one warp per row, x staged in dynamic shared memory (k floats).  Rows of L
-// are taken 32 at a time: first the part of each row's sum over the x already
-// known (independent dot products, four rows per pass, loads overlapped),
-// then a 32-step solve with the diagonal block held one row per lane.
-__global__ void __launch_bounds__(32) fz_tri_inv_rows_kernel(const float *__restrict__ L, int k,
-                                                             float *__restrict__ LinvT) {
-    extern __shared__ float xs[];
-    const int r = blockIdx.x, lane = threadIdx.x;
-    float *out = LinvT + int64_t(r) * k;
-    for (int c = lane; c < r; c += 32) out[c] = 0.f;
-    for (int c0 = r; c0 < k; c0 += 32) {
-        const int nb = min(32, k - c0);
-        float s = (c0 == r && lane == 0) ? 1.f : 0.f;  // e_r restricted to rows c0 .. c0 + 31
-        for (int j0 = 0; j0 < nb; j0 += 4) {
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int t = r + lane; t < c0; t += 32) {
-                const float xt = xs[t];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (j0 + q < nb) d[q] = fmaf(L[int64_t(c0 + j0 + q) * k + t], xt, d[q]);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float v = d[q];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == j0 + q) s -= v;
-            }
-        }
-        float lrow[32];  // L[c0 + lane][c0 .. c0 + lane]
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-            lrow[jj] = (lane < nb && jj <= lane) ? L[int64_t(c0 + lane) * k + c0 + jj] : 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            if (jj < nb) {
-                const float xj = __shfl_sync(0xffffffffu, lane == jj ? s / lrow[jj] : 0.f, jj);
-                if (lane > jj) s = fmaf(-lrow[jj], xj, s);
-                if (lane == jj) xs[c0 + jj] = xj;
-            }
-        }
-        __syncwarp();
+// ---------------------------------------------- triangular inverse by blocks
+//
+// X = L^-1 (lower) and Z = L^-T = X^T (upper) of the Cholesky factor L (the
+// lower triangle of G), by recursion on the diagonal: for
+// L = [[L11, 0], [L21, L22]], X = [[X11, 0], [X21, X22]] with
+// X21 = -X22 L21 X11, which two NT GEMMs give from the halves' inverses:
+// Tt = Z11 L21^T (= (L21 X11)^T), then X21 = -X22 Tt^T, and Z12 = X21^T.
+// The leaves (kTriLeaf rows) are solved by forward substitution.  The GEMMs
+// read whole blocks, so X and Z start zeroed.
+
+constexpr int kTriLeaf = 128;
+
+__global__ void __launch_bounds__(256) fz_zero2_kernel(float *a, float *b, int64_t n) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        a[i] = 0.f;
+        b[i] = 0.f;
     }
-    for (int c = r + lane; c < k; c += 32) out[c] = xs[c];
+}
+
+// One leaf block [lo, lo + nb) per CTA, one thread per column c of its
+// inverse: x[i][c] = (delta_ic - sum_{t<i} L[i][t] x[t][c]) / L[i][i] for
+// i >= c (0 above), the block of L and the columns of x in shared memory;
+// then X's block row-major and Z's block as its transpose.
+__global__ void __launch_bounds__(kTriLeaf) fz_tri_leaf_kernel(const float *__restrict__ G, int k,
+                                                               float *__restrict__ X, float *__restrict__ Z) {
+    extern __shared__ float tri_sm[];
+    float *Ls = tri_sm;                              // [kTriLeaf][kTriLeaf + 1]
+    float *xs = tri_sm + kTriLeaf * (kTriLeaf + 1);  // [kTriLeaf][kTriLeaf + 1]
+    constexpr int ld = kTriLeaf + 1;
+    const int lo = blockIdx.x * kTriLeaf, nb = min(kTriLeaf, k - lo), c = threadIdx.x;
+    for (int e = c; e < nb * kTriLeaf; e += kTriLeaf) {
+        const int i = e / kTriLeaf, t = e - i * kTriLeaf;
+        Ls[i * ld + t] = (t <= i && t < nb) ? G[int64_t(lo + i) * k + lo + t] : 0.f;
+    }
+    __syncthreads();
+    if (c < nb) {
+        for (int i = 0; i < nb; ++i) {
+            float v = 0.f;
+            if (i >= c) {
+                float s = (i == c) ? 1.f : 0.f;
+                for (int t = c; t < i; ++t) s = fmaf(-Ls[i * ld + t], xs[t * ld + c], s);
+                v = s / Ls[i * ld + i];
+            }
+            xs[i * ld + c] = v;
+        }
+    }
+    __syncthreads();
+    for (int i = 0; i < nb; ++i)
+        if (c < nb) X[int64_t(lo + i) * k + lo + c] = xs[i * ld + c];  // row i of the block
+    for (int r = 0; r < nb; ++r)
+        if (c < nb) Z[int64_t(lo + r) * k + lo + c] = xs[c * ld + r];  // row r of Z = column r of x
+}
+
+// out[j][i] = in[i][j] for an rows x cols block with row strides ldi, ldo
+// (32 x 32 tiles, block 32 x 8).
+__global__ void fz_transpose_block_kernel(const float *__restrict__ in, int64_t ldi, int rows, int cols,
+                                          float *__restrict__ out, int64_t ldo) {
+    __shared__ float tile[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int dy = threadIdx.y; dy < 32; dy += 8) {
+        const int r = r0 + dy, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[dy][threadIdx.x] = in[int64_t(r) * ldi + c];
+    }
+    __syncthreads();
+    for (int dy = threadIdx.y; dy < 32; dy += 8) {
+        const int c = c0 + dy, r = r0 + threadIdx.x;
+        if (c < cols && r < rows) out[int64_t(c) * ldo + r] = tile[threadIdx.x][dy];
+    }
 }
 
 // out[i] = sum_j |Y[i][j]| * v[j] (v == null: the constant vconst), one warp
@@ -469,7 +492,7 @@ cudaError_t gemm_nt(int m, int n, int kk, float alpha, const float *A, int64_t l
 
 // Scratch of one factorization, carved from the caller's workspace.
 struct FzScratch {
-    float *Wt, *F, *G, *LinvT, *Ginv, *Cw, *UY, *u, *part, *rho;
+    float *Wt, *F, *G, *LinvT, *Ginv, *Cw, *UY, *u, *part, *rho, *Tt;
     // split forms [hi | lo] of the tensor-core GEMMs' operands: W, W^T, F, the inverse and the
     // right-hand side
     float *W2, *Wt2, *F2, *Ginv2, *RHS2;
@@ -502,6 +525,7 @@ size_t carve(void *base, int64_t N, int64_t M, int64_t k, FzScratch *s) {
     t.u = reinterpret_cast<float *>(take(sizeof(float) * size_t(nmax)));
     t.part = reinterpret_cast<float *>(take(sizeof(float) * size_t(kMaxColChunks) * k));
     t.rho = reinterpret_cast<float *>(take(sizeof(float) * 4));
+    t.Tt = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * k));  // blocked inverse scratch
     t.Bt = reinterpret_cast<int8_t *>(take(size_t(M) * k));
     if (s) *s = t;
     return off;
@@ -509,15 +533,52 @@ size_t carve(void *base, int64_t N, int64_t M, int64_t k, FzScratch *s) {
 
 int chol_steps(int k) { return (k + kCholNB - 1) / kCholNB; }
 
+int tri_leaves(int k) { return (k + kTriLeaf - 1) / kTriLeaf; }
+size_t tri_leaf_smem() { return sizeof(float) * 2 * kTriLeaf * (kTriLeaf + 1); }
+
+// Merge leaves [l0, l1) of the blocked inverse (both halves first).
+cudaError_t tri_merge(const float *G, int k, float *X, float *Z, float *Tt, int l0, int l1, cudaStream_t s) {
+    if (l1 - l0 <= 1) return cudaSuccess;
+    const int lm = l0 + (l1 - l0 + 1) / 2;
+    cudaError_t e;
+    if ((e = tri_merge(G, k, X, Z, Tt, l0, lm, s)) != cudaSuccess) return e;
+    if ((e = tri_merge(G, k, X, Z, Tt, lm, l1, s)) != cudaSuccess) return e;
+    const int lo = l0 * kTriLeaf, mid = lm * kTriLeaf, hi = std::min(k, l1 * kTriLeaf);
+    const int s1 = mid - lo, s2 = hi - mid;
+    // Tt = Z11 L21^T  [s1 x s2]
+    if ((e = gemm_nt(s1, s2, s1, 1.f, Z + int64_t(lo) * k + lo, k, G + int64_t(mid) * k + lo, k, 0.f, Tt, s2, s)) !=
+        cudaSuccess)
+        return e;
+    // X21 = -X22 Tt^T  [s2 x s1]
+    if ((e = gemm_nt(s2, s1, s2, -1.f, X + int64_t(mid) * k + mid, k, Tt, s2, 0.f, X + int64_t(mid) * k + lo, k,
+                     s)) != cudaSuccess)
+        return e;
+    // Z12 = X21^T
+    fz_transpose_block_kernel<<<dim3(cdiv(s1, 32), cdiv(s2, 32)), dim3(32, 8), 0, s>>>(
+        X + int64_t(mid) * k + lo, k, s2, s1, Z + int64_t(lo) * k + mid, k);
+    return cudaGetLastError();
+}
+
+// X = L^-1, Z = L^-T of the lower triangle L of G [k x k].
+cudaError_t tri_inverse(const float *G, int k, float *X, float *Z, float *Tt, cudaStream_t s) {
+    const int64_t kk = int64_t(k) * k;
+    fz_zero2_kernel<<<unsigned(std::min<int64_t>((kk + 255) / 256, 4736)), 256, 0, s>>>(X, Z, kk);
+    fz_tri_leaf_kernel<<<tri_leaves(k), kTriLeaf, tri_leaf_smem(), s>>>(G, k, X, Z);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return tri_merge(G, k, X, Z, Tt, 0, tri_leaves(k), s);
+}
+
 // Launches of one ADMM step (a half of an alternating round).
 int step_launches(int k, int inner, int power_iters) {
     if (inner <= 0) return 0;
     const int chol = 3 * chol_steps(k) - 2;  // the last block has no panel and no trailing update
     const int svid = (power_iters > 0 ? 3 * power_iters : 1) + 1;
-    // F and its split form, F F^T, ridge; Cholesky; L^-T rows, inverse, its mirror and its split
-    // form, T F^T, first dual pass; per iteration the P-update GEMM, the SVID passes and (but the
-    // last) a dual pass
-    return 4 + chol + 6 + inner * (1 + svid) + (inner - 1);
+    // F and its split form, F F^T, ridge; Cholesky; the blocked L^-1 (zero fill, leaves, two GEMMs
+    // and a transpose per merge); inverse, its mirror and its split form, T F^T, first dual pass;
+    // per iteration the P-update GEMM, the SVID passes and (but the last) a dual pass
+    const int tri = 2 + 3 * (tri_leaves(k) - 1);
+    return 4 + chol + tri + 5 + inner * (1 + svid) + (inner - 1);
 }
 
 // SVID of Y [n x k]: c (= v) by power iteration, then r = |Y| c; S_out optional.
@@ -570,9 +631,8 @@ cudaError_t admm_step(const float *T2, int n, int p, int k, const float *r2, con
                 return e;
         }
     }
-    const size_t tri_smem = sizeof(float) * size_t(k);
-    fz_tri_inv_rows_kernel<<<k, 32, tri_smem, s>>>(w.G, k, w.LinvT);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // L^-1 (in Ginv until the product below overwrites it) and L^-T by blocks
+    if ((e = tri_inverse(w.G, k, w.Ginv, w.LinvT, w.Tt, s)) != cudaSuccess) return e;
     // L^-T (L^-T)^T: the lower triangle, then the upper one copied from it
     if ((e = gemm_nt(k, k, k, 1.f, w.LinvT, k, w.LinvT, k, 0.f, w.Ginv, k, s, 1)) != cudaSuccess) return e;
     fz_mirror_lower_kernel<<<dim3(cdiv(k, 32), cdiv(k, 32)), dim3(32, 8), 0, s>>>(w.Ginv, k);
@@ -608,16 +668,18 @@ int factorize_launch_count(int64_t N, int64_t M, int64_t k, const dbf_factorize_
     return 4 + p.outer * 2 * step_launches(int(k), p.inner, p.power_iters) + 1;
 }
 
-size_t factorize_tri_smem(int64_t k) { return sizeof(float) * size_t(k); }
+size_t factorize_tri_smem(int64_t k) {
+    (void)k;
+    return tri_leaf_smem();
+}
 
 cudaError_t prepare_factorize(int64_t k) {
     cudaError_t e = cudaFuncSetAttribute(fz_gemm_nt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kGemmSmem));
     if (e != cudaSuccess) return e;
     if ((e = tc_prepare()) != cudaSuccess) return e;
-    const size_t smem = factorize_tri_smem(k);
-    if (smem <= 48 * 1024) return cudaSuccess;
-    return cudaFuncSetAttribute(fz_tri_inv_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    return cudaFuncSetAttribute(fz_tri_leaf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(factorize_tri_smem(k)));
 }
 
 size_t factorize_weighted_workspace_bytes(int64_t N, int64_t M, int64_t k) {

@@ -135,20 +135,20 @@ def test_factorize_host_checks(lib):
 
 def test_factorize_sizes_and_launch_counts(lib):
     ws = lib.factorize_workspace_bytes(4096, 4096, 1024)
-    # W^T, F, three k x k, two n x k, the split forms ([hi | lo], twice the size) of W, W^T, F,
+    # W^T, F, four k x k, two n x k, the split forms ([hi | lo], twice the size) of W, W^T, F,
     # the inverse and the right-hand side, the sign transpose, small vectors
-    assert ws >= 4 * (5 * 4096 * 4096 + 3 * 1024 * 4096 + 5 * 1024 * 1024 + 4 * 4096 * 1024) + 4096 * 1024
+    assert ws >= 4 * (5 * 4096 * 4096 + 3 * 1024 * 4096 + 6 * 1024 * 1024 + 4 * 4096 * 1024) + 4096 * 1024
     assert ws % 256 == 0
     assert lib.factorize_workspace_bytes(0, 4, 4) == 0
     assert lib.factorize_workspace_bytes(4, 4, 16385) == 0
     # per call: transposes of W and B, split forms of W and W^T, the rounds, transpose of B out.
-    # per step: F and its split form, F F^T, ridge; 3 per 32-column Cholesky block less 2; L^-T,
-    # inverse, its mirror and its split form, T F^T, first dual; per iteration 1 GEMM + 3q + 1
-    # SVID passes, dual between iterations
+    # per step: F and its split form, F F^T, ridge; 3 per 32-column Cholesky block less 2; the
+    # blocked L^-1 (zero fill and one leaf of 128 rows at k = 70); inverse, its mirror and its split
+    # form, T F^T, first dual; per iteration 1 GEMM + 3q + 1 SVID passes, dual between iterations
     k, inner, q = 70, 4, 5
-    step = 4 + (3 * 3 - 2) + 6 + inner * (1 + 3 * q + 1) + (inner - 1)
+    step = 4 + (3 * 3 - 2) + 2 + 5 + inner * (1 + 3 * q + 1) + (inner - 1)
     assert lib.factorize_launch_count(100, 80, k, 3, inner, q, 1.0) == 4 + 3 * 2 * step + 1
-    step0 = 4 + (3 * 3 - 2) + 6 + inner * (1 + 1 + 1) + (inner - 1)   # power_iters = 0: fill + rows
+    step0 = 4 + (3 * 3 - 2) + 2 + 5 + inner * (1 + 1 + 1) + (inner - 1)   # power_iters = 0: fill + rows
     assert lib.factorize_launch_count(100, 80, k, 1, inner, 0, 1.0) == 4 + 2 * step0 + 1
     assert lib.factorize_launch_count(100, 80, k, 0, inner, q, 1.0) == 0
     assert lib.factorize_launch_count(100, 80, k, 1, 0, q, 1.0) == 0
