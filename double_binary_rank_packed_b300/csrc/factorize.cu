@@ -224,60 +224,75 @@ __global__ void __launch_bounds__(1024) fz_ridge_kernel(float *G, int k, float r
     if (threadIdx.x == 0) *rho_out = rho;
 }
 
-// Cholesky of the nb x nb diagonal block at (j0, j0) in place (one warp):
-// lane = row, the row held in registers, column c passed between lanes by
-// shuffles (right-looking: pivot, scale column c, update the columns right of
-// it); the strict upper triangle of the block is zeroed.  A pivot that is not
-// positive records DBF_ERR_NUMERIC and continues with FLT_MIN.
-__global__ void __launch_bounds__(32) fz_chol_diag_kernel(float *G, int k, int j0, int nb, int *status) {
-    __shared__ float T[kCholNB][kCholNB + 1];
-    const int lane = threadIdx.x;
-    if (lane < nb)
-#pragma unroll 8
-        for (int a = 0; a < nb; ++a) T[a][lane] = G[int64_t(j0 + a) * k + j0 + lane];  // row a, coalesced
-    __syncwarp();
-    float row[kCholNB];
-#pragma unroll
-    for (int c = 0; c < kCholNB; ++c) row[c] = (lane < nb && c < nb) ? T[lane][c] : 0.f;
-#pragma unroll
-    for (int c = 0; c < kCholNB; ++c) {
-        if (c < nb) {  // warp-uniform
-            float d = __shfl_sync(0xffffffffu, row[c], c);
-            if (!(d > 0.f)) {
-                if (lane == 0) record_status(status, DBF_ERR_NUMERIC);
-                d = FLT_MIN;
-            }
-            const float sd = sqrtf(d);
-            if (lane == c) row[c] = sd;
-            else if (lane > c) row[c] = row[c] / sd;
-            const float lc = row[c];
-#pragma unroll
-            for (int cc = c + 1; cc < kCholNB; ++cc) {
-                const float lcc = __shfl_sync(0xffffffffu, lc, cc);  // L[cc][c]
-                if (lane >= cc) row[cc] = fmaf(-lc, lcc, row[cc]);
-            }
+// One step of the 32-column right-looking Cholesky, diagonal block and panel in
+// one launch.  Every CTA factors the nb x nb diagonal block at (j0, j0) itself
+// (warp 0: lane = row, the row held in registers, column c passed between
+// lanes by shuffles; a pivot that is not positive records DBF_ERR_NUMERIC and
+// continues with FLT_MIN), then solves its 128 panel rows r >= j0 + nb,
+// x L_jj^T = G[r, j0:j0+nb], by forward substitution (one thread per row).
+// The factored block cannot go back into G in this launch (other CTAs may
+// still be reading the original), so CTA 0 parks it in slot (j0 / 32) & 1 of
+// `park` and the next step's CTA 0 writes it into G, with the strict upper
+// triangle zeroed; the last step (no panel) writes its own block as well.
+__global__ void __launch_bounds__(128) fz_chol_step_kernel(float *G, int k, int j0, int nb, float *park,
+                                                           int *status) {
+    __shared__ float L[kCholNB][kCholNB + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool last = j0 + nb >= k;
+    if (blockIdx.x == 0 && j0 > 0) {
+        // the previous step's factored block into G
+        const float *prev = park + (((j0 / kCholNB) - 1) & 1) * kCholNB * kCholNB;
+        const int pj = j0 - kCholNB;
+        for (int e = tid; e < kCholNB * kCholNB; e += blockDim.x) {
+            const int a = e / kCholNB, b = e - a * kCholNB;
+            G[int64_t(pj + a) * k + pj + b] = (b <= a) ? prev[e] : 0.f;
         }
     }
-    __syncwarp();
-#pragma unroll
-    for (int c = 0; c < kCholNB; ++c) T[lane][c] = row[c];
-    __syncwarp();
-    if (lane < nb)
+    if (warp == 0) {
+        if (lane < nb)
 #pragma unroll 8
-        for (int a = 0; a < nb; ++a) G[int64_t(j0 + a) * k + j0 + lane] = (lane <= a) ? T[a][lane] : 0.f;
-}
-
-// Panel below the diagonal block: row r >= j0 + nb solves x L_jj^T = G[r, j0:j0+nb]
-// by forward substitution (one thread per row).
-__global__ void __launch_bounds__(128) fz_chol_panel_kernel(float *G, int k, int j0, int nb) {
-    __shared__ float L[kCholNB][kCholNB + 1];
-    for (int e = threadIdx.x; e < nb * nb; e += blockDim.x) {
-        const int a = e / nb, b = e - a * nb;
-        L[a][b] = G[int64_t(j0 + a) * k + j0 + b];
+            for (int a = 0; a < nb; ++a) L[a][lane] = G[int64_t(j0 + a) * k + j0 + lane];  // row a, coalesced
+        __syncwarp();
+        float row[kCholNB];
+#pragma unroll
+        for (int c = 0; c < kCholNB; ++c) row[c] = (lane < nb && c < nb) ? L[lane][c] : 0.f;
+#pragma unroll
+        for (int c = 0; c < kCholNB; ++c) {
+            if (c < nb) {  // warp-uniform
+                float d = __shfl_sync(0xffffffffu, row[c], c);
+                if (!(d > 0.f)) {
+                    if (lane == 0 && blockIdx.x == 0) record_status(status, DBF_ERR_NUMERIC);
+                    d = FLT_MIN;
+                }
+                const float sd = sqrtf(d);
+                if (lane == c) row[c] = sd;
+                else if (lane > c) row[c] = row[c] / sd;
+                const float lc = row[c];
+#pragma unroll
+                for (int cc = c + 1; cc < kCholNB; ++cc) {
+                    const float lcc = __shfl_sync(0xffffffffu, lc, cc);  // L[cc][c]
+                    if (lane >= cc) row[cc] = fmaf(-lc, lcc, row[cc]);
+                }
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < kCholNB; ++c) L[lane][c] = row[c];
     }
     __syncthreads();
-    const int r = j0 + nb + blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= k) return;
+    if (blockIdx.x == 0) {
+        if (last) {
+            for (int e = tid; e < nb * nb; e += blockDim.x) {
+                const int a = e / nb, b = e - a * nb;
+                G[int64_t(j0 + a) * k + j0 + b] = (b <= a) ? L[a][b] : 0.f;
+            }
+        } else {
+            float *slot = park + ((j0 / kCholNB) & 1) * kCholNB * kCholNB;
+            for (int e = tid; e < kCholNB * kCholNB; e += blockDim.x) slot[e] = L[e / kCholNB][e % kCholNB];
+        }
+    }
+    const int r = j0 + nb + blockIdx.x * blockDim.x + tid;
+    if (last || r >= k) return;
     float *row = G + int64_t(r) * k + j0;
     float x[kCholNB];
 #pragma unroll
@@ -492,7 +507,7 @@ cudaError_t gemm_nt(int m, int n, int kk, float alpha, const float *A, int64_t l
 
 // Scratch of one factorization, carved from the caller's workspace.
 struct FzScratch {
-    float *Wt, *F, *G, *LinvT, *Ginv, *Cw, *UY, *u, *part, *rho, *Tt;
+    float *Wt, *F, *G, *LinvT, *Ginv, *Cw, *UY, *u, *part, *rho, *Tt, *park;
     // split forms [hi | lo] of the tensor-core GEMMs' operands: W, W^T, F, the inverse and the
     // right-hand side
     float *W2, *Wt2, *F2, *Ginv2, *RHS2;
@@ -526,6 +541,7 @@ size_t carve(void *base, int64_t N, int64_t M, int64_t k, FzScratch *s) {
     t.part = reinterpret_cast<float *>(take(sizeof(float) * size_t(kMaxColChunks) * k));
     t.rho = reinterpret_cast<float *>(take(sizeof(float) * 4));
     t.Tt = reinterpret_cast<float *>(take(sizeof(float) * size_t(k) * k));  // blocked inverse scratch
+    t.park = reinterpret_cast<float *>(take(sizeof(float) * 2 * kCholNB * kCholNB));  // Cholesky blocks
     t.Bt = reinterpret_cast<int8_t *>(take(size_t(M) * k));
     if (s) *s = t;
     return off;
@@ -572,7 +588,7 @@ cudaError_t tri_inverse(const float *G, int k, float *X, float *Z, float *Tt, cu
 // Launches of one ADMM step (a half of an alternating round).
 int step_launches(int k, int inner, int power_iters) {
     if (inner <= 0) return 0;
-    const int chol = 3 * chol_steps(k) - 2;  // the last block has no panel and no trailing update
+    const int chol = 2 * chol_steps(k) - 1;  // diagonal + panel, then the trailing update (none after the last)
     const int svid = (power_iters > 0 ? 3 * power_iters : 1) + 1;
     // F and its split form, F F^T, ridge; Cholesky; the blocked L^-1 (zero fill, leaves, two GEMMs
     // and a transpose per merge); inverse, its mirror and its split form, T F^T, first dual pass;
@@ -622,10 +638,9 @@ cudaError_t admm_step(const float *T2, int n, int p, int k, const float *r2, con
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     for (int j0 = 0; j0 < k; j0 += kCholNB) {
         const int nb = std::min(kCholNB, k - j0);
-        fz_chol_diag_kernel<<<1, 32, 0, s>>>(w.G, k, j0, nb, status);
         const int j1 = j0 + nb;
+        fz_chol_step_kernel<<<j1 < k ? cdiv(k - j1, 128) : 1, 128, 0, s>>>(w.G, k, j0, nb, w.park, status);
         if (j1 < k) {
-            fz_chol_panel_kernel<<<cdiv(k - j1, 128), 128, 0, s>>>(w.G, k, j0, nb);
             if ((e = gemm_nt(k - j1, k - j1, nb, -1.f, w.G + int64_t(j1) * k + j0, k, w.G + int64_t(j1) * k + j0, k,
                              1.f, w.G + int64_t(j1) * k + j1, k, s, 1)) != cudaSuccess)
                 return e;

@@ -142,13 +142,14 @@ def test_factorize_sizes_and_launch_counts(lib):
     assert lib.factorize_workspace_bytes(0, 4, 4) == 0
     assert lib.factorize_workspace_bytes(4, 4, 16385) == 0
     # per call: transposes of W and B, split forms of W and W^T, the rounds, transpose of B out.
-    # per step: F and its split form, F F^T, ridge; 3 per 32-column Cholesky block less 2; the
-    # blocked L^-1 (zero fill and one leaf of 128 rows at k = 70); inverse, its mirror and its split
-    # form, T F^T, first dual; per iteration 1 GEMM + 3q + 1 SVID passes, dual between iterations
+    # per step: F and its split form, F F^T, ridge; 2 per 32-column Cholesky block less 1 (diagonal
+    # and panel, trailing update); the blocked L^-1 (zero fill and one leaf of 128 rows at k = 70);
+    # inverse, its mirror and its split form, T F^T, first dual; per iteration 1 GEMM + 3q + 1 SVID
+    # passes, dual between iterations
     k, inner, q = 70, 4, 5
-    step = 4 + (3 * 3 - 2) + 2 + 5 + inner * (1 + 3 * q + 1) + (inner - 1)
+    step = 4 + (2 * 3 - 1) + 2 + 5 + inner * (1 + 3 * q + 1) + (inner - 1)
     assert lib.factorize_launch_count(100, 80, k, 3, inner, q, 1.0) == 4 + 3 * 2 * step + 1
-    step0 = 4 + (3 * 3 - 2) + 2 + 5 + inner * (1 + 1 + 1) + (inner - 1)   # power_iters = 0: fill + rows
+    step0 = 4 + (2 * 3 - 1) + 2 + 5 + inner * (1 + 1 + 1) + (inner - 1)   # power_iters = 0: fill + rows
     assert lib.factorize_launch_count(100, 80, k, 1, inner, 0, 1.0) == 4 + 2 * step0 + 1
     assert lib.factorize_launch_count(100, 80, k, 0, inner, q, 1.0) == 0
     assert lib.factorize_launch_count(100, 80, k, 1, 0, q, 1.0) == 0
