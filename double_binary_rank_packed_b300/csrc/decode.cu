@@ -242,8 +242,8 @@ __host__ __device__ inline FusedSmem fused_smem(int CPAD, int RBW, int Wc, int R
 constexpr int kAdTableSmemMax = 8192;  // adapter tables up to this size go to shared memory
 static_assert(sizeof(dbf_factors) % 16 == 0, "the adapter table is copied in 16-byte pieces");
 
-__device__ __noinline__ bool fused_find_chunk(const int32_t *off, const int32_t *seg_ad, int S, int T, int tpc, int q,
-                                              int &s, int &o0, int &jt, int &jn, int &ad, int *sm) {
+__device__ __forceinline__ bool fused_find_chunk(const int32_t *off, const int32_t *seg_ad, int S, int T, int tpc, int q,
+                                                 int &s, int &o0, int &jt, int &jn, int &ad, int *sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int kPer = (kChunkMapMaxS + kThreads - 1) / kThreads;  // segments per thread
     int lo[kPer], hi[kPer], sa[kPer], cnt[kPer];
