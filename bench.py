@@ -247,9 +247,11 @@ def call_footprint(N, M, R, ell, T, ldw1, ldw2):
 class DecodeWorkload:
     """L independent dbf_matmul calls per step (streamed decode)."""
 
-    def __init__(self, dbf, key, proj, T, outlier_scale=0.0, max_calls=4096, transposed=False):
+    def __init__(self, dbf, key, proj, T, outlier_scale=0.0, max_calls=4096, transposed=False, one_launch=False):
         """transposed: time the backward product dx = dy dW (dy [T, N] -> dx [T, M]) through the
-        transposed factors instead of the forward one."""
+        transposed factors instead of the forward one.  one_launch: the two decode stages in one
+        cooperative launch with a grid-wide barrier (dbf_selftest_decode_one_launch), the
+        comparison arm of the two launches dbf_matmul makes for large R."""
         import torch
         self.dbf, self.key, self.T = dbf, key, T
         self.N, self.M, self.R, self.ell = proj.N, proj.M, proj.R, proj.ell
@@ -268,6 +270,11 @@ class DecodeWorkload:
         self.y = [torch.empty((T, base.N), dtype=torch.bfloat16, device="cuda") for _ in range(self.L)]
         self.ws = dbf.new_workspace(dbf.workspace_bytes(base, T), "cuda")
         self.launches_per_call = dbf.launch_count(base, T)
+        self.one_launch = one_launch
+        if one_launch:
+            self.ws = dbf.new_workspace(dbf.workspace_bytes(base, T, dbf.PATH_DECODE), "cuda")
+            self.barrier = torch.zeros(2, dtype=torch.int32, device="cuda")
+            self.launches_per_call = 1
         self.fp_call = fp
         self.bytes_per_call = CFG.algorithmic_bytes(self.N, self.M, self.R, self.ell, T)
         self.flops_per_call = CFG.flops(self.N, self.M, self.R, self.ell, T)
@@ -276,10 +283,14 @@ class DecodeWorkload:
 
     def run_eager(self):
         for l in range(self.L):
-            self.dbf.matmul(self.factors[l], self.x[l], self.y[l], workspace=self.ws)
+            self.call_one(l)
 
     def call_one(self, l):
-        self.dbf.matmul(self.factors[l], self.x[l], self.y[l], workspace=self.ws)
+        if self.one_launch:
+            self.dbf.selftest_decode_one_launch(self.factors[l], self.x[l], self.barrier, self.y[l],
+                                                workspace=self.ws)
+        else:
+            self.dbf.matmul(self.factors[l], self.x[l], self.y[l], workspace=self.ws)
 
     def footprint_per_step(self):
         return self.L * self.fp_call
@@ -788,6 +799,8 @@ def time_oracle_workload(key, seconds=2.0):
     cores = oracle_threads()
     name, _, tok = key.rpartition("_T")
     T = int(tok) if tok.isdigit() else 0
+    if name == "dbf1p5_one":
+        name = "dbf1p5"  # the same product, one launch instead of two
     out = {}
 
     def obj(tokens, n, el, route, sample):
@@ -893,7 +906,7 @@ def workload_line(wl, ms_step, steps, peaks, extra=None):
 
 
 def make_workload(dbf, key, max_calls=None):
-    """Workload by key: adapter4k_T{1,4,16}, dbf1p5_T{1,8}, tiny_T{1,8}, multiadapter_T256, dbfmlp_T2048,
+    """Workload by key: adapter4k_T{1,4,16}, dbf1p5_T{1,8}, dbf1p5_one_T8, tiny_T{1,8}, multiadapter_T256, dbfmlp_T2048,
     adapter4k_dx_T16, dbfmlp_dx_T2048, dbfmlp_bwd_T2048, dbfqkv_T8 (grouped), dbfqkv_sep_T8."""
     if key == "dbffact1p5":
         return FactorizeWorkload(dbf, key)
@@ -915,6 +928,9 @@ def make_workload(dbf, key, max_calls=None):
     if name == "dbf1p5":
         return DecodeWorkload(dbf, key, CFG.DBF_1P5.projections[0], T, outlier_scale=CFG.DBF_1P5.outlier_scale,
                               **cap)
+    if name == "dbf1p5_one":
+        return DecodeWorkload(dbf, key, CFG.DBF_1P5.projections[0], T, outlier_scale=CFG.DBF_1P5.outlier_scale,
+                              one_launch=True, **cap)
     if name == "tiny":
         return DecodeWorkload(dbf, key, CFG.TINY.projections[0], T, **cap)
     if name == "multiadapter":
@@ -927,6 +943,8 @@ def make_workload(dbf, key, max_calls=None):
 WORKLOAD_TITLES = {
     "adapter4k": "adapter4k: LoRDBA adapter branch N=M=4096 R=64 ell=1, T={T} decode tokens",
     "dbf1p5": "dbf1p5: DBF 1.5 bits/weight N=M=4096 R=3072 ell=1, 1% outlier columns x20, T={T} decode tokens",
+    "dbf1p5_one": "dbf1p5_one: the dbf1p5 decode with both stages in one cooperative launch (grid-wide "
+                  "barrier between them), the comparison arm of the two-launch form, T={T} decode tokens",
     "tiny": "tiny: N=M=256 R=32 ell=1, T={T} tokens",
     "multiadapter": "multiadapter: 64 adapters N=M=4096 R=32 ell=2, T={T} routed decode tokens",
     "dbfmlp": "dbfmlp: DBF MLP up 14336x4096 + down 4096x14336, R=5013 ell=2, T={T} prefill tokens",
@@ -942,7 +960,7 @@ WORKLOAD_TITLES = {
                   "8 power iterations per SVID)",
 }
 
-SECONDARY = ["adapter4k_T1", "adapter4k_T4", "dbf1p5_T1", "dbf1p5_T8", "tiny_T8", "multiadapter_T256",
+SECONDARY = ["adapter4k_T1", "adapter4k_T4", "dbf1p5_T1", "dbf1p5_T8", "dbf1p5_one_T8", "tiny_T8", "multiadapter_T256",
              "dbfmlp_T2048", "adapter4k_dx_T16", "dbfmlp_dx_T2048", "dbfmlp_bwd_T2048", "dbfqkv_T8",
              "dbfqkv_sep_T8", "dbffact1p5"]
 

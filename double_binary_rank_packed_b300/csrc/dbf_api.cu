@@ -582,6 +582,41 @@ int dbf_matmul(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, 
     return dbf_matmul_path(f, x, T, y, accumulate, workspace, ws_bytes, stream, DBF_PATH_AUTO);
 }
 
+int dbf_selftest_decode_one_launch(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y, int accumulate,
+                                   void *workspace, size_t ws_bytes, uint32_t *barrier, void *stream) {
+    const int rc = dbfk::check_matmul_args(f, x, T, y, accumulate, DBF_PATH_DECODE);
+    if (rc != DBF_OK || T == 0) return rc;
+    if (T > kDecodeMaxTokens || !barrier || (reinterpret_cast<uintptr_t>(barrier) & 7) != 0)
+        return DBF_ERR_INVALID_ARG;
+    const size_t need = ws_for(f, T, DBF_PATH_DECODE);
+    if (!workspace || ws_bytes < need) return DBF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DBF_ERR_ALIGNMENT;
+    if (!status_ptr()) return cuda_fail(cudaGetLastError(), "status word");
+    dbfk::DecodeCall c = {};
+    c.f = f;
+    c.N = f->N;
+    c.M = f->M;
+    c.R = f->R;
+    c.ell = f->ell;
+    c.T = static_cast<int>(T);
+    c.tokens_per_problem = static_cast<int>(T);
+    c.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    c.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    c.accumulate = accumulate;
+    c.status = status_ptr();
+    const cudaError_t e =
+        dbfk::launch_decode_one_launch(c, static_cast<__half *>(workspace), static_cast<int>(v_ld(f->R)), barrier,
+                                       num_sms(), static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported) {
+        snprintf(g_last_error, sizeof(g_last_error), "one-launch decode: %s",
+                 e == cudaErrorNotSupported ? "the two stages' plans split K over different cluster sizes, or "
+                                                                 "need more shared memory than a CTA has"
+                                            : "the grid does not fit on the GPU at once");
+        return DBF_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? DBF_OK : cuda_fail(e, "one-launch decode");
+}
+
 }  // extern "C"
 
 namespace {

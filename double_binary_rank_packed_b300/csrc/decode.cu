@@ -806,14 +806,17 @@ __host__ __device__ inline StageSmem stage_smem(int CPAD, int RBW, int KS, int W
 }
 
 // bx: this CTA's index along the rows of its problem (blockIdx.x, or the
-// offset inside its problem's range in a grouped launch)
+// offset inside its problem's range in a grouped launch); smem_off: where this
+// stage's shared-memory layout starts in the dynamic shared memory (a 128-byte
+// multiple; nonzero only when one launch runs both stages)
 template <int CT, int RBW, int STAGE, bool SEG>
-__device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx) {
+__device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx, const uint32_t smem_off = 0) {
     constexpr int CPAD = 8 * CT;
     constexpr int C4 = CPAD / 4;
     constexpr int RWS = 16 * RBW;
     constexpr int NWB = words_per_batch<CT>();
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem_dyn[];
+    unsigned char *const smem = smem_dyn + smem_off;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, c = lane & 3;
     const int KS = a.KS, Wc = a.Wc;
@@ -1128,6 +1131,80 @@ __global__ void __launch_bounds__(kThreads, 2) dec_stage_group_kernel(const __gr
     dec_stage_body<CT, RBW, STAGE, false>(g.p[p], b - g.block0[p]);
 }
 
+// One-launch form of the two stages (the comparison arm of the two-launch
+// path): CTAs [0, grid1) run stage 1 and write V, every CTA meets at a
+// grid-wide barrier, then CTAs [0, grid2) run stage 2 from V.  The launch's
+// cluster is the larger of the two stages' K splits and the other split is
+// either the same or 1 (a stage with KS = 1 uses no cluster feature), so a
+// cluster is wholly inside or wholly outside a stage's range; stage 2's
+// shared memory starts at smem2 so that no mbarrier is re-initialised in
+// place.  The launch is cooperative (every CTA resident), the barrier wait is
+// bounded.
+struct PairArgs {
+    DecArgs a1, a2;
+    int grid1, grid2;
+    uint32_t smem2;
+    unsigned int *bar;  // [0] arrivals of the current phase, [1] phase count; 0, 0 before the first call
+};
+
+// Grid-wide barrier over nblocks CTAs.  Thread 0 of each CTA reads the phase
+// count (it cannot advance before this CTA arrives), publishes the CTA's
+// writes (the __syncthreads before makes them cumulative) and arrives; the
+// last arrival resets the arrival count and advances the phase, the others
+// poll it with acquire loads for at most kWaitLimitNs.  Returns false in every
+// thread of a CTA whose wait ran out (DBF_ERR_TIMEOUT recorded).
+__device__ __noinline__ bool grid_barrier_bounded(unsigned int *bar, unsigned int nblocks, int *status) {
+    __shared__ int ok_s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        unsigned int phase;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(phase) : "l"(bar + 1) : "memory");
+        __threadfence();
+        const unsigned int old = atomicAdd(bar, 1u);
+        if (old == nblocks - 1) {
+            atomicExch(bar, 0u);
+            __threadfence();
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(bar + 1), "r"(phase + 1u) : "memory");
+        } else {
+            const uint64_t t0 = global_ns();
+            for (;;) {
+                unsigned int now;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(bar + 1) : "memory");
+                if (now != phase) break;
+                if (global_ns() - t0 > kWaitLimitNs) {
+                    record_status(status, DBF_ERR_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        ok_s = ok;
+    }
+    __syncthreads();
+    return ok_s != 0;
+}
+
+template <int CT, int RBW1, int RBW>
+__global__ void __launch_bounds__(kThreads, 2) dec_stage_pair_kernel(const __grid_constant__ PairArgs p) {
+    const int bx = static_cast<int>(blockIdx.x);
+    if (bx < p.grid2) {
+        // this CTA's stage-2 sign rows into L2 while stage 1 runs (factor memory: no earlier
+        // kernel writes it)
+        const int KS = p.a2.KS, rank = (KS > 1) ? static_cast<int>(cluster_ctarank()) : 0;
+        const int r0 = (bx / KS) * 16 * RBW, w0 = rank * p.a2.Wc;
+        const int nr = max(0, min(16 * RBW, p.a2.rows - r0));
+        const int nw = max(0, min(p.a2.Wc, p.a2.Kw - w0));
+        for (int e = threadIdx.x; e < 2 * nr; e += kThreads)  // first and last word of each row slice
+            if (nw > 0) prefetch_l2(p.a2.bits + size_t(r0 + (e >> 1)) * p.a2.ldw + w0 + (e & 1) * (nw - 1));
+    }
+    if (bx < p.grid1) dec_stage_body<CT, RBW1, 1, false>(p.a1, bx, 0);
+    pdl_wait();  // CTAs past grid1 have not waited yet; V's readers must not overlap the previous kernel
+    if (!grid_barrier_bounded(p.bar, gridDim.x, p.a1.status)) return;
+    if (bx < p.grid2) dec_stage_body<CT, RBW, 2, false>(p.a2, bx, p.smem2);
+}
+
 // ================================================================ launchers
 
 template <typename Kern, typename Args>
@@ -1371,7 +1448,9 @@ cudaError_t launch_decode_fused(bool segmented, const FusedPlan &plan, const Fus
 // Both decode stages of one call (or of a routed batch when seg_off is set):
 // stage 1 writes V = beta * (B2 (gamma * x)) to `V` (fp16, [ell*T][ldv]),
 // stage 2 reads it.
-cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int num_sms, cudaStream_t stream) {
+// The plans and arguments of the two stages of one decode call.
+static cudaError_t plan_two_stage(const DecodeCall &c, __half *V, int ldv, int num_sms, DecPlan &p1, DecArgs &a1,
+                                  DecPlan &p2, DecArgs &a2) {
     const int ell = c.ell;
     const int64_t cols = std::min<int64_t>(int64_t(ell) * c.tokens_per_problem, 64);
     const int problems = std::max(1, c.S);
@@ -1393,7 +1472,7 @@ cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int
     a.status = c.status;
     const bool seg = c.seg_off != nullptr;
 
-    DecArgs a1 = a;
+    a1 = a;
     if (!seg) {
         a1.bits = c.f->B2;
         a1.ldw = c.f->ldw2;
@@ -1404,11 +1483,11 @@ cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int
     a1.rows_out = (c.R + 31) & ~31;
     a1.K = c.M;
     a1.Kw = (c.M + 31) / 32;
-    DecPlan p1 = plan_decode_stage(a1.rows_out, a1.Kw, static_cast<int>(cols), 8, sms_per_problem, ell, true);
+    p1 = plan_decode_stage(a1.rows_out, a1.Kw, static_cast<int>(cols), 8, sms_per_problem, ell, true);
     a1.KS = p1.KS;
     a1.Wc = p1.Wc;
 
-    DecArgs a2 = a;
+    a2 = a;
     if (!seg) {
         a2.bits = c.f->B1;
         a2.ldw = c.f->ldw1;
@@ -1418,16 +1497,107 @@ cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int
     a2.rows_out = c.N;
     a2.K = c.R;
     a2.Kw = (c.R + 31) / 32;
-    DecPlan p2 = plan_decode_stage(c.N, a2.Kw, static_cast<int>(cols), p1.CT, sms_per_problem, ell, false);
+    p2 = plan_decode_stage(c.N, a2.Kw, static_cast<int>(cols), p1.CT, sms_per_problem, ell, false);
     p2.CT = p1.CT;  // both stages use the same column chunking
     if (p2.smem == 0 || p1.smem == 0) return cudaErrorNotSupported;
     if (p2.CT >= 8 && p2.RBW > 2) return cudaErrorNotSupported;
     p2.smem = stage_smem(8 * p2.CT, p2.RBW, p2.KS, p2.Wc, ell, false, c.accumulate != 0).total;
     a2.KS = p2.KS;
     a2.Wc = p2.Wc;
-    cudaError_t e = launch_decode_stage(1, seg, p1, a1, problems, stream, true);
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int num_sms, cudaStream_t stream) {
+    DecPlan p1, p2;
+    DecArgs a1, a2;
+    cudaError_t e = plan_two_stage(c, V, ldv, num_sms, p1, a1, p2, a2);
+    if (e != cudaSuccess) return e;
+    const bool seg = c.seg_off != nullptr;
+    const int problems = std::max(1, c.S);
+    e = launch_decode_stage(1, seg, p1, a1, problems, stream, true);
     if (e != cudaSuccess) return e;
     return launch_decode_stage(2, seg, p2, a2, problems, stream, true);
+}
+
+template <int CT, int RBW1, int RBW2>
+static cudaError_t launch_pair_one(const PairArgs &pa, int grid, int cluster, size_t smem, cudaStream_t stream) {
+    static int configured = 0;
+    auto kern = dec_stage_pair_kernel<CT, RBW1, RBW2>;
+    if (smem > 48 * 1024 && static_cast<int>(smem) > configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = static_cast<int>(smem);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[3];
+    int na = 0;
+    if (cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    // every CTA must be resident at once: check before launching, then ask for a cooperative launch
+    int active = 0;
+    if (cluster > 1) {
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        active *= cluster;
+    } else {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&active, kern, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        active *= sms;
+    }
+    if (active < grid) return cudaErrorCooperativeLaunchTooLarge;
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, pa);
+}
+
+cudaError_t launch_decode_one_launch(const DecodeCall &c, __half *V, int ldv, unsigned int *bar, int num_sms,
+                                     cudaStream_t stream) {
+    if (c.seg_off != nullptr || bar == nullptr) return cudaErrorInvalidValue;
+    DecPlan p1, p2;
+    PairArgs pa = {};
+    cudaError_t e = plan_two_stage(c, V, ldv, num_sms, p1, pa.a1, p2, pa.a2);
+    if (e != cudaSuccess) return e;
+    const int cluster = std::max(p1.KS, p2.KS);
+    if (std::min(p1.KS, p2.KS) != 1 && p1.KS != p2.KS) return cudaErrorNotSupported;
+    pa.grid1 = p1.grid_x;
+    pa.grid2 = p2.grid_x;
+    pa.smem2 = static_cast<uint32_t>((p1.smem + 127) & ~size_t(127));
+    pa.bar = bar;
+    const int grid = (std::max(pa.grid1, pa.grid2) + cluster - 1) / cluster * cluster;
+    const size_t smem = pa.smem2 + p2.smem;
+    if (smem > size_t(227) * 1024) return cudaErrorNotSupported;
+    switch (p1.CT * 100 + p1.RBW * 10 + p2.RBW) {
+        case 122: return launch_pair_one<1, 2, 2>(pa, grid, cluster, smem, stream);
+        case 124: return launch_pair_one<1, 2, 4>(pa, grid, cluster, smem, stream);
+        case 142: return launch_pair_one<1, 4, 2>(pa, grid, cluster, smem, stream);
+        case 144: return launch_pair_one<1, 4, 4>(pa, grid, cluster, smem, stream);
+        case 222: return launch_pair_one<2, 2, 2>(pa, grid, cluster, smem, stream);
+        case 224: return launch_pair_one<2, 2, 4>(pa, grid, cluster, smem, stream);
+        case 242: return launch_pair_one<2, 4, 2>(pa, grid, cluster, smem, stream);
+        case 244: return launch_pair_one<2, 4, 4>(pa, grid, cluster, smem, stream);
+        case 422: return launch_pair_one<4, 2, 2>(pa, grid, cluster, smem, stream);
+        case 822: return launch_pair_one<8, 2, 2>(pa, grid, cluster, smem, stream);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 // Plan of a grouped stage: one CT, RBW and KS for every problem of the launch

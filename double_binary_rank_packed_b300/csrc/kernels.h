@@ -163,6 +163,11 @@ struct DecodeCall {
 // Both stages; V is device scratch of ell*T rows x ldv halves.  Returns
 // cudaErrorNotSupported when no tile plan fits the shape.
 cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int num_sms, cudaStream_t stream);
+// The same two stages in one cooperative launch with a grid-wide barrier
+// between them; bar: two device words, zero before the first call, owned by
+// one stream at a time (every completed call leaves the arrival count at 0).
+cudaError_t launch_decode_one_launch(const DecodeCall &c, __half *V, int ldv, unsigned int *bar, int num_sms,
+                                     cudaStream_t stream);
 
 // G independent problems (same ell and T, any N, M, R), both stages in one
 // launch each; V[p] is scratch of ell*T rows x ldv[p] halves.  Returns

@@ -49,7 +49,7 @@ EXPORTED = (
     "dbf_grouped_launch_count", "dbf_matmul_hostio_batch", "dbf_hostio_batch_workspace_bytes",
     "dbf_factorize", "dbf_factorize_workspace_bytes", "dbf_factorize_launch_count",
     "dbf_factorize_weighted", "dbf_factorize_weighted_workspace_bytes", "dbf_factorize_weighted_launch_count",
-    "dbf_selftest_split_gemm", "dbf_selftest_split_gemm_workspace_bytes",
+    "dbf_selftest_split_gemm", "dbf_selftest_split_gemm_workspace_bytes", "dbf_selftest_decode_one_launch",
 )
 
 
@@ -105,6 +105,7 @@ def _load():
         "dbf_selftest_split_gemm_workspace_bytes": (sz, [i32, i32, i32]),
         "dbf_selftest_split_gemm": (ci, [i32, i32, i32, ctypes.c_float, vp, i64, vp, i64, ctypes.c_float, vp, i64,
                                          ci, vp, sz, vp]),
+        "dbf_selftest_decode_one_launch": (ci, [fp, vp, i64, vp, ci, vp, sz, vp, vp]),
         "dbf_status_string": (ctypes.c_char_p, [ci]),
         "dbf_last_cuda_error": (ctypes.c_char_p, []),
         "dbf_launch_count": (ci, [fp, i64, ci]),
@@ -604,6 +605,31 @@ def selftest_split_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, alpha
                                         C.stride(0), int(lower), _ptr(ws), ws.numel(), _stream_handle(stream)),
            "dbf_selftest_split_gemm")
     return C
+
+
+@_on_stream
+def selftest_decode_one_launch(f: PackedFactors, x: torch.Tensor, barrier: torch.Tensor,
+                               y: torch.Tensor | None = None, accumulate: bool = False,
+                               workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The decode path's two stages in one cooperative launch (dbf_selftest_decode_one_launch).
+    barrier: int32 CUDA tensor of >= 2 elements, zero before the first call, one per concurrent stream."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != f.M:
+        raise ValueError("x must be bf16 [T, M]")
+    if barrier.dtype != torch.int32 or not barrier.is_cuda or barrier.numel() < 2:
+        raise ValueError("barrier must be an int32 CUDA tensor of at least 2 elements")
+    x = x.contiguous()
+    T = x.shape[0]
+    if y is None:
+        if accumulate:
+            raise ValueError("accumulate needs y")
+        y = torch.empty((T, f.N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = new_workspace(workspace_bytes(f, T, PATH_DECODE), x.device)
+    rc = _lib.dbf_selftest_decode_one_launch(ctypes.byref(f.struct), _ptr(x), T, _ptr(y), int(bool(accumulate)),
+                                             _ptr(workspace), workspace.numel(), _ptr(barrier),
+                                             _stream_handle(stream))
+    _check(rc, "dbf_selftest_decode_one_launch")
+    return y
 
 
 # ------------------------------------------------------- no-allocation variant

@@ -352,6 +352,34 @@ int dbf_selftest_split_gemm(int32_t m, int32_t n, int32_t kk, float alpha, const
                             void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * dbf_selftest_decode_one_launch: the decode path's two stages (x -> V and
+ * V -> y, DBF page, section 2, "Cálculo en la inferencia": the gamma, B2,
+ * beta, B1, alpha chain) in ONE cooperative launch, with a grid-wide barrier
+ * between the stage that writes V and the stage that reads it, instead of two
+ * launches.  The comparison arm of the two-launch form that dbf_matmul takes
+ * for large R; for tests and timing.
+ *   f, x, T, y, accumulate, workspace, ws_bytes, stream: as dbf_matmul_path
+ *      with DBF_PATH_DECODE (1 <= T <= dbf_decode_max_tokens(); T = 0 does
+ *      nothing).  Any R; the same stage code, arithmetic and summation
+ *      order as the two-launch form, so the result is bit for bit that of
+ *      dbf_matmul_path with DBF_PATH_DECODE wherever that call takes the
+ *      two launches (R > 256).
+ *   barrier  device, two uint32 words, 8-byte aligned, zero before the first
+ *      call; every call that completes leaves them ready for the next.  Calls
+ *      that may overlap on the GPU need a pair each.
+ * DBF_ERR_UNSUPPORTED (reason in dbf_last_cuda_error()) when the two stages'
+ * tile plans split K over different cluster sizes (neither of them 1), when
+ * their shared memory together exceeds a CTA's, or when the grid cannot be
+ * resident at once; DBF_ERR_INVALID_ARG for a missing or misaligned
+ * barrier or T above the decode range.  A barrier wait that runs out (1 s)
+ * records DBF_ERR_TIMEOUT; the call's y is then undefined and the barrier
+ * words must be zeroed again.
+ */
+int dbf_selftest_decode_one_launch(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
+                                   int accumulate, void *workspace, size_t ws_bytes, uint32_t *barrier,
+                                   void *stream);
+
+/*
  * dbf_matmul_decode_noalloc: dbf_matmul_path(..., DBF_PATH_DECODE) for
  * callers that cannot allocate device memory for a call: serving loops that
  * must never take cudaMalloc's implicit device synchronisation on the token
