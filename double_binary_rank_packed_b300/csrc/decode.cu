@@ -808,9 +808,13 @@ __host__ __device__ inline StageSmem stage_smem(int CPAD, int RBW, int KS, int W
 // bx: this CTA's index along the rows of its problem (blockIdx.x, or the
 // offset inside its problem's range in a grouped launch); smem_off: where this
 // stage's shared-memory layout starts in the dynamic shared memory (a 128-byte
-// multiple; nonzero only when one launch runs both stages)
-template <int CT, int RBW, int STAGE, bool SEG>
+// multiple; nonzero only when one launch runs both stages).  PART 0 runs the
+// whole stage; when one launch runs both stages, PART 1 only starts the
+// asynchronous copies of the signs and scales (no wait) and PART 2 runs the
+// rest without them, after the CTA's own cp.async groups have completed.
+template <int CT, int RBW, int STAGE, bool SEG, int PART = 0>
 __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx, const uint32_t smem_off = 0) {
+    static_assert(PART == 0 || !SEG, "split stages are not segmented");
     constexpr int CPAD = 8 * CT;
     constexpr int C4 = CPAD / 4;
     constexpr int RWS = 16 * RBW;
@@ -868,17 +872,20 @@ __device__ __forceinline__ void dec_stage_body(const DecArgs &a, const int bx, c
     float *slots = reinterpret_cast<float *>(smem + L.slots);
 
     // ---- 1. inputs no earlier kernel writes: packed signs and scales
-    copy_rows_async(bits_s, ldws * 4, bits + size_t(row0) * ldw + w0, size_t(ldw) * 4, nr, Wslice * 4, tid,
-                    kThreads);
-    zero_rows(bits_s + nr * ldws, ldws * 4, RWS - nr, Wslice * 4, tid, kThreads);
-    copy_rows_async(sc_s, RWS * 2, scale_out + row0, size_t(a.rows) * 2, ell, nr * 2, tid, kThreads);
-    zero_half_tails(sc_s, ell, RWS, nr, tid, kThreads);
-    if (STAGE == 1) {
-        if (kvalid > 0)
-            copy_rows_async(gam_s, 64 * Wc, scale_in + 32 * w0, size_t(a.K) * 2, ell, kvalid * 2, tid, kThreads);
-        zero_half_tails(gam_s, ell, 32 * Wc, kvalid, tid, kThreads);
+    if constexpr (PART != 2) {
+        copy_rows_async(bits_s, ldws * 4, bits + size_t(row0) * ldw + w0, size_t(ldw) * 4, nr, Wslice * 4, tid,
+                        kThreads);
+        zero_rows(bits_s + nr * ldws, ldws * 4, RWS - nr, Wslice * 4, tid, kThreads);
+        copy_rows_async(sc_s, RWS * 2, scale_out + row0, size_t(a.rows) * 2, ell, nr * 2, tid, kThreads);
+        zero_half_tails(sc_s, ell, RWS, nr, tid, kThreads);
+        if (STAGE == 1) {
+            if (kvalid > 0)
+                copy_rows_async(gam_s, 64 * Wc, scale_in + 32 * w0, size_t(a.K) * 2, ell, kvalid * 2, tid, kThreads);
+            zero_half_tails(gam_s, ell, 32 * Wc, kvalid, tid, kThreads);
+        }
+        cp_async_commit();
     }
-    cp_async_commit();
+    if constexpr (PART == 1) return;
     // KS > 1: the partial of every owned row arrives from each CTA of the cluster with st.async;
     // one mbarrier per buffer counts the bytes of one chunk
     uint64_t *xbar = reinterpret_cast<uint64_t *>(smem + L.slots + align16(size_t(2) * RWS * CPAD * 4));
@@ -1144,41 +1151,41 @@ struct PairArgs {
     DecArgs a1, a2;
     int grid1, grid2;
     uint32_t smem2;
-    unsigned int *bar;  // [0] arrivals of the current phase, [1] phase count; 0, 0 before the first call
+    unsigned int *bar;  // [0] arrival counter (a multiple of kPairQuantum between calls), [1] reserved, 0
 };
 
-// Grid-wide barrier over nblocks CTAs.  Thread 0 of each CTA reads the phase
-// count (it cannot advance before this CTA arrives), publishes the CTA's
-// writes (the __syncthreads before makes them cumulative) and arrives; the
-// last arrival resets the arrival count and advances the phase, the others
-// poll it with acquire loads for at most kWaitLimitNs.  Returns false in every
-// thread of a CTA whose wait ran out (DBF_ERR_TIMEOUT recorded).
+// Each launch advances the arrival counter by exactly this much, whatever its grid (<= this).
+constexpr unsigned int kPairQuantum = 1024;
+
+// Grid-wide barrier over nblocks <= kPairQuantum CTAs with one atomic per CTA
+// and no reset: CTA 0 adds kPairQuantum - (nblocks - 1), every other CTA 1,
+// so the launch moves the counter from base to base + kPairQuantum and every
+// CTA's pre-add value lies in [base, base + kPairQuantum).  Thread 0 of each
+// CTA fences (the __syncthreads before makes the CTA's writes cumulative),
+// adds, and polls the counter with acquire loads until it reaches the next
+// multiple of kPairQuantum, for at most kWaitLimitNs.  Returns false in every
+// thread of a CTA whose wait ran out (DBF_ERR_TIMEOUT recorded; the counter is
+// then off its multiple and must be zeroed before the next call).
 __device__ __noinline__ bool grid_barrier_bounded(unsigned int *bar, unsigned int nblocks, int *status) {
     __shared__ int ok_s;
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        unsigned int phase;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(phase) : "l"(bar + 1) : "memory");
+        const unsigned int inc = (blockIdx.x == 0) ? kPairQuantum - (nblocks - 1u) : 1u;
         __threadfence();
-        const unsigned int old = atomicAdd(bar, 1u);
-        if (old == nblocks - 1) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(bar + 1), "r"(phase + 1u) : "memory");
-        } else {
-            const uint64_t t0 = global_ns();
-            for (;;) {
-                unsigned int now;
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(bar + 1) : "memory");
-                if (now != phase) break;
-                if (global_ns() - t0 > kWaitLimitNs) {
-                    record_status(status, DBF_ERR_TIMEOUT);
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(64);
+        const unsigned int old = atomicAdd(bar, inc);
+        const unsigned int target = (old & ~(kPairQuantum - 1u)) + kPairQuantum;
+        const uint64_t t0 = global_ns();
+        for (;;) {
+            unsigned int now;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(bar) : "memory");
+            if (static_cast<int>(now - target) >= 0) break;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                record_status(status, DBF_ERR_TIMEOUT);
+                ok = 0;
+                break;
             }
+            __nanosleep(100);  // spaces the polls of up to 1024 CTAs on one word
         }
         ok_s = ok;
     }
@@ -1189,20 +1196,18 @@ __device__ __noinline__ bool grid_barrier_bounded(unsigned int *bar, unsigned in
 template <int CT, int RBW1, int RBW>
 __global__ void __launch_bounds__(kThreads, 2) dec_stage_pair_kernel(const __grid_constant__ PairArgs p) {
     const int bx = static_cast<int>(blockIdx.x);
-    if (bx < p.grid2) {
-        // this CTA's stage-2 sign rows into L2 while stage 1 runs (factor memory: no earlier
-        // kernel writes it)
-        const int KS = p.a2.KS, rank = (KS > 1) ? static_cast<int>(cluster_ctarank()) : 0;
-        const int r0 = (bx / KS) * 16 * RBW, w0 = rank * p.a2.Wc;
-        const int nr = max(0, min(16 * RBW, p.a2.rows - r0));
-        const int nw = max(0, min(p.a2.Wc, p.a2.Kw - w0));
-        for (int e = threadIdx.x; e < 2 * nr; e += kThreads)  // first and last word of each row slice
-            if (nw > 0) prefetch_l2(p.a2.bits + size_t(r0 + (e >> 1)) * p.a2.ldw + w0 + (e & 1) * (nw - 1));
-    }
+    // this CTA's stage-2 signs and scales into its stage-2 shared memory while stage 1 runs
+    // (factor memory: no earlier kernel writes it); stage 1's cp.async wait covers these too
+    if (bx < p.grid2) dec_stage_body<CT, RBW, 2, false, 1>(p.a2, bx, p.smem2);
     if (bx < p.grid1) dec_stage_body<CT, RBW1, 1, false>(p.a1, bx, 0);
-    pdl_wait();  // CTAs past grid1 have not waited yet; V's readers must not overlap the previous kernel
+    // CTAs past grid1 have not waited yet: the previous kernel (possibly the previous call on this
+    // barrier, still counting its arrivals) must be complete before any CTA arrives
+    pdl_wait();
     if (!grid_barrier_bounded(p.bar, gridDim.x, p.a1.status)) return;
-    if (bx < p.grid2) dec_stage_body<CT, RBW, 2, false>(p.a2, bx, p.smem2);
+    if (bx < p.grid2) {
+        cp_async_wait_all();  // CTAs that ran no stage 1
+        dec_stage_body<CT, RBW, 2, false, 2>(p.a2, bx, p.smem2);
+    }
 }
 
 // ================================================================ launchers
@@ -1584,7 +1589,7 @@ cudaError_t launch_decode_one_launch(const DecodeCall &c, __half *V, int ldv, un
     pa.bar = bar;
     const int grid = (std::max(pa.grid1, pa.grid2) + cluster - 1) / cluster * cluster;
     const size_t smem = pa.smem2 + p2.smem;
-    if (smem > size_t(227) * 1024) return cudaErrorNotSupported;
+    if (smem > size_t(227) * 1024 || grid > static_cast<int>(kPairQuantum)) return cudaErrorNotSupported;
     switch (p1.CT * 100 + p1.RBW * 10 + p2.RBW) {
         case 122: return launch_pair_one<1, 2, 2>(pa, grid, cluster, smem, stream);
         case 124: return launch_pair_one<1, 2, 4>(pa, grid, cluster, smem, stream);

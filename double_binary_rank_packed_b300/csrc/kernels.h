@@ -165,7 +165,8 @@ struct DecodeCall {
 cudaError_t launch_decode_two_stage(const DecodeCall &c, __half *V, int ldv, int num_sms, cudaStream_t stream);
 // The same two stages in one cooperative launch with a grid-wide barrier
 // between them; bar: two device words, zero before the first call, owned by
-// one stream at a time (every completed call leaves the arrival count at 0).
+// one stream at a time (every completed call advances bar[0] by 1024 and
+// leaves bar[1] at 0).
 cudaError_t launch_decode_one_launch(const DecodeCall &c, __half *V, int ldv, unsigned int *bar, int num_sms,
                                      cudaStream_t stream);
 

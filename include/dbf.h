@@ -365,15 +365,16 @@ int dbf_selftest_split_gemm(int32_t m, int32_t n, int32_t kk, float alpha, const
  *      dbf_matmul_path with DBF_PATH_DECODE wherever that call takes the
  *      two launches (R > 256).
  *   barrier  device, two uint32 words, 8-byte aligned, zero before the first
- *      call; every call that completes leaves them ready for the next.  Calls
- *      that may overlap on the GPU need a pair each.
+ *      call; every call that completes advances the first word by 1024
+ *      (modulo 2^32) and leaves the second at 0, ready for the next call.
+ *      Calls that may overlap on the GPU need a pair each.
  * DBF_ERR_UNSUPPORTED (reason in dbf_last_cuda_error()) when the two stages'
  * tile plans split K over different cluster sizes (neither of them 1), when
  * their shared memory together exceeds a CTA's, or when the grid cannot be
  * resident at once; DBF_ERR_INVALID_ARG for a missing or misaligned
  * barrier or T above the decode range.  A barrier wait that runs out (1 s)
  * records DBF_ERR_TIMEOUT; the call's y is then undefined and the barrier
- * words must be zeroed again.
+ * words must be zeroed again.  Grids above 1024 CTAs are DBF_ERR_UNSUPPORTED.
  */
 int dbf_selftest_decode_one_launch(const dbf_factors *f, const uint16_t *x, int64_t T, uint16_t *y,
                                    int accumulate, void *workspace, size_t ws_bytes, uint32_t *barrier,

@@ -56,7 +56,7 @@ def test_one_launch_dbf_1p5_bits(cuda_lib, T):
     y, _ = O.matmul(xb, f)
     U.assert_close(got, y, f"one-launch dbf1p5 T={T}")
     assert np.array_equal(got, _two_launch(cuda_lib, df, x))
-    assert bar.cpu().tolist() == [0, 1]
+    assert bar.cpu().tolist() == [1024, 0]  # one call advances the arrival counter by 1024
 
 
 # plans covered: stage 2 without a K split in a cluster launch (300 x 520), stage 1 without one
@@ -102,8 +102,8 @@ def test_one_launch_integer_mode_bit_exact(cuda_lib):
 
 
 def test_one_launch_barrier_reuse(cuda_lib):
-    # 24 calls on one barrier pair, streamed back to back: the same bits every call, the arrival
-    # count back at 0 and the phase count at 24
+    # 24 calls on one barrier pair, streamed back to back: the same bits every call and the
+    # arrival counter at 24 * 1024
     w = C.DBF_1P5
     p = w.projections[0]
     f = G.make_factors(p.N, p.M, p.R, p.ell, p.seed)
@@ -115,7 +115,7 @@ def test_one_launch_barrier_reuse(cuda_lib):
         cuda_lib.selftest_decode_one_launch(df, x, bar, y)
     torch.cuda.synchronize()
     assert cuda_lib.check_status() == 0
-    assert bar.cpu().tolist() == [0, 24]
+    assert bar.cpu().tolist() == [24 * 1024, 0]
     for y in ys[1:]:
         assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
 
