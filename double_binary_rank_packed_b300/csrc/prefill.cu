@@ -36,8 +36,9 @@ namespace {
 constexpr int kPfThreads = 192;
 constexpr int kBK = 64;  // K elements per stage (128 bytes of fp16)
 
-// Tile layouts.  BN = 192: two CTAs per SM, each with 256 tensor-memory
-// columns (accumulator [0, 192), a 2-stage ring of A slices after it) and a
+// Tile layouts.  BN <= 192 (192, or 176 and 160 for ell <= 2, which leave a
+// smaller last wave): two CTAs per SM, each with 256 tensor-memory columns
+// (accumulator [0, BN), a 2-stage ring of A slices from column 192) and a
 // 4-stage shared-memory ring; the two CTAs interleave their MMA streams and
 // hide each other's tile prologue and epilogue.  Wider tiles: one CTA per SM,
 // 6-stage rings, all 512 columns.  The A ring (signs in tensor memory) and
@@ -557,9 +558,13 @@ cudaError_t launch_gemm_stage(const CUtensorMap &map, const PfArgs &a, int bn, c
         case 1256: return launch_gemm_t<256, STAGE, 1>(map, a, stream, pdl);
         case 1240: return launch_gemm_t<240, STAGE, 1>(map, a, stream, pdl);
         case 1192: return launch_gemm_t<192, STAGE, 1>(map, a, stream, pdl);
+        case 1176: return launch_gemm_t<176, STAGE, 1>(map, a, stream, pdl);
+        case 1160: return launch_gemm_t<160, STAGE, 1>(map, a, stream, pdl);
         case 2256: return launch_gemm_t<256, STAGE, 2>(map, a, stream, pdl);
         case 2240: return launch_gemm_t<240, STAGE, 2>(map, a, stream, pdl);
         case 2192: return launch_gemm_t<192, STAGE, 2>(map, a, stream, pdl);
+        case 2176: return launch_gemm_t<176, STAGE, 2>(map, a, stream, pdl);
+        case 2160: return launch_gemm_t<160, STAGE, 2>(map, a, stream, pdl);
         case 3240: return launch_gemm_t<240, STAGE, 3>(map, a, stream, pdl);
         case 3192: return launch_gemm_t<192, STAGE, 3>(map, a, stream, pdl);
         case 4256: return launch_gemm_t<256, STAGE, 4>(map, a, stream, pdl);
@@ -577,14 +582,14 @@ cudaError_t launch_gemm_stage(const CUtensorMap &map, const PfArgs &a, int bn, c
 // SM: a K step measured max(2*BN, ~400) cycles for a 128-row tile with its A
 // operand in tensor memory, plus a tile's prologue, pipeline fill and
 // epilogue (~8 us, from the gap between that rate and the measured GEMMs).
-// Two CTAs per SM (BN = 192): their MMA streams keep the pipe busy at 2*BN
+// Two CTAs per SM (BN <= 192): their MMA streams keep the pipe busy at 2*BN
 // cycles a step each, and the per-tile costs overlap the other CTA's MMAs.
 // Equal costs keep the first candidate.  0 when no candidate keeps the grid's
 // second dimension within 65535.
 int prefill_pick_bn(int ell, int rows_cover, int64_t C, int nk, int num_sms) {
-    static const int w12[] = {256, 240, 192}, w3[] = {240, 192}, w4[] = {256, 224, 192};
+    static const int w12[] = {256, 240, 192, 176, 160}, w3[] = {240, 192}, w4[] = {256, 224, 192};
     const int *w = (ell == 3) ? w3 : (ell == 4 ? w4 : w12);
-    const int nw = (ell == 3) ? 2 : 3;
+    const int nw = (ell == 3) ? 2 : (ell == 4 ? 3 : 5);
     const int64_t rb = (rows_cover + 127) / 128;
     const double tile_cost = 15000.0;  // cycles
     int best = 0;

@@ -31,7 +31,7 @@ SMALL_OUTPUT = 1000
 # Activation rows per tile that the prefill GEMMs can be launched with (the
 # launch picks one per GEMM from the shape); activation row t*ell + i holds
 # token t, term i, so a tile of BN rows spans BN / ell tokens.
-PREFILL_TILE_ROWS = (192, 224, 240, 256)
+PREFILL_TILE_ROWS = (160, 176, 192, 224, 240, 256)
 
 
 def tile_boundary_tokens(T, ell):
