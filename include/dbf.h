@@ -207,7 +207,7 @@ int dbf_grouped_launch_count(const dbf_factors *fs, int32_t G, int64_t T);
 
 /*
  * dbf_matmul_hostio_batch: L independent dbf_matmul_hostio calls (host x in,
- * host y out, each with its own factors fs[l]) pipelined over three slots of
+ * host y out, each with its own factors fs[l]) pipelined over four slots of
  * device buffers: the copy of x[l+1] to the device and of y[l-1] back to the
  * host run while the kernels of call l run, on the library's own copy-in,
  * compute and read-back streams, which start after the work already queued on
@@ -219,7 +219,7 @@ int dbf_grouped_launch_count(const dbf_factors *fs, int32_t G, int64_t T);
  *   workspace       device, >= dbf_hostio_batch_workspace_bytes(fs, L, T)
  * Consecutive calls whose host buffers follow one another inside one
  * page-locked allocation (e.g. one [L][T][M] buffer sliced per call) share
- * one copy each way, up to 16 calls per copy; other calls are copied one by
+ * one copy each way, up to 32 calls per copy; other calls are copied one by
  * one.  L = 0 or T = 0 is a no-op.  Host-thread safe (an internal lock); the
  * pipeline streams are shared per device, so concurrent batches serialise.
  * Errors as dbf_matmul; after an error the pipeline is still joined back

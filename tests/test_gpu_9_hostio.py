@@ -92,11 +92,12 @@ def test_hostio_batch_empty_and_errors(cuda_lib):
 
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_hostio_batch_contiguous_buffers_share_copies(cuda_lib, accumulate):
-    # calls whose host buffers follow one another are moved in chunks of up to 16 with one copy each
-    # way; 37 calls give chunks of 16, 16 and 5, and the shapes differ from call to call
+    # calls whose host buffers follow one another are moved in chunks of up to 32 with one copy each
+    # way over four device slots; 140 calls give chunks of 32, 32, 32, 32 and 12 (the fifth reuses
+    # the first slot once its read-back is done), and the shapes differ from call to call
     T = 8
     shapes = [(256, 512, 32), (512, 256, 48), (384, 384, 40)]
-    fs = [G.make_factors(*shapes[k % 3], 1, 4700 + k) for k in range(37)]
+    fs = [G.make_factors(*shapes[k % 3], 1, 4700 + k) for k in range(140)]
     dfs = [U.device_factors(f) for f in fs]
     xbs = [G.make_x(T, f.M, 4800 + k) for k, f in enumerate(fs)]
     ybs = [G.make_x(T, f.N, 4900 + k) for k, f in enumerate(fs)]
