@@ -866,6 +866,15 @@ int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *co
     if (e != cudaSuccess) rc = cuda_fail(e, "hostio pipeline fork");  // still joined below
     char *ws = static_cast<char *>(workspace);
     const size_t chunk_cap = size_t(std::min(L, kPipeChunk));
+    // Chunk sizes ramp up (4, 8, 16, ... calls) so that the first kernels start after a short
+    // copy-in, and down over the last 2 * kPipeChunk calls (half of what is left, at least 4) so
+    // that the last read-back is short.
+    auto cap_for = [&](int c, int l0) {
+        size_t cap = std::min(chunk_cap, size_t(4) << std::min(c, 20));
+        const int left = L - l0;
+        if (left <= 2 * kPipeChunk) cap = std::min(cap, size_t(std::max(4, left / 2)));
+        return std::max<size_t>(1, cap);
+    };
     int l0 = 0;
     for (int c = 0; l0 < L && rc == DBF_OK; ++c) {
         // the chunk: calls l0 .. l1-1 whose host x (and y) follow one another in memory, with
@@ -875,8 +884,9 @@ int dbf_matmul_hostio_batch(const dbf_factors *fs, int32_t L, const uint16_t *co
         // (both ends of a merged copy inside one allocation)
         int l1 = l0 + 1;
         uintptr_t xa = 0, xe = 0, ya = 0, ye = 0;
-        if (chunk_cap > 1 && host_allocation(x_host[l0], &xa, &xe) && host_allocation(y_host[l0], &ya, &ye)) {
-            while (l1 < L && size_t(l1 - l0) < chunk_cap && xbytes(l1 - 1) % 16 == 0 && ybytes(l1 - 1) % 16 == 0) {
+        const size_t cap = cap_for(c, l0);
+        if (cap > 1 && host_allocation(x_host[l0], &xa, &xe) && host_allocation(y_host[l0], &ya, &ye)) {
+            while (l1 < L && size_t(l1 - l0) < cap && xbytes(l1 - 1) % 16 == 0 && ybytes(l1 - 1) % 16 == 0) {
                 const uintptr_t xp = reinterpret_cast<uintptr_t>(x_host[l1]);
                 const uintptr_t yp = reinterpret_cast<uintptr_t>(y_host[l1]);
                 if (xp != reinterpret_cast<uintptr_t>(x_host[l1 - 1]) + xbytes(l1 - 1) ||

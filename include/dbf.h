@@ -219,8 +219,9 @@ int dbf_grouped_launch_count(const dbf_factors *fs, int32_t G, int64_t T);
  *   workspace       device, >= dbf_hostio_batch_workspace_bytes(fs, L, T)
  * Consecutive calls whose host buffers follow one another inside one
  * page-locked allocation (e.g. one [L][T][M] buffer sliced per call) share
- * one copy each way, up to 32 calls per copy; other calls are copied one by
- * one.  L = 0 or T = 0 is a no-op.  Host-thread safe (an internal lock); the
+ * one copy each way, up to 32 calls per copy (fewer in the first and last
+ * copies of a batch, so the pipeline fills and drains quickly); other calls
+ * are copied one by one.  L = 0 or T = 0 is a no-op.  Host-thread safe (an internal lock); the
  * pipeline streams are shared per device, so concurrent batches serialise.
  * Errors as dbf_matmul; after an error the pipeline is still joined back
  * into `stream`, and calls of the batch may or may not have run.

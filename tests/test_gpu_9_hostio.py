@@ -93,8 +93,9 @@ def test_hostio_batch_empty_and_errors(cuda_lib):
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_hostio_batch_contiguous_buffers_share_copies(cuda_lib, accumulate):
     # calls whose host buffers follow one another are moved in chunks of up to 32 with one copy each
-    # way over four device slots; 140 calls give chunks of 32, 32, 32, 32 and 12 (the fifth reuses
-    # the first slot once its read-back is done), and the shapes differ from call to call
+    # way over four device slots, the sizes ramping up at the start and down at the end: 140 calls
+    # give chunks of 4, 8, 16, 32, 32, 24, 12, 6, 4 and 2 (the fifth and later reuse slots once their
+    # read-back is done), and the shapes differ from call to call
     T = 8
     shapes = [(256, 512, 32), (512, 256, 48), (384, 384, 40)]
     fs = [G.make_factors(*shapes[k % 3], 1, 4700 + k) for k in range(140)]
