@@ -140,6 +140,11 @@ def test_one_launch_argument_errors(cuda_lib):
         cuda_lib.DBF_ERR_INVALID_ARG
     assert L.dbf_selftest_decode_one_launch(*args[:5], ws.data_ptr(), 16, bar.data_ptr(), s) == \
         cuda_lib.DBF_ERR_WORKSPACE
+    bad_acc = args[:4] + (2,) + args[5:]
+    assert L.dbf_selftest_decode_one_launch(*bad_acc, bar.data_ptr(), s) == cuda_lib.DBF_ERR_INVALID_ARG
+    # T = 0: nothing to do, not even a launch
+    assert L.dbf_selftest_decode_one_launch(ctypes.byref(df.struct), x.data_ptr(), 0, y.data_ptr(), 0, None, 0,
+                                            bar.data_ptr(), s) == cuda_lib.DBF_OK
     torch.cuda.synchronize()
     assert bar.cpu().tolist() == [0, 0, 0, 0]
     assert cuda_lib.check_status() == 0
