@@ -1193,9 +1193,33 @@ __device__ __noinline__ bool grid_barrier_bounded(unsigned int *bar, unsigned in
     return ok_s != 0;
 }
 
+// True in every CTA of the cluster when `ok` holds in all of them.  Stage 2
+// pushes partials into the other CTAs of its cluster, so after a barrier wait
+// that ran out somewhere, either the whole cluster runs stage 2 or none of it
+// does: no CTA exits while a peer may still write into its shared memory.
+// `bad` is this CTA's flag, cleared and published to the cluster (a cluster
+// barrier) at the start of the kernel; a CTA whose wait ran out sets it in
+// every CTA of the cluster, and one more cluster barrier makes the sets
+// visible before each CTA reads its own.
+__device__ __noinline__ bool cluster_all_ok(bool ok, uint32_t *bad) {
+    if (cluster_nctarank() == 1) return ok;
+    if (threadIdx.x == 0 && !ok) {
+        const uint32_t n = cluster_nctarank();
+        for (uint32_t r = 0; r < n; ++r)
+            asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa_shared(smem_u32(bad), r)), "r"(1u)
+                         : "memory");
+    }
+    cluster_sync_all();
+    return *reinterpret_cast<volatile uint32_t *>(bad) == 0u;
+}
+
 template <int CT, int RBW1, int RBW>
 __global__ void __launch_bounds__(kThreads, 2) dec_stage_pair_kernel(const __grid_constant__ PairArgs p) {
     const int bx = static_cast<int>(blockIdx.x);
+    __shared__ uint32_t bad;  // a CTA of the cluster gave up at the grid barrier
+    if (threadIdx.x == 0) bad = 0u;
+    if (cluster_nctarank() > 1)
+        cluster_sync_all();  // every CTA's flag is clear before any peer may set it
     // this CTA's stage-2 signs and scales into its stage-2 shared memory while stage 1 runs
     // (factor memory: no earlier kernel writes it); stage 1's cp.async wait covers these too
     if (bx < p.grid2) dec_stage_body<CT, RBW, 2, false, 1>(p.a2, bx, p.smem2);
@@ -1203,7 +1227,11 @@ __global__ void __launch_bounds__(kThreads, 2) dec_stage_pair_kernel(const __gri
     // CTAs past grid1 have not waited yet: the previous kernel (possibly the previous call on this
     // barrier, still counting its arrivals) must be complete before any CTA arrives
     pdl_wait();
-    if (!grid_barrier_bounded(p.bar, gridDim.x, p.a1.status)) return;
+    const bool passed = grid_barrier_bounded(p.bar, gridDim.x, p.a1.status);
+    if (!cluster_all_ok(passed, &bad)) {
+        cp_async_wait_all();  // this CTA's own stage-2 copies land before it exits
+        return;
+    }
     if (bx < p.grid2) {
         cp_async_wait_all();  // CTAs that ran no stage 1
         dec_stage_body<CT, RBW, 2, false, 2>(p.a2, bx, p.smem2);
